@@ -1,0 +1,183 @@
+/*
+ * wq.h -- C ABI of the GB300 (sm_103a) group-quantized INT4-weight GEMM
+ * library (libwq.so).
+ *
+ * The operation ("Marlin INT4 on Ada -- how it works", TinyLoop docs, section
+ * "The core mismatch: symmetric vs asymmetric"):
+ *
+ *   asymmetric weight    W[k][n]     = q[k][n] * scale[g][n] + zero[g][n]
+ *   symmetric weight     W_sym[k][n] = (q[k][n] - 8) * scale[g][n]
+ *   residual             delta[g][n] = zero[g][n] + 8 * scale[g][n]
+ *   product              Y = X @ W = X @ W_sym + A_group_sum @ delta
+ *                        A_group_sum[m][g] = sum over k in group g of X[m][k]
+ *
+ * with codes q in [0, 15], g = k / group_size, and group_size = K meaning one
+ * group per column (section "How the dispatcher chooses").  The W4A8 entry
+ * follows the HyperQwen W4A8 article (kwkr.cn): activations quantized per
+ * token to int8, weights with signed fp16 group scales folded at pack time
+ * (section "hidden mine: the negative group scale bug").
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device buffers must be device memory of the current
+ *    CUDA device; the caller allocates and owns every buffer.  The library
+ *    never allocates, frees or synchronizes (unless WQ_CHECKED=1 is set in
+ *    the environment, which adds a stream synchronize and a device-status
+ *    check after each launch).
+ *  - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *    stream.  Work is enqueued asynchronously on it.
+ *  - Return value: WQ_OK or one of the WQ_ERR_* codes below; on error no work
+ *    has been enqueued (except WQ_ERR_CUDA / WQ_ERR_TIMEOUT, which report a
+ *    failure of work already enqueued) and wq_last_error() describes it.
+ *  - Shapes: K and N multiples of 128 (the kernel tile; the same rule as the
+ *    pages' Marlin preconditions), M >= 0 (M == 0 is a no-op), group_size 128
+ *    or K (-1 is accepted as K).  Other shapes return WQ_ERR_UNSUPPORTED_SHAPE.
+ *  - Device pointers that a kernel reads with TMA or vector loads must be
+ *    16-byte aligned: X, Xq, Bpacked, Y, the workspace.  Otherwise
+ *    WQ_ERR_INVALID_ARG.
+ *  - Only sm_103 devices are supported (WQ_ERR_ARCH otherwise).
+ */
+#ifndef WQ_H_
+#define WQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define WQ_OK 0
+#define WQ_ERR_INVALID_ARG 1       /* null or misaligned pointer, bad dtype, negative size */
+#define WQ_ERR_UNSUPPORTED_SHAPE 2 /* K or N not a multiple of 128, bad group size */
+#define WQ_ERR_WORKSPACE 3         /* workspace missing or smaller than wq_workspace_size() */
+#define WQ_ERR_ARCH 4              /* current device is not sm_103 */
+#define WQ_ERR_CUDA 5              /* a CUDA runtime call or launch failed */
+#define WQ_ERR_TIMEOUT 6           /* a bounded device-side wait expired (checked mode) */
+
+/* element types */
+#define WQ_DTYPE_F16 0
+#define WQ_DTYPE_BF16 1
+#define WQ_DTYPE_F32 2
+
+/* workspace variants for wq_workspace_size */
+#define WQ_VARIANT_W4A16 0      /* wq_gemm_w4a16 with delta (asymmetric) */
+#define WQ_VARIANT_W4A16_SYM 1  /* wq_gemm_w4a16 with delta == NULL */
+#define WQ_VARIANT_W4A8 2       /* wq_gemm_w4a8 */
+
+/*
+ * Load-time pack of asymmetric W4A16 weights ("Marlin INT4 on Ada", section
+ * "The pipeline, end to end": codes packed 8 x int4 per uint32, and
+ * delta = zero + 8 * scale per group and column).
+ *   q        [K][N] uint8 device, one code 0..15 per byte (row k, column n).
+ *   scale    [G][N] fp16 device, G = K / group_size.
+ *   zero     [G][N] fp16 device.
+ *   Bpacked  [N][K/8] uint32 device, output.  Word (n, w) holds q[8w + j][n]
+ *            for j = 0..7, code j in bits [4*(j/2) + 16*(j%2), +4).
+ *   S        [G][N] fp16 device, output: a copy of scale.
+ *   delta    [G][N] fp32 device, output: fp32(zero) + 8*fp32(scale), rounded
+ *            once (exact for operands of similar magnitude).
+ * Codes outside 0..15 are reduced to their low 4 bits.
+ */
+int wq_pack_w4a16(const uint8_t* q, const void* scale, const void* zero, uint32_t* Bpacked,
+                  void* S, float* delta, int K, int N, int group_size, void* stream);
+
+/*
+ * Load-time pack of W4A8 weights with signed group scales (HyperQwen article,
+ * section "hidden mine"): for every (g, n) with scale < 0, scale -> -scale and
+ * each code v of the group -> min(16 - v, 15).  Exact except the code v = 0
+ * (value -8), which becomes +7 instead of +8.
+ *   q             [K][N] uint8 device, uint4b8 codes (value = v - 8).
+ *   scale_signed  [G][N] fp16 device.
+ *   Bpacked       [N][K/8] uint32 device, output (layout as wq_pack_w4a16).
+ *   S_abs         [G][N] fp16 device, output: the folded (non-negative) scales.
+ */
+int wq_pack_w4a8(const uint8_t* q, const void* scale_signed, uint32_t* Bpacked, void* S_abs,
+                 int K, int N, int group_size, void* stream);
+
+/* Inverse of the packing: Bpacked [N][K/8] -> q [K][N] uint8 codes. */
+int wq_unpack_w4(const uint32_t* Bpacked, uint8_t* q, int K, int N, void* stream);
+
+/*
+ * Dequantized symmetric weights, the values the GEMM feeds to the tensor
+ * cores: W[k][n] = RN((q - 8) * S[g][n]) rounded once to w_dtype
+ * (WQ_DTYPE_F16 or WQ_DTYPE_BF16).  W is [K][N] device, output.
+ */
+int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, int K, int N,
+                  int group_size, void* stream);
+
+/*
+ * W4A16 GEMM with the fused zero-point correction:
+ *   Y[m][n] = sum_k X[m][k] * W_sym[k][n] + (A_group_sum @ delta)[m][n]
+ *   X        [M][K] device, fp16 or bf16 (x_dtype), row-major.
+ *   Bpacked  [N][K/8] uint32 device (from wq_pack_w4a16).
+ *   S        [G][N] fp16 device.
+ *   delta    [G][N] fp32 device, or NULL for symmetric weights (no correction).
+ *   Y        [M][N] device, output, overwritten (y_dtype F16, BF16 or F32).
+ *   workspace / workspace_bytes: device scratch of at least
+ *            wq_workspace_size(variant, M, N, K, group_size) bytes.  Its first
+ *            4096 bytes hold split-K tile counters that must be zero before the
+ *            first call that uses this workspace; every call leaves them zero.
+ *            Calls that run concurrently must use different workspaces.
+ * Accumulation is fp32.  The weights are dequantized as RN((q-8)*scale) in
+ * the activation type; the correction is added in the same accumulator.
+ */
+int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S,
+                  const float* delta, void* Y, int y_dtype, int M, int N, int K, int group_size,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * W4A8 GEMM (symmetric, folded weights):
+ *   Y[m][n] = x_scale[m] * sum_k Xq[m][k] * (q[k][n] - 8) * S_abs[g][n]
+ *   Xq       [M][K] int8 device (per-token quantized activations).
+ *   x_scale  [M] fp32 device.
+ *   Bpacked, S_abs from wq_pack_w4a8.  Other arguments as wq_gemm_w4a16.
+ * sm_103a has no int8 tcgen05 MMA, so the int8 activations and the
+ * (q - 8) * scale weights are fed to the fp16 tensor-core path; int8 values
+ * are exact in fp16.
+ */
+int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked,
+                 const void* S_abs, void* Y, int y_dtype, int M, int N, int K, int group_size,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Per-token int8 quantization of fp16 activations (HyperQwen article, "why
+ * W4A8": activations quantized per token):
+ *   x_scale[m] = fp32_RN(max_k |x[m][k]| / 127)
+ *   Xq[m][k]   = clamp(rint(fp32_RN(x[m][k] / x_scale[m])), -127, 127)
+ * An all-zero row gives x_scale = 0 and zero codes.  Any K >= 1.
+ */
+int wq_quantize_per_token(const void* x, int8_t* Xq, float* x_scale, int M, int K, void* stream);
+
+/* Bytes of workspace the GEMM needs for this problem (0 if none). */
+size_t wq_workspace_size(int variant, int M, int N, int K, int group_size);
+
+/* 1 if `device` is an sm_103 GPU this library can run on, else 0. */
+int wq_device_supported(int device);
+
+/* Description of the last error on this thread ("" if none). */
+const char* wq_last_error(void);
+
+/* Library version string. */
+const char* wq_version(void);
+
+/*
+ * Synchronizes `stream`, then reads the device status word of the current
+ * device into *status (bit 0..3: a bounded wait in the GEMM expired, bit 4:
+ * the wait probe expired) and clears it if `reset` is nonzero.  Returns
+ * WQ_ERR_TIMEOUT if any bit was set, else WQ_OK.
+ */
+int wq_device_status(unsigned int* status, int reset, void* stream);
+
+/*
+ * Test aid: launches one thread that waits on a barrier nothing will ever
+ * complete, with a limit of limit_ns nanoseconds (<= 10 s).  The kernel gives
+ * up, sets bit 4 of the device status word and returns normally.
+ */
+int wq_debug_wait_probe(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WQ_H_ */

@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads and exports every symbol include/wq.h declares;
+host-side argument checks return their error codes before any device work.
+No GPU needed: nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import weight_only_int4_g128_gb300 as wq
+from weight_only_int4_g128_gb300 import build as wq_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "wq.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    wq_build.build()
+    return wq.load_library()
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s*(wq_\w+)\s*\(", text,
+                                 re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for must in ("wq_pack_w4a16", "wq_pack_w4a8", "wq_unpack_w4", "wq_gemm_w4a16",
+                 "wq_gemm_w4a8", "wq_workspace_size", "wq_device_supported", "wq_last_error",
+                 "wq_version"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert names
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in wq.EXPORTS, name
+    assert set(wq.EXPORTS) == set(names)
+
+
+def test_library_links_no_driver_library():
+    out = os.popen(f"ldd {wq_build.LIB}").read()
+    assert "libcuda.so" not in out
+
+
+def test_version_and_workspace_queries(lib):
+    assert b"sm_103a" in lib.wq_version()
+    # symmetric small-M decode: split-K partials only
+    a = lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 128)
+    b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 16, 4096, 4096, 128)
+    c = lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
+    assert a > b > 0 and c > b
+    assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4000, 128) == 0  # K % 128
+    assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 64) == 0   # group size
+    assert lib.wq_workspace_size(9, 16, 4096, 4096, 128) == 0
+
+
+def test_shape_and_argument_errors_before_device_work(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    # K not a multiple of 128
+    rc = lib.wq_gemm_w4a16(fake, 0, fake, fake, fake, fake, 0, 16, 256, 200, 128, fake, 1 << 20, None)
+    assert rc == 2 and b"multiples of 128" in lib.wq_last_error()
+    # N not a multiple of 128 (the vocab-size projection case, V = 50257)
+    rc = lib.wq_gemm_w4a16(fake, 0, fake, fake, fake, fake, 0, 16, 50257, 256, 128, fake, 1 << 20, None)
+    assert rc == 2
+    # group size other than 128 or K
+    rc = lib.wq_gemm_w4a16(fake, 0, fake, fake, fake, fake, 0, 16, 256, 256, 64, fake, 1 << 20, None)
+    assert rc == 2
+    # bad dtypes
+    assert lib.wq_gemm_w4a16(fake, 7, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1, None) == 1
+    assert lib.wq_gemm_w4a16(fake, 0, fake, fake, fake, fake, 9, 16, 256, 256, 128, fake, 1, None) == 1
+    # null / misaligned pointers
+    assert lib.wq_gemm_w4a16(None, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1, None) == 1
+    odd = P(0x10008)
+    assert lib.wq_gemm_w4a16(odd, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1, None) == 1
+    assert lib.wq_gemm_w4a8(None, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1, None) == 1
+    # empty problem is a no-op that succeeds
+    assert lib.wq_gemm_w4a16(None, 0, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0
+    assert lib.wq_gemm_w4a8(None, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0
+    assert lib.wq_quantize_per_token(None, None, None, 0, 64, None) == 0
+    # negative M
+    assert lib.wq_gemm_w4a16(fake, 0, fake, fake, fake, fake, 0, -1, 256, 256, 128, fake, 1, None) == 2
+    # pack shape checks
+    assert lib.wq_pack_w4a16(fake, fake, fake, fake, fake, fake, 100, 256, 128, None) == 2
+    assert lib.wq_pack_w4a8(fake, fake, fake, fake, 256, 256, 32, None) == 2
+    assert lib.wq_pack_w4a16(None, fake, fake, fake, fake, fake, 256, 256, 128, None) == 1
+    assert lib.wq_dequant_w4(fake, fake, fake, 2, 256, 256, 128, None) == 1
+    assert lib.wq_debug_wait_probe(0, None) == 1
+
+
+def test_no_device_means_an_error_not_a_fallback(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    rc = lib.wq_pack_w4a16(fake, fake, fake, fake, fake, fake, 256, 256, 128, None)
+    assert rc in (4, 5)  # WQ_ERR_ARCH or WQ_ERR_CUDA, never success
+    assert lib.wq_device_supported(0) == 0

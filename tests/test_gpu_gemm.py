@@ -1,0 +1,259 @@
+"""GPU GEMM parity against the fp64 oracle, through the C ABI.
+
+Bar (from the benchmark spec): ||Y - C_ref||_F / ||C_ref||_F <= 2e-3 for
+W4A16 (fp32 accumulate); W4A8 <= 2e-3 against the oracle over the int8
+activations and <= 5 % against the fp16-activation oracle.  Special cases whose
+result is exact (one-hot rows, integer weights, zero weights) are compared bit
+for bit, and repeated runs must be bitwise identical.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_W4A16 = 2e-3
+TOL_W4A8 = 2e-3
+TOL_W4A8_VS_F16 = 5e-2
+
+
+@pytest.fixture(scope="module")
+def wq():
+    import weight_only_int4_g128_gb300 as m
+    m.load_library(build_if_missing=True)
+    assert m.device_supported(torch.cuda.current_device())
+    return m
+
+
+def _cuda(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def _x(d):
+    if d["a_dtype"] == "bf16":
+        return _cuda(d["A"].view(np.int16)).view(torch.bfloat16)
+    return _cuda(d["A"])
+
+
+def _w4a16(wq, d, out_dtype=torch.float16, sym=False):
+    gs = d["group_size"]
+    Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), gs)
+    Y = wq.gemm_w4a16(_x(d), Bp, S, None if sym else dl, gs, out_dtype)
+    torch.cuda.synchronize()
+    return Y, (Bp, S, dl)
+
+
+def _ref_w4a16(d, sym=False, rows=None, cols=None):
+    A = oracle.activations_to_double(d["A"], d["a_dtype"])
+    if rows is not None:
+        A = A[rows]
+    sb = oracle.half_bits(d["scale"])
+    if sym:
+        return oracle.gemm_asym_identity(A, d["q"], sb, None, d["group_size"], cols=cols)
+    return oracle.gemm_asym_plain(A, d["q"], sb, oracle.half_bits(d["zero"]), d["group_size"],
+                                  cols=cols)
+
+
+SMALL = [
+    # M, K, N, group, a_dtype        (tiles of 128 columns, token tiles 16..256, ragged M)
+    (1, 256, 256, 128, "f16"),
+    (16, 256, 256, 128, "f16"),      # the K=256 shape of the small config
+    (5, 1024, 384, 128, "f16"),
+    (17, 512, 256, 128, "f16"),
+    (40, 768, 128, 128, "f16"),
+    (100, 384, 256, 128, "f16"),
+    (300, 512, 384, 128, "f16"),
+    (3, 128, 128, 128, "f16"),       # a single k-block
+    (24, 1024, 256, -1, "f16"),      # one group per column
+    (9, 640, 256, 128, "bf16"),
+    (200, 1280, 256, 128, "bf16"),
+    (64, 2048, 256, -1, "bf16"),
+]
+
+
+@pytest.mark.parametrize("M,K,N,gs,adt", SMALL)
+def test_w4a16_small_parity(wq, M, K, N, gs, adt):
+    d = synth.make_inputs(1000 + M * 7 + K, M, K, N, group_size=gs, a_dtype=adt)
+    Y, _ = _w4a16(wq, d)
+    ref = _ref_w4a16(d)
+    err = oracle.rel_fro(Y.double().cpu().numpy(), ref)
+    assert err <= TOL_W4A16, err
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_w4a16_output_dtypes(wq, out_dtype):
+    d = synth.make_inputs(77, 33, 512, 256)
+    Y, _ = _w4a16(wq, d, out_dtype)
+    assert Y.dtype == out_dtype
+    err = oracle.rel_fro(Y.double().cpu().numpy(), _ref_w4a16(d))
+    assert err <= (TOL_W4A16 if out_dtype != torch.float32 else 1e-3), err
+
+
+@pytest.mark.parametrize("M", [4, 130])
+def test_w4a16_symmetric_parity(wq, M):
+    d = synth.make_inputs(88 + M, M, 512, 256)
+    Y, _ = _w4a16(wq, d, torch.float32, sym=True)
+    err = oracle.rel_fro(Y.double().cpu().numpy(), _ref_w4a16(d, sym=True))
+    assert err <= 1e-3, err
+
+
+@pytest.mark.parametrize("adt", ["f16", "bf16"])
+@pytest.mark.parametrize("K", [128, 256, 1024])
+def test_one_hot_rows_give_dequantized_weights_bit_exact(wq, adt, K):
+    """X = I_K (one-hot rows): Y[k, :] is the dequantized row k, bit for bit."""
+    N = 256
+    d = synth.make_inputs(500 + K, K, K, N, a_dtype=adt)
+    eye = np.eye(K, dtype=np.float32)
+    if adt == "bf16":
+        d["A"] = (eye.view(np.uint32) >> 16).astype(np.uint16)
+        out, fn = torch.bfloat16, oracle.dequant_sym_bf16
+    else:
+        d["A"] = eye.astype(np.float16)
+        out, fn = torch.float16, oracle.dequant_sym_f16
+    Y, _ = _w4a16(wq, d, out, sym=True)
+    got = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+    want = fn(d["q"], oracle.half_bits(d["scale"]), 128)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,K", [(8, 512), (70, 1024), (257, 256)])
+def test_integer_weights_exact(wq, M, K):
+    """scale = 1, zero = -8 (so delta = 0): C = X @ (q - 8) is an exact integer matmul."""
+    N = 256
+    rng = np.random.Generator(np.random.PCG64(M))
+    d = synth.make_inputs(600 + M, M, K, N)
+    d["A"] = rng.integers(-3, 4, (M, K)).astype(np.float16)
+    d["scale"] = np.ones_like(d["scale"])
+    d["zero"] = np.full_like(d["zero"], -8.0)
+    Y, _ = _w4a16(wq, d, torch.float32)
+    want = d["A"].astype(np.int64) @ (d["q"].astype(np.int64) - 8)
+    assert np.array_equal(Y.cpu().numpy().astype(np.int64), want)
+    assert np.array_equal(Y.cpu().numpy(), want.astype(np.float32))
+
+
+def test_zero_weights_give_exact_zero(wq):
+    """q == 8 and zero = -8*scale: W == 0, delta == 0, so Y == 0 exactly."""
+    d = synth.make_inputs(700, 33, 512, 256)
+    d["q"] = np.full_like(d["q"], 8)
+    d["zero"] = (-8.0 * d["scale"].astype(np.float64)).astype(np.float16)
+    Y, _ = _w4a16(wq, d, torch.float32)
+    assert torch.count_nonzero(Y).item() == 0
+
+
+def test_correction_term_matters(wq):
+    """Dropping delta changes the result by exactly the A_group_sum @ delta term."""
+    d = synth.make_inputs(701, 16, 1024, 256)
+    Ya, (Bp, S, dl) = _w4a16(wq, d, torch.float32)
+    Ys = wq.gemm_w4a16(_x(d), Bp, S, None, 128, torch.float32)
+    A = oracle.activations_to_double(d["A"], "f16")
+    corr = oracle.group_sum(A, 128) @ dl.cpu().double().numpy()
+    err = oracle.rel_fro((Ya - Ys).double().cpu().numpy(), corr)
+    assert err < 1e-4, err
+
+
+@pytest.mark.parametrize("M", [1, 16, 100])
+def test_repeat_runs_bitwise_identical(wq, M):
+    d = synth.make_inputs(800 + M, M, 4096, 512)
+    Y1, (Bp, S, dl) = _w4a16(wq, d)
+    X = _x(d)
+    for _ in range(3):
+        Y2 = wq.gemm_w4a16(X, Bp, S, dl, 128)
+        assert torch.equal(Y1, Y2)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 256, 256), (16, 512, 384), (100, 1024, 256),
+                                   (300, 256, 128)])
+def test_w4a8_parity(wq, M, K, N):
+    d = synth.make_inputs(900 + M, M, K, N, mode="w4a8")
+    gXq, gxs = wq.quantize_per_token(_cuda(d["A"]))
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    assert np.array_equal(gXq.cpu().numpy(), Xq) and np.array_equal(gxs.cpu().numpy(), xs)
+    Bp, S = wq.pack_w4a8(_cuda(d["q"]), _cuda(d["scale"]), 128)
+    Y = wq.gemm_w4a8(gXq, gxs, Bp, S, 128, torch.float32)
+    torch.cuda.synchronize()
+    qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), 128)
+    ref8 = oracle.gemm_w4a8(Xq, xs, qf, sf, 128)
+    y = Y.double().cpu().numpy()
+    assert oracle.rel_fro(y, ref8) <= TOL_W4A8
+    ref16 = oracle.gemm_asym_identity(oracle.activations_to_double(d["A"], "f16"), qf, sf, None, 128)
+    assert oracle.rel_fro(y, ref16) <= TOL_W4A8_VS_F16
+
+
+def test_w4a8_gpu_quantizer_end_to_end(wq):
+    d = synth.make_inputs(950, 24, 1024, 256, mode="w4a8")
+    Xq, xs = wq.quantize_per_token(_cuda(d["A"]))
+    Bp, S = wq.pack_w4a8(_cuda(d["q"]), _cuda(d["scale"]), 128)
+    Y = wq.gemm_w4a8(Xq, xs, Bp, S, 128)
+    oXq, oxs = oracle.quantize_per_token(d["A"])
+    qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), 128)
+    ref8 = oracle.gemm_w4a8(oXq, oxs, qf, sf, 128)
+    assert oracle.rel_fro(Y.double().cpu().numpy(), ref8) <= TOL_W4A8
+
+
+def test_empty_and_error_paths(wq):
+    d = synth.make_inputs(960, 4, 256, 256)
+    Y, (Bp, S, dl) = _w4a16(wq, d)
+    X0 = torch.empty((0, 256), dtype=torch.float16, device="cuda")
+    assert wq.gemm_w4a16(X0, Bp, S, dl, 128).shape == (0, 256)
+    small = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(wq.WQError) as e:
+        wq.gemm_w4a16(_x(d), Bp, S, dl, 128, workspace=small)
+    assert e.value.code == 3
+
+
+def test_bounded_wait_expires_and_context_survives(wq):
+    """A wait nothing will complete gives up after its limit and reports it; the
+    context stays usable afterwards."""
+    wq.device_status(reset=True)
+    wq.debug_wait_probe(50_000_000)  # 50 ms
+    st = wq.device_status(reset=True)
+    assert st & (1 << 4)
+    d = synth.make_inputs(970, 16, 256, 256)
+    Y, _ = _w4a16(wq, d)
+    assert oracle.rel_fro(Y.double().cpu().numpy(), _ref_w4a16(d)) <= TOL_W4A16
+    assert wq.device_status(reset=True) == 0
+
+
+# ---------------------------------------------------------------- full-size configs, sampled
+def _sample_cols(N, width=48):
+    return [(0, width), (N // 2 - 64, N // 2 - 64 + width), (N - width, N)]
+
+
+def _sample_rows(M, count=48):
+    if M <= count:
+        return np.arange(M)
+    return np.unique(np.linspace(0, M - 1, count).astype(np.int64))
+
+
+FULL = [(w, i) for w in ("c0", "c1", "c2", "c3", "c4") for i in range(len(synth.shapes(w)))]
+
+
+@pytest.mark.parametrize("workload,idx", FULL)
+def test_full_size_workloads_sampled(wq, workload, idx):
+    seed, s = synth.shapes(workload)[idx]
+    d = synth.make_inputs(seed, **s)
+    rows = _sample_rows(s["M"])
+    gs = s["group_size"]
+    if s["mode"] == "w4a8":
+        Xq, xs = wq.quantize_per_token(_cuda(d["A"]))
+        Bp, S = wq.pack_w4a8(_cuda(d["q"]), _cuda(d["scale"]), gs)
+        Y = wq.gemm_w4a8(Xq, xs, Bp, S, gs)
+        torch.cuda.synchronize()
+        Xq_h, xs_h = Xq.cpu().numpy(), xs.cpu().numpy()
+        oXq, oxs = oracle.quantize_per_token(d["A"][rows])
+        assert np.array_equal(Xq_h[rows], oXq) and np.array_equal(xs_h[rows], oxs)
+        qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), gs)
+        for c in _sample_cols(s["N"]):
+            ref8 = oracle.gemm_w4a8(oXq, oxs, qf, sf, gs, cols=c)
+            got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
+            assert oracle.rel_fro(got, ref8) <= TOL_W4A8
+    else:
+        Y, _ = _w4a16(wq, d)
+        for c in _sample_cols(s["N"]):
+            ref = _ref_w4a16(d, rows=rows, cols=c)
+            got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
+            err = oracle.rel_fro(got, ref)
+            assert err <= TOL_W4A16, (c, err)

@@ -1,0 +1,267 @@
+"""Python binding of libwq.so, the GB300 (sm_103a) group-quantized INT4-weight GEMM.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/wq.h.  PyTorch supplies device
+memory and the current stream.  There is no CPU or PyTorch fallback: if the
+library is not built, or the device is not sm_103, calls raise.
+
+    Bpacked, S, delta = pack_w4a16(q, scale, zero, group_size)
+    Y = gemm_w4a16(X, Bpacked, S, delta, group_size)       # X fp16 or bf16 [M, K]
+    Bpacked, S_abs = pack_w4a8(q, scale_signed, group_size)
+    Xq, x_scale = quantize_per_token(x)
+    Y = gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = [
+    "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
+    "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a8", "workspace_size",
+    "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
+    "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
+    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8",
+]
+
+DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
+VARIANT_W4A16, VARIANT_W4A16_SYM, VARIANT_W4A8 = 0, 1, 2
+ERRORS = {1: "WQ_ERR_INVALID_ARG", 2: "WQ_ERR_UNSUPPORTED_SHAPE", 3: "WQ_ERR_WORKSPACE",
+          4: "WQ_ERR_ARCH", 5: "WQ_ERR_CUDA", 6: "WQ_ERR_TIMEOUT"}
+
+_P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+# name -> (restype, argtypes); one entry per function declared in include/wq.h
+EXPORTS = {
+    "wq_pack_w4a16": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "wq_pack_w4a8": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
+    "wq_unpack_w4": (_I, [_P, _P, _I, _I, _P]),
+    "wq_dequant_w4": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
+    "wq_gemm_w4a16": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_gemm_w4a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_quantize_per_token": (_I, [_P, _P, _P, _I, _I, _P]),
+    "wq_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "wq_device_supported": (_I, [_I]),
+    "wq_last_error": (ctypes.c_char_p, []),
+    "wq_version": (ctypes.c_char_p, []),
+    "wq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint), _I, _P]),
+    "wq_debug_wait_probe": (_I, [ctypes.c_ulonglong, _P]),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class WQError(RuntimeError):
+    def __init__(self, code: int, where: str, msg: str):
+        super().__init__(f"{where}: {ERRORS.get(code, code)}: {msg}")
+        self.code = code
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libwq.so.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if build_if_missing and _build.is_stale():
+                _build.build()
+            if not os.path.exists(_build.LIB):
+                raise RuntimeError(
+                    "libwq.so is not built: run `python -m weight_only_int4_g128_gb300.build` "
+                    "(there is no CPU fallback)")
+            lib = ctypes.CDLL(_build.LIB)
+            for name, (res, args) in EXPORTS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise WQError(rc, where, load_library().wq_last_error().decode())
+
+
+def _stream(t=None):
+    torch = _torch()
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else None
+
+
+def _dtype_code(dt) -> int:
+    torch = _torch()
+    return {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}[dt]
+
+
+def _gs(K: int, group_size: int) -> int:
+    return K if group_size in (-1, K) else group_size
+
+
+def _require_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# -- packing -------------------------------------------------------------------------
+
+def pack_w4a16(q, scale, zero, group_size: int = 128):
+    """q [K,N] uint8 codes, scale/zero [G,N] fp16 -> (Bpacked [N,K/8] int32, S, delta fp32)."""
+    torch = _torch()
+    _require_cuda(q, scale, zero)
+    K, N = q.shape
+    G = K // _gs(K, group_size)
+    Bp = torch.empty((N, K // 8), dtype=torch.int32, device=q.device)
+    S = torch.empty((G, N), dtype=torch.float16, device=q.device)
+    d = torch.empty((G, N), dtype=torch.float32, device=q.device)
+    _check(load_library().wq_pack_w4a16(_ptr(q), _ptr(scale), _ptr(zero), _ptr(Bp), _ptr(S),
+                                        _ptr(d), K, N, group_size, _stream()), "wq_pack_w4a16")
+    return Bp, S, d
+
+
+def pack_w4a8(q, scale_signed, group_size: int = 128):
+    """q [K,N] uint4b8 codes, signed scale [G,N] fp16 -> (Bpacked, S_abs) with the sign fold."""
+    torch = _torch()
+    _require_cuda(q, scale_signed)
+    K, N = q.shape
+    G = K // _gs(K, group_size)
+    Bp = torch.empty((N, K // 8), dtype=torch.int32, device=q.device)
+    S = torch.empty((G, N), dtype=torch.float16, device=q.device)
+    _check(load_library().wq_pack_w4a8(_ptr(q), _ptr(scale_signed), _ptr(Bp), _ptr(S), K, N,
+                                       group_size, _stream()), "wq_pack_w4a8")
+    return Bp, S
+
+
+def unpack_w4(Bpacked, K: int, N: int):
+    torch = _torch()
+    _require_cuda(Bpacked)
+    q = torch.empty((K, N), dtype=torch.uint8, device=Bpacked.device)
+    _check(load_library().wq_unpack_w4(_ptr(Bpacked), _ptr(q), K, N, _stream()), "wq_unpack_w4")
+    return q
+
+
+def dequant_w4(Bpacked, S, K: int, N: int, group_size: int = 128, dtype=None):
+    torch = _torch()
+    dtype = dtype or torch.float16
+    _require_cuda(Bpacked, S)
+    W = torch.empty((K, N), dtype=dtype, device=Bpacked.device)
+    _check(load_library().wq_dequant_w4(_ptr(Bpacked), _ptr(S), _ptr(W), _dtype_code(dtype), K, N,
+                                        group_size, _stream()), "wq_dequant_w4")
+    return W
+
+
+def quantize_per_token(x):
+    torch = _torch()
+    _require_cuda(x)
+    M, K = x.shape
+    Xq = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    xs = torch.empty((M,), dtype=torch.float32, device=x.device)
+    _check(load_library().wq_quantize_per_token(_ptr(x), _ptr(Xq), _ptr(xs), M, K, _stream()),
+           "wq_quantize_per_token")
+    return Xq, xs
+
+
+# -- workspace -------------------------------------------------------------------------
+
+def workspace_size(variant: int, M: int, N: int, K: int, group_size: int) -> int:
+    return int(load_library().wq_workspace_size(variant, M, N, K, group_size))
+
+
+class Workspace:
+    """Zero-initialised device scratch for one stream, grown on demand (torch-allocated)."""
+
+    def __init__(self, device=None):
+        self.device = device
+        self.buf = None
+
+    def get(self, nbytes: int):
+        torch = _torch()
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=self.device)
+        return self.buf
+
+
+_ws = {}
+
+
+def _workspace(device, nbytes):
+    torch = _torch()
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _ws.get(key)
+    if ws is None:
+        ws = _ws[key] = Workspace(device)
+    return ws.get(nbytes)
+
+
+# -- GEMMs -----------------------------------------------------------------------------
+
+def gemm_w4a16(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=None,
+               workspace=None):
+    """Y = X @ W_sym + A_group_sum @ delta  (delta None: symmetric).  X [M,K] fp16/bf16."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.float16
+    _require_cuda(X, Bpacked, S, delta, out)
+    M, K = X.shape
+    N = Bpacked.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=X.device)
+    variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
+    need = workspace_size(variant, M, N, K, group_size) if M > 0 else 0
+    ws = workspace if workspace is not None else (_workspace(X.device, need) if need else None)
+    _check(load_library().wq_gemm_w4a16(
+        _ptr(X), _dtype_code(X.dtype), _ptr(Bpacked), _ptr(S), _ptr(delta), _ptr(Y),
+        _dtype_code(Y.dtype), M, N, K, group_size, _ptr(ws),
+        ws.numel() if ws is not None else 0, _stream()), "wq_gemm_w4a16")
+    return Y
+
+
+def gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size: int = 128, out_dtype=None, out=None,
+              workspace=None):
+    """Y = x_scale[m] * Xq @ W_sym  (folded weights).  Xq [M,K] int8."""
+    torch = _torch()
+    out_dtype = out_dtype or torch.float16
+    _require_cuda(Xq, x_scale, Bpacked, S_abs, out)
+    M, K = Xq.shape
+    N = Bpacked.shape[0]
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=Xq.device)
+    need = workspace_size(VARIANT_W4A8, M, N, K, group_size) if M > 0 else 0
+    ws = workspace if workspace is not None else (_workspace(Xq.device, need) if need else None)
+    _check(load_library().wq_gemm_w4a8(
+        _ptr(Xq), _ptr(x_scale), _ptr(Bpacked), _ptr(S_abs), _ptr(Y), _dtype_code(Y.dtype),
+        M, N, K, group_size, _ptr(ws), ws.numel() if ws is not None else 0, _stream()),
+        "wq_gemm_w4a8")
+    return Y
+
+
+# -- device queries ------------------------------------------------------------------------
+
+def device_supported(device: int = 0) -> bool:
+    return bool(load_library().wq_device_supported(device))
+
+
+def device_status(reset: bool = True) -> int:
+    st = ctypes.c_uint(0)
+    load_library().wq_device_status(ctypes.byref(st), 1 if reset else 0, _stream())
+    return int(st.value)
+
+
+def debug_wait_probe(limit_ns: int):
+    _check(load_library().wq_debug_wait_probe(limit_ns, _stream()), "wq_debug_wait_probe")
+
+
+def version() -> str:
+    return load_library().wq_version().decode()

@@ -1,0 +1,406 @@
+// wq_api.cu -- the extern "C" entry points of libwq.so: argument checks,
+// shape heuristics, TMA tensor maps, workspace carving and launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "wq.h"
+#include "wq_internal.h"
+
+namespace {
+
+thread_local char t_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(WQ_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_device() {
+  static int cache[64];  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev >= 0 && dev < 64 && cache[dev] == 1) return WQ_OK;
+  if (!wq_device_supported(dev)) {
+    if (dev >= 0 && dev < 64) cache[dev] = 2;
+    return fail(WQ_ERR_ARCH, "device %d is not an sm_103 GPU", dev);
+  }
+  if (dev >= 0 && dev < 64) cache[dev] = 1;
+  return WQ_OK;
+}
+
+bool checked_mode() {
+  static int v = -1;
+  if (v < 0) {
+    const char* s = getenv("WQ_CHECKED");
+    v = (s && s[0] && s[0] != '0') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+unsigned long long timeout_ns() {
+  static unsigned long long v = 0;
+  if (v == 0) {
+    const char* s = getenv("WQ_WAIT_LIMIT_MS");
+    long long ms = s ? atoll(s) : 2000;
+    if (ms <= 0 || ms > 10000) ms = 2000;
+    v = static_cast<unsigned long long>(ms) * 1000000ull;
+  }
+  return v;
+}
+
+int after_launch(cudaError_t e, const char* where, cudaStream_t st) {
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  if (checked_mode()) {
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, where);
+    unsigned int status = 0;
+    e = wq::read_status(&status);
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (status) return fail(WQ_ERR_TIMEOUT, "%s: bounded device wait expired (status 0x%x)", where, status);
+  }
+  return WQ_OK;
+}
+
+int norm_group(int K, int group_size, int* gs_out) {
+  int gs = (group_size == -1) ? K : group_size;
+  if (gs != 128 && gs != K)
+    return fail(WQ_ERR_UNSUPPORTED_SHAPE, "group_size %d: only 128 or K (-1) are supported", group_size);
+  if (gs <= 0 || K % gs != 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "K %% group_size != 0");
+  *gs_out = gs;
+  return WQ_OK;
+}
+
+int check_kn(int K, int N) {
+  if (K <= 0 || N <= 0 || K % 128 != 0 || N % 128 != 0)
+    return fail(WQ_ERR_UNSUPPORTED_SHAPE, "K=%d N=%d: both must be positive multiples of 128", K, N);
+  return WQ_OK;
+}
+
+// ---------------------------------------------------------------- tensor maps
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                              CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                              CUtensorMapFloatOOBfill);
+
+EncodeFn get_encode() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [rows][cols] of `esize`-byte elements; box [box_rows][box_cols].
+int make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* ptr, uint64_t rows,
+             uint64_t cols, uint32_t box_rows, uint32_t box_cols, CUtensorMapSwizzle sw) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * esize};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return WQ_OK;
+}
+
+// ---------------------------------------------------------------- heuristics
+struct Plan {
+  int bt;
+  int splits;
+  int kb_per_split;
+  int kaug;       // 0 without correction
+  size_t off_aug, off_x16, off_part;  // byte offsets into the workspace
+  size_t bytes;
+};
+
+constexpr size_t kCounterBytes = 4096;  // split-K tile counters at the start of the workspace
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+Plan make_plan(int variant, int M, int N, int K, int gs) {
+  Plan p{};
+  p.bt = (M <= 16) ? 16 : (M <= 32) ? 32 : (M <= 64) ? 64 : (M <= 128) ? 128 : 256;
+  const int G = K / gs;
+  const int kb = K / 128;
+  const int ntiles = N / 128;
+  const int mtiles = (M + p.bt - 1) / p.bt;
+  const int tiles = ntiles * mtiles;
+  const int slots = (p.bt <= 32) ? 2 * wq::kNumSMs : wq::kNumSMs;
+  int splits = 1;
+  if (tiles < slots) {
+    splits = (slots + tiles - 1) / tiles;
+    if (splits > kb) splits = kb;
+    if (tiles * 1 > static_cast<int>(kCounterBytes / 4)) splits = 1;
+  }
+  p.kb_per_split = (kb + splits - 1) / splits;
+  p.splits = (kb + p.kb_per_split - 1) / p.kb_per_split;
+  p.kaug = (variant == WQ_VARIANT_W4A16) ? ((3 * G + 127) / 128) * 128 : 0;
+  size_t off = kCounterBytes;
+  p.off_aug = off;
+  if (p.kaug) off = align256(off + static_cast<size_t>(M) * p.kaug * 2);
+  p.off_x16 = off;
+  if (variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(M) * K * 2);
+  p.off_part = off;
+  if (p.splits > 1) off = align256(off + static_cast<size_t>(p.splits) * M * N * 4);
+  p.bytes = off;
+  return p;
+}
+
+// ---------------------------------------------------------------- GEMM core
+int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S, const float* delta,
+              const float* x_scale, void* Y, int y_kind, int M, int N, int K, int gs, int variant,
+              void* ws, size_t ws_bytes, cudaStream_t st, const char* name) {
+  const Plan plan = make_plan(variant, M, N, K, gs);
+  if (!ws || ws_bytes < plan.bytes)
+    return fail(WQ_ERR_WORKSPACE, "%s: workspace of %zu bytes given, %zu needed", name, ws_bytes, plan.bytes);
+  if (!aligned16(ws)) return fail(WQ_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const int G = K / gs;
+  cudaError_t e;
+
+  const void* xg = X;
+  if (variant == WQ_VARIANT_W4A8) {
+    __half* x16 = reinterpret_cast<__half*>(wsb + plan.off_x16);
+    e = wq::launch_i8_to_f16(static_cast<const int8_t*>(X), x16, static_cast<long long>(M) * K, st);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 -> fp16 pre-pass");
+    xg = x16;
+  }
+  __nv_bfloat16* aug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_aug);
+  if (plan.kaug) {
+    e = wq::launch_aug_prep(X, x_kind, M, K, gs, G, plan.kaug, aug, st);
+    if (e != cudaSuccess) return cuda_fail(e, "group-sum pre-pass");
+  }
+
+  CUtensorMap tm_x, tm_w, tm_aug;
+  int rc = make_map(&tm_x, x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    2, xg, M, K, plan.bt, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc) return rc;
+  rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Bpacked, N, K / 8, 128, 16,
+                CU_TENSOR_MAP_SWIZZLE_64B);
+  if (rc) return rc;
+  if (plan.kaug) {
+    rc = make_map(&tm_aug, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aug, M, plan.kaug, plan.bt, 64,
+                  CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc) return rc;
+  } else {
+    tm_aug = tm_x;  // unused
+  }
+
+  wq::GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.group_size = gs;
+  p.G = G;
+  p.kb_total = K / 128;
+  p.kb_per_split = plan.kb_per_split;
+  p.splits = plan.splits;
+  p.aug_stages = plan.kaug / 128;
+  p.kaug = plan.kaug;
+  p.S = static_cast<const __half*>(S);
+  p.delta = plan.kaug ? delta : nullptr;
+  p.x_scale = x_scale;
+  p.Y = Y;
+  p.y_kind = y_kind;
+  p.partials = reinterpret_cast<float*>(wsb + plan.off_part);
+  p.counters = reinterpret_cast<int*>(wsb);
+  p.timeout_ns = timeout_ns();
+  e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_w, tm_aug, p, st);
+  return after_launch(e, name, st);
+}
+
+int y_kind_of(int y_dtype) {
+  switch (y_dtype) {
+    case WQ_DTYPE_F16: return wq::kYF16;
+    case WQ_DTYPE_BF16: return wq::kYBF16;
+    case WQ_DTYPE_F32: return wq::kYF32;
+    default: return -1;
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int wq_device_supported(int device) {
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return (major == 10 && minor == 3) ? 1 : 0;
+}
+
+const char* wq_last_error(void) { return t_err; }
+
+const char* wq_version(void) { return "wq 0.1.0 (sm_103a, tcgen05)"; }
+
+size_t wq_workspace_size(int variant, int M, int N, int K, int group_size) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
+  int gs = (group_size == -1) ? K : group_size;
+  if (gs != 128 && gs != K) return 0;
+  if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8) return 0;
+  return make_plan(variant, M, N, K, gs).bytes;
+}
+
+int wq_pack_w4a16(const uint8_t* q, const void* scale, const void* zero, uint32_t* Bpacked, void* S,
+                  float* delta, int K, int N, int group_size, void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (!q || !scale || !zero || !Bpacked || !S || !delta)
+    return fail(WQ_ERR_INVALID_ARG, "wq_pack_w4a16: null pointer");
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wq::launch_pack(q, static_cast<const __half*>(scale), static_cast<const __half*>(zero), 0,
+                                  Bpacked, static_cast<__half*>(S), delta, K, N, gs, st);
+  return after_launch(e, "wq_pack_w4a16", st);
+}
+
+int wq_pack_w4a8(const uint8_t* q, const void* scale_signed, uint32_t* Bpacked, void* S_abs, int K, int N,
+                 int group_size, void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (!q || !scale_signed || !Bpacked || !S_abs) return fail(WQ_ERR_INVALID_ARG, "wq_pack_w4a8: null pointer");
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wq::launch_pack(q, static_cast<const __half*>(scale_signed), nullptr, 1, Bpacked,
+                                  static_cast<__half*>(S_abs), nullptr, K, N, gs, st);
+  return after_launch(e, "wq_pack_w4a8", st);
+}
+
+int wq_unpack_w4(const uint32_t* Bpacked, uint8_t* q, int K, int N, void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  if (!Bpacked || !q) return fail(WQ_ERR_INVALID_ARG, "wq_unpack_w4: null pointer");
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return after_launch(wq::launch_unpack(Bpacked, q, K, N, st), "wq_unpack_w4", st);
+}
+
+int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, int K, int N, int group_size,
+                  void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (!Bpacked || !S || !W) return fail(WQ_ERR_INVALID_ARG, "wq_dequant_w4: null pointer");
+  if (w_dtype != WQ_DTYPE_F16 && w_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "wq_dequant_w4: w_dtype must be F16 or BF16");
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return after_launch(wq::launch_dequant(Bpacked, static_cast<const __half*>(S), W,
+                                         w_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16, K, N, gs, st),
+                      "wq_dequant_w4", st);
+}
+
+int wq_quantize_per_token(const void* x, int8_t* Xq, float* x_scale, int M, int K, void* stream) {
+  if (M < 0 || K <= 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_quantize_per_token: M=%d K=%d", M, K);
+  if (M == 0) return WQ_OK;
+  if (!x || !Xq || !x_scale) return fail(WQ_ERR_INVALID_ARG, "wq_quantize_per_token: null pointer");
+  int rc = check_device();
+  if (rc) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return after_launch(wq::launch_quantize_per_token(static_cast<const __half*>(x), Xq, x_scale, M, K, st),
+                      "wq_quantize_per_token", st);
+}
+
+int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                  void* Y, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a16: M=%d", M);
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (x_dtype != WQ_DTYPE_F16 && x_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: x_dtype must be F16 or BF16");
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!X || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: null pointer");
+  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: X, Bpacked and Y must be 16-byte aligned");
+  if ((rc = check_device())) return rc;
+  const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
+  return gemm_core(X, x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16, Bpacked, S, delta, nullptr, Y, yk, M, N,
+                   K, gs, variant, workspace, workspace_bytes, static_cast<cudaStream_t>(stream),
+                   "wq_gemm_w4a16");
+}
+
+int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S_abs, void* Y,
+                 int y_dtype, int M, int N, int K, int group_size, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a8: M=%d", M);
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!Xq || !x_scale || !Bpacked || !S_abs || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: null pointer");
+  if (!aligned16(Xq) || !aligned16(Bpacked) || !aligned16(Y))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: Xq, Bpacked and Y must be 16-byte aligned");
+  if ((rc = check_device())) return rc;
+  return gemm_core(Xq, wq::kXF16, Bpacked, S_abs, nullptr, x_scale, Y, yk, M, N, K, gs, WQ_VARIANT_W4A8,
+                   workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "wq_gemm_w4a8");
+}
+
+int wq_device_status(unsigned int* status, int reset, void* stream) {
+  if (!status) return fail(WQ_ERR_INVALID_ARG, "wq_device_status: null pointer");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_device_status");
+  e = wq::read_status(status);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_device_status");
+  if (reset) {
+    e = wq::clear_status();
+    if (e != cudaSuccess) return cuda_fail(e, "wq_device_status");
+  }
+  return *status ? fail(WQ_ERR_TIMEOUT, "device status 0x%x", *status) : WQ_OK;
+}
+
+int wq_debug_wait_probe(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 10000000000ull)
+    return fail(WQ_ERR_INVALID_ARG, "wq_debug_wait_probe: limit must be in (0, 10 s]");
+  int rc = check_device();
+  if (rc) return rc;
+  cudaError_t e = wq::launch_wait_probe(limit_ns, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "wq_debug_wait_probe");
+  return WQ_OK;
+}
+
+}  // extern "C"

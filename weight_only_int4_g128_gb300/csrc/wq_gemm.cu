@@ -1,0 +1,448 @@
+// wq_gemm.cu -- the tcgen05 W4A16 / W4A8 GEMM for sm_103a.
+//
+// What it computes (from "Marlin INT4 on Ada -- how it works", section "The
+// core mismatch: symmetric vs asymmetric"):
+//   Y[m][n] = sum_k X[m][k] * W_sym[k][n] + sum_g a_sum[m][g] * delta[g][n]
+//   W_sym[k][n] = (q[k][n] - 8) * scale[g][n],  a_sum[m][g] = sum_{k in g} X[m][k]
+// The second term is the zero-point correction; it is accumulated into the
+// same TMEM accumulator as extra "K" steps (see below), so there is no
+// second pass over Y.  For W4A8 (HyperQwen article, "hidden mine") the int8
+// activations arrive converted to fp16, delta is absent and the accumulator
+// is multiplied by the per-token scale in the epilogue.
+//
+// Tiling (swap-AB): one CTA owns 128 output columns n (the MMA's M = 128,
+// i.e. 128 TMEM lanes, one weight row per lane) and BT tokens (the MMA's N).
+//   warp 0      TMA producer: activation tile [BT x 128 k] (two 128-byte
+//               swizzled boxes) and the packed weight tile [128 n x 16 words]
+//               (64-byte swizzle) into a shared-memory ring.
+//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM,
+//               B = activations from shared memory) and tcgen05.commit.
+//   warps 2..5  dequant: each thread owns one weight row, turns 128 codes into
+//               128 scaled fp16/bf16 values in registers and stores them into
+//               a TMEM A-stage with tcgen05.st (the weights never pass through
+//               shared memory once dequantized); then the epilogue.
+// Correction as K-augmentation: a_sum (fp32, computed once by a pre-pass) is
+// split into bf16 hi/lo and laid out as extra activation columns
+// [a_hi | a_lo | a_hi]; the dequant warps write the matching weight-side
+// columns [d_hi | d_hi | d_lo] (delta split the same way).  Their bf16 MMAs add
+// a_hi*d_hi + a_lo*d_hi + a_hi*d_lo, which is a_sum*delta up to ~2^-16
+// relative.
+// Split-K: gridDim.z segments of k-blocks; each writes an fp32 partial and
+// the last CTA to arrive on a per-tile counter sums the partials in segment
+// order (deterministic) and writes Y.
+//
+// Every wait is bounded; on expiry the CTA records a status bit, drains what
+// it issued, frees its TMEM and returns.
+#include "wq_device.cuh"
+
+namespace wq {
+
+// Device status word: bounded waits that expire OR a code into it.
+static __device__ unsigned int g_status = 0;
+
+template <int BT>
+struct Cfg {
+  static constexpr int kXStageBytes = BT * kKBlock * 2;              // two SW128 atoms
+  static constexpr int kXAtomBytes = BT * 128;                        // one box of 64 k
+  static constexpr int kWStageBytes = kTileN * kWordsPerKBlock * 4;  // 8 KB
+  static constexpr int kNSX = (BT >= 256) ? 3 : (BT >= 128) ? 5 : (BT >= 64) ? 8 : (BT >= 32) ? 6 : 8;
+  static constexpr int kNSA = (BT <= 32) ? 3 : 4;                     // TMEM A-stages (64 cols each)
+  static constexpr int kDCol = (BT <= 32) ? 192 : 256;                // accumulator columns
+  static constexpr int kTmemCols = (BT <= 32) ? 256 : 512;
+  static constexpr int kNumBars = 2 * kNSX + 2 * kNSA + 1;
+  static constexpr int kSmemBytes =
+      1024 /*align slack*/ + kNSX * (kXStageBytes + kWStageBytes) + kNumBars * 8 + 16;
+  static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N for M=128 is 16..256, step 16");
+  static_assert(kDCol + BT <= kTmemCols, "TMEM budget");
+  static_assert(kNSA * 64 <= kDCol, "TMEM budget");
+};
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// All lanes wait; the warp proceeds only if every lane saw the phase complete,
+// so the .sync.aligned tcgen05 ops that follow stay warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const WaitCtx& w) {
+  const bool ok = mbar_wait(bar, parity, w);
+  return __all_sync(0xffffffffu, ok);
+}
+
+template <int YK>
+__device__ __forceinline__ void store_y(void* Y, size_t idx, float v) {
+  if (YK == kYF16) {
+    reinterpret_cast<__half*>(Y)[idx] = __float2half_rn(v);
+  } else if (YK == kYBF16) {
+    reinterpret_cast<__nv_bfloat16*>(Y)[idx] = __float2bfloat16_rn(v);
+  } else {
+    reinterpret_cast<float*>(Y)[idx] = v;
+  }
+}
+
+__device__ __forceinline__ void store_y_dyn(void* Y, int yk, size_t idx, float v) {
+  if (yk == kYF16) store_y<kYF16>(Y, idx, v);
+  else if (yk == kYBF16) store_y<kYBF16>(Y, idx, v);
+  else store_y<kYF32>(Y, idx, v);
+}
+
+template <int BT, int XK>
+__global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
+                const __grid_constant__ CUtensorMap tm_aug, const GemmParams p) {
+  using C = Cfg<BT>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* const gbase = smem_raw + (base - raw);
+  const uint32_t sx = base;
+  const uint32_t sw = sx + C::kNSX * C::kXStageBytes;
+  const uint32_t sbar = sw + C::kNSX * C::kWStageBytes;
+  auto full_x = [&](int s) { return sbar + 8u * s; };
+  auto empty_x = [&](int s) { return sbar + 8u * (C::kNSX + s); };
+  auto full_a = [&](int a) { return sbar + 8u * (2 * C::kNSX + a); };
+  auto empty_a = [&](int a) { return sbar + 8u * (2 * C::kNSX + C::kNSA + a); };
+  const uint32_t done_bar = sbar + 8u * (2 * C::kNSX + 2 * C::kNSA);
+  const uint32_t misc = sbar + 8u * C::kNumBars;
+  uint8_t* const gmisc = gbase + (misc - base);
+  volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gmisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(gmisc + 8);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kTileN;
+  const int m0 = blockIdx.y * BT;
+  const int seg = blockIdx.z;
+  const int kb0 = seg * p.kb_per_split;
+  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  const int n_aug = (seg == 0) ? p.aug_stages : 0;
+  const int n_stages = n_aug + max(0, kb1 - kb0);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kNSX; ++s) {
+      mbar_init(full_x(s), 1);
+      mbar_init(empty_x(s), 1 + 4);  // MMA commit + one arrive per dequant warp
+    }
+    for (int a = 0; a < C::kNSA; ++a) {
+      mbar_init(full_a(a), 4);
+      mbar_init(empty_a(a), 1);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0;
+    *last_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tm_x);
+    prefetch_tensormap(&tm_w);
+    if (p.aug_stages > 0) prefetch_tensormap(&tm_aug);
+  }
+  if (warp == 1) {
+    tmem_alloc(misc, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, &g_status};
+      int issued = 0;
+      for (int it = 0; it < n_stages; ++it) {
+        const int s = it % C::kNSX;
+        const uint32_t ph = (it / C::kNSX) & 1;
+        if (!mbar_wait(empty_x(s), ph ^ 1, wc)) break;
+        const uint32_t xdst = sx + s * C::kXStageBytes;
+        if (it < n_aug) {
+          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes);
+          tma_load_2d(xdst, &tm_aug, full_x(s), it * kKBlock, m0);
+          tma_load_2d(xdst + C::kXAtomBytes, &tm_aug, full_x(s), it * kKBlock + 64, m0);
+        } else {
+          const int kb = kb0 + (it - n_aug);
+          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes);
+          tma_load_2d(xdst, &tm_x, full_x(s), kb * kKBlock, m0);
+          tma_load_2d(xdst + C::kXAtomBytes, &tm_x, full_x(s), kb * kKBlock + 64, m0);
+          tma_load_2d(sw + s * C::kWStageBytes, &tm_w, full_x(s), kb * kWordsPerKBlock, n0);
+        }
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        // Drain: let every copy this thread issued land before the CTA exits.
+        volatile int never = 0;
+        const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, &g_status};
+        for (int it = max(0, issued - C::kNSX); it < issued; ++it)
+          mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMma, &g_status};
+      const uint32_t d_tmem = tmem + C::kDCol;
+      const uint32_t id_x = idesc_f16(XK, 128, BT);
+      const uint32_t id_aug = idesc_f16(1, 128, BT);
+      for (int it = 0; it < n_stages; ++it) {
+        const int s = it % C::kNSX;
+        const uint32_t ph = (it / C::kNSX) & 1;
+        const int a = it % C::kNSA;
+        const uint32_t pha = (it / C::kNSA) & 1;
+        if (!mbar_wait(full_x(s), ph, wc)) break;
+        if (!mbar_wait(full_a(a), pha, wc)) break;
+        tc_fence_after();
+        const uint32_t xs = sx + s * C::kXStageBytes;
+        const uint32_t id = (it < n_aug) ? id_aug : id_x;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint64_t bd = desc_kmajor_sw128(xs + (i >> 2) * C::kXAtomBytes + (i & 3) * 32);
+          mma_ts(d_tmem, tmem + a * 64 + i * 8, bd, id, (it > 0 || i > 0) ? 1u : 0u);
+        }
+        mma_commit(empty_x(s));
+        mma_commit(empty_a(a));
+      }
+      mma_commit(done_bar);
+    }
+  } else {
+    // ------------------------------------------------------------ dequant + epilogue
+    const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, &g_status};
+    const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;        // weight row of the tile = TMEM lane
+    const int n = n0 + row;
+    const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+    const uint8_t* wring = gbase + (sw - base);
+
+    for (int it = 0; it < n_stages; ++it) {
+      const int s = it % C::kNSX;
+      const uint32_t ph = (it / C::kNSX) & 1;
+      const int a = it % C::kNSA;
+      const uint32_t pha = (it / C::kNSA) & 1;
+      const uint32_t a_tmem = tmem + lane_base + a * 64;
+      if (it < n_aug) {
+        // weight-side correction columns: [d_hi | d_hi | d_lo], zero padded
+        uint32_t v[64];
+        const int G = p.G;
+#pragma unroll 4
+        for (int i = 0; i < 64; ++i) {
+          __nv_bfloat16 e[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int j = it * kKBlock + 2 * i + h;
+            e[h] = __float2bfloat16_rn(0.0f);
+            if (j < 3 * G) {
+              const int t = j / G;
+              const int g = j - t * G;
+              __nv_bfloat16 hi, lo;
+              split_bf16(__ldg(p.delta + static_cast<size_t>(g) * p.N + n), hi, lo);
+              e[h] = (t == 2) ? lo : hi;
+            }
+          }
+          v[i] = pack_bf16x2(e[0], e[1]);
+        }
+        if (!warp_wait(full_x(s), ph, wc)) break;
+        if (lane == 0) mbar_arrive(empty_x(s));
+        if (!warp_wait(empty_a(a), pha ^ 1, wc)) break;
+        tmem_st32(a_tmem, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+        tmem_st32(a_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      } else {
+        const int kb = kb0 + (it - n_aug);
+        const int g = (kb * kKBlock) / p.group_size;
+        const __half sc = p.S[static_cast<size_t>(g) * p.N + n];
+        if (!warp_wait(full_x(s), ph, wc)) break;
+        uint4 wv[4];
+        const uint8_t* wrow = wring + s * C::kWStageBytes + row * 64;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          wv[c] = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ ((row >> 1) & 3)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_x(s));
+        const uint32_t words[16] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w, wv[1].x, wv[1].y,
+                                    wv[1].z, wv[1].w, wv[2].x, wv[2].y, wv[2].z, wv[2].w,
+                                    wv[3].x, wv[3].y, wv[3].z, wv[3].w};
+        uint32_t v0[32], v1[32];
+        if (XK == kXF16) {
+          const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            uint32_t o[4], o2[4];
+            dq8_f16_scaled(words[w], s2, o);
+            dq8_f16_scaled(words[w + 8], s2, o2);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v0[4 * w + e] = o[e];
+              v1[4 * w + e] = o2[e];
+            }
+          }
+        } else {
+          const float sf = __half2float(sc);
+#pragma unroll
+          for (int w = 0; w < 8; ++w) {
+            uint32_t o[4], o2[4];
+            dq8_bf16_scaled(words[w], sf, o);
+            dq8_bf16_scaled(words[w + 8], sf, o2);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              v0[4 * w + e] = o[e];
+              v1[4 * w + e] = o2[e];
+            }
+          }
+        }
+        if (!warp_wait(empty_a(a), pha ^ 1, wc)) break;
+        tmem_st32(a_tmem, v0);
+        tmem_st32(a_tmem + 32, v1);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_a(a));
+    }
+
+    // ---- epilogue: accumulator -> Y (or fp32 partial)
+    warp_wait(done_bar, 0, wc);
+    named_bar_sync(1, 128);
+    const bool ok = !*abort_flag;  // uniform: no wait can set the flag past this point
+    tc_fence_after();
+    if (ok) {
+      const uint32_t dt = tmem + lane_base + C::kDCol;
+      const bool direct = (p.splits == 1);
+      const int mlim = min(BT, p.M - m0);
+      for (int c = 0; c < BT / 16; ++c) {
+        if (16 * c >= mlim) break;
+        uint32_t r[16];
+        tmem_ld16(dt + 16 * c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int ml = 16 * c + j;
+          if (ml < mlim) {
+            const int m = m0 + ml;
+            float val = __uint_as_float(r[j]);
+            if (p.x_scale) val *= __ldg(p.x_scale + m);
+            if (direct) {
+              store_y_dyn(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
+            } else {
+              p.partials[(static_cast<size_t>(seg) * p.M + m) * p.N + n] = val;
+            }
+          }
+        }
+      }
+      if (!direct) {
+        __threadfence();
+        named_bar_sync(1, 128);
+        const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+        if (threadIdx.x == 64) {
+          const int old = atomicAdd(p.counters + tile, 1);
+          *last_flag = (old == p.splits - 1) ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        if (*last_flag) {
+          __threadfence();
+          for (int ml = 0; ml < mlim; ++ml) {
+            const int m = m0 + ml;
+            float acc = 0.0f;
+            for (int sg = 0; sg < p.splits; ++sg)
+              acc += __ldcg(p.partials + (static_cast<size_t>(sg) * p.M + m) * p.N + n);
+            store_y_dyn(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
+          }
+          if (threadIdx.x == 64) p.counters[tile] = 0;
+        }
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    // Every MMA this CTA issued has completed once the final commit arrived.
+    volatile int never = 0;
+    const WaitCtx drain{&never, 50000000ull, kDevTimeoutMma, &g_status};
+    mbar_wait(done_bar, 0, drain);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int BT, int XK>
+static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t st) {
+  using C = Cfg<BT>;
+  static unsigned long long attr_mask = 0;  // one bit per device that has the attribute set
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_mask & bit)) {
+    e = cudaFuncSetAttribute(gemm_kernel<BT, XK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_mask |= bit;
+  }
+  dim3 grid(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
+  gemm_kernel<BT, XK><<<grid, 192, C::kSmemBytes, st>>>(tm_x, tm_w, tm_aug, p);
+  return cudaGetLastError();
+}
+
+template <int XK>
+static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                             const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t st) {
+  switch (bt) {
+    case 16: return launch_bt<16, XK>(tm_x, tm_w, tm_aug, p, st);
+    case 32: return launch_bt<32, XK>(tm_x, tm_w, tm_aug, p, st);
+    case 64: return launch_bt<64, XK>(tm_x, tm_w, tm_aug, p, st);
+    case 128: return launch_bt<128, XK>(tm_x, tm_w, tm_aug, p, st);
+    case 256: return launch_bt<256, XK>(tm_x, tm_w, tm_aug, p, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                        const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t stream) {
+  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_w, tm_aug, p, stream)
+                          : launch_xk<kXF16>(bt, tm_x, tm_w, tm_aug, p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Bounded-wait probe: one thread waits on an mbarrier that nothing arrives
+// on.  The wait gives up after limit_ns, records kDevTimeoutProbe in the
+// status word and the kernel returns normally.
+// ---------------------------------------------------------------------------
+__global__ void wait_probe_kernel(unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(smem_u32(&bar), 1);
+    fence_mbar_init();
+    const WaitCtx w{&abort_flag, limit_ns, kDevTimeoutProbe, &g_status};
+    mbar_wait(smem_u32(&bar), 0, w);
+  }
+}
+
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t st) {
+  wait_probe_kernel<<<1, 32, 0, st>>>(limit_ns);
+  return cudaGetLastError();
+}
+
+cudaError_t read_status(unsigned int* out) {
+  return cudaMemcpyFromSymbol(out, g_status, sizeof(unsigned int));
+}
+
+cudaError_t clear_status() {
+  const unsigned int zero = 0;
+  return cudaMemcpyToSymbol(g_status, &zero, sizeof(zero));
+}
+
+size_t gemm_smem_bytes(int bt) {
+  switch (bt) {
+    case 16: return Cfg<16>::kSmemBytes;
+    case 32: return Cfg<32>::kSmemBytes;
+    case 64: return Cfg<64>::kSmemBytes;
+    case 128: return Cfg<128>::kSmemBytes;
+    case 256: return Cfg<256>::kSmemBytes;
+    default: return 0;
+  }
+}
+
+}  // namespace wq

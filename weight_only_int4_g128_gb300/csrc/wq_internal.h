@@ -1,0 +1,69 @@
+// wq_internal.h -- declarations shared by the library's translation units
+// (not part of the public C ABI; see include/wq.h for that).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace wq {
+
+constexpr int kTileN = 128;        // weight rows (output columns) per CTA = MMA M
+constexpr int kKBlock = 128;       // K elements per pipeline stage
+constexpr int kWordsPerKBlock = kKBlock / 8;
+constexpr int kNumSMs = 152;
+
+// Status bits written by kernels into the device status word.
+constexpr unsigned kDevTimeoutProducer = 1u << 0;
+constexpr unsigned kDevTimeoutMma = 1u << 1;
+constexpr unsigned kDevTimeoutMath = 1u << 2;
+constexpr unsigned kDevTimeoutFixup = 1u << 3;
+constexpr unsigned kDevTimeoutProbe = 1u << 4;
+
+enum XKind { kXF16 = 0, kXBF16 = 1 };
+enum YKind { kYF16 = 0, kYBF16 = 1, kYF32 = 2 };
+
+struct GemmParams {
+  int M, N, K;
+  int group_size;        // K for one group per column
+  int G;                 // number of groups
+  int kb_total;          // K / 128
+  int kb_per_split;      // k-blocks per split segment
+  int splits;            // number of K segments (gridDim.z)
+  int aug_stages;        // correction stages (Kaug / 128), 0 when there is no correction
+  int kaug;              // padded correction length (multiple of 128)
+  const __half* S;       // [G][N] group scales
+  const float* delta;    // [G][N] zero-point residual, or null
+  const float* x_scale;  // [M] per-token activation scale (W4A8), or null
+  void* Y;               // [M][N]
+  int y_kind;
+  float* partials;       // [splits][M][N] fp32 (split-K only)
+  int* counters;         // one per output tile (split-K only)
+  unsigned long long timeout_ns;
+};
+
+// Host-side launchers (wq_gemm.cu).
+cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                        const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t stream);
+size_t gemm_smem_bytes(int bt);
+
+// Pre-pass kernels (wq_kernels.cu).
+cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
+                            int kaug, __nv_bfloat16* aug, cudaStream_t stream);
+cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t stream);
+cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
+                        uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,
+                        cudaStream_t stream);
+cudaError_t launch_unpack(const uint32_t* Bpacked, uint8_t* q, int K, int N, cudaStream_t stream);
+cudaError_t launch_dequant(const uint32_t* Bpacked, const __half* S, void* W, int w_kind, int K,
+                           int N, int group_size, cudaStream_t stream);
+cudaError_t launch_quantize_per_token(const __half* x, int8_t* Xq, float* x_scale, int M, int K,
+                                      cudaStream_t stream);
+cudaError_t launch_wait_probe(unsigned long long limit_ns, cudaStream_t stream);
+cudaError_t read_status(unsigned int* out);
+cudaError_t clear_status();
+
+}  // namespace wq

@@ -1,0 +1,260 @@
+// wq_kernels.cu -- the small kernels around the GEMM: load-time pack (with
+// the W4A8 sign fold), unpack, dequant, per-token int8 quantization, and the
+// per-call pre-passes (group sums for the zero-point correction, int8 -> fp16
+// activations for W4A8).
+#include "wq_device.cuh"
+
+namespace wq {
+
+// ---------------------------------------------------------------------------
+// Pack ("Marlin INT4 on Ada -- how it works", section "The pipeline, end to
+// end": 8 x int4 per uint32, delta = zero + 8 * scale per group and column;
+// HyperQwen W4A8 article, section "hidden mine": negative group scales fold
+// into the codes, s -> -s, v -> 16 - v clamped to 15).
+//
+// Layout: Bpacked[n][K/8]; word (n, w) holds codes q[8w + j][n] with code j at
+// bit 4*(j/2) + 16*(j%2).  A 32 (n) x 32 (word) tile goes through shared
+// memory so that both the code reads and the word writes are coalesced.
+// ---------------------------------------------------------------------------
+__global__ void pack_kernel(const uint8_t* __restrict__ q, const __half* __restrict__ scale,
+                            int fold, uint32_t* __restrict__ Bpacked, int K, int N,
+                            int group_size) {
+  __shared__ uint32_t tile[32][33];
+  const int KW = K / 8;
+  const int w0 = blockIdx.x * 32;
+  const int nb = blockIdx.y * 32;
+  const int tx = threadIdx.x;  // 0..31
+  const int ty = threadIdx.y;  // 0..7
+  const int n = nb + tx;
+  for (int r = ty; r < 32; r += 8) {
+    const int w = w0 + r;
+    uint32_t word = 0;
+    if (w < KW && n < N) {
+      bool neg = false;
+      if (fold) {
+        const int g = (8 * w) / group_size;
+        neg = __half2float(scale[static_cast<size_t>(g) * N + n]) < 0.0f;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t v = q[static_cast<size_t>(8 * w + j) * N + n] & 0xFu;
+        if (neg) v = min(16u - v, 15u);
+        word |= v << (4 * (j >> 1) + 16 * (j & 1));
+      }
+    }
+    tile[r][tx] = word;
+  }
+  __syncthreads();
+  for (int r = ty; r < 32; r += 8) {
+    const int nn = nb + r;
+    const int w = w0 + tx;
+    if (nn < N && w < KW) Bpacked[static_cast<size_t>(nn) * KW + w] = tile[tx][r];
+  }
+}
+
+// S = |scale| (fold) or scale; delta = fp32(zero) + 8 * fp32(scale) rounded once.
+__global__ void pack_scales_kernel(const __half* __restrict__ scale, const __half* __restrict__ zero,
+                                   int fold, __half* __restrict__ S, float* __restrict__ delta,
+                                   long long count) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= count) return;
+  const __half s = scale[i];
+  if (fold) {
+    S[i] = (__half2float(s) < 0.0f) ? __hneg(s) : s;
+  } else {
+    S[i] = s;
+  }
+  if (delta) delta[i] = __fmaf_rn(8.0f, __half2float(s), __half2float(zero[i]));
+}
+
+__global__ void unpack_kernel(const uint32_t* __restrict__ Bpacked, uint8_t* __restrict__ q, int K,
+                              int N) {
+  const int KW = K / 8;
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= static_cast<long long>(KW) * N) return;
+  const int n = static_cast<int>(i % N);  // n fastest: coalesced code writes
+  const int w = static_cast<int>(i / N);
+  const uint32_t word = Bpacked[static_cast<size_t>(n) * KW + w];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    q[static_cast<size_t>(8 * w + j) * N + n] = (word >> (4 * (j >> 1) + 16 * (j & 1))) & 0xFu;
+}
+
+// W[k][n] = RN((v - 8) * s) in fp16 or bf16: the same dequant routines the
+// GEMM uses, exposed so the dequantized weights can be checked bit for bit.
+__global__ void dequant_kernel(const uint32_t* __restrict__ Bpacked, const __half* __restrict__ S,
+                               void* __restrict__ W, int w_kind, int K, int N, int group_size) {
+  const int KW = K / 8;
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= static_cast<long long>(KW) * N) return;
+  const int n = static_cast<int>(i % N);
+  const int w = static_cast<int>(i / N);
+  const uint32_t word = Bpacked[static_cast<size_t>(n) * KW + w];
+  const int g = (8 * w) / group_size;
+  const __half sc = S[static_cast<size_t>(g) * N + n];
+  uint32_t o[4];
+  if (w_kind == kXF16) {
+    dq8_f16_scaled(word, static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u, o);
+  } else {
+    dq8_bf16_scaled(word, __half2float(sc), o);
+  }
+  uint16_t* out = reinterpret_cast<uint16_t*>(W);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    out[static_cast<size_t>(8 * w + 2 * p) * N + n] = static_cast<uint16_t>(o[p] & 0xFFFFu);
+    out[static_cast<size_t>(8 * w + 2 * p + 1) * N + n] = static_cast<uint16_t>(o[p] >> 16);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Per-token int8 quantization (HyperQwen article, "why W4A8": activations are
+// quantized per token to int8).  x_scale = fp32_RN(amax / 127); code =
+// clamp(rint(fp32_RN(x / x_scale)), -127, 127); an all-zero row gives zeros.
+// One block per row.
+// ---------------------------------------------------------------------------
+__global__ void quantize_per_token_kernel(const __half* __restrict__ x, int8_t* __restrict__ Xq,
+                                          float* __restrict__ x_scale, int K) {
+  __shared__ float red[32];
+  const int m = blockIdx.x;
+  const __half* row = x + static_cast<size_t>(m) * K;
+  float amax = 0.0f;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(__half2float(row[k])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = (threadIdx.x < (blockDim.x + 31) / 32) ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float xs = __fdiv_rn(amax, 127.0f);
+  if (threadIdx.x == 0) x_scale[m] = xs;
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    int code = 0;
+    if (xs > 0.0f) {
+      float r = rintf(__fdiv_rn(__half2float(row[k]), xs));
+      r = fminf(fmaxf(r, -127.0f), 127.0f);
+      code = static_cast<int>(r);
+    }
+    Xq[static_cast<size_t>(m) * K + k] = static_cast<int8_t>(code);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Correction pre-pass: a_sum[m][g] = sum_{k in g} X[m][k] in fp32 ("Marlin
+// INT4 on Ada", section "The core mismatch"), written as the activation-side
+// correction columns aug[m][0..kaug) = [a_hi | a_lo | a_hi | 0...] in bf16.
+// One block per row m; warp w sums groups w, w+4, ...
+// ---------------------------------------------------------------------------
+template <int XK>
+__global__ void aug_prep_kernel(const void* __restrict__ X, int K, int group_size, int G, int kaug,
+                                __nv_bfloat16* __restrict__ aug) {
+  const int m = blockIdx.x;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint16_t* row = reinterpret_cast<const uint16_t*>(X) + static_cast<size_t>(m) * K;
+  __nv_bfloat16* arow = aug + static_cast<size_t>(m) * kaug;
+  for (int g = warp; g < G; g += blockDim.x >> 5) {
+    float acc = 0.0f;
+    const uint16_t* gp = row + static_cast<size_t>(g) * group_size;
+    for (int k = lane * 8; k < group_size; k += 256) {
+      const uint4 v = *reinterpret_cast<const uint4*>(gp + k);
+      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float lo, hi;
+        if (XK == kXF16) {
+          lo = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu)));
+          hi = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
+        } else {
+          lo = __uint_as_float(u[i] << 16);
+          hi = __uint_as_float(u[i] & 0xFFFF0000u);
+        }
+        acc += lo;
+        acc += hi;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      __nv_bfloat16 h, l;
+      split_bf16(acc, h, l);
+      arow[g] = h;
+      arow[G + g] = l;
+      arow[2 * G + g] = h;
+    }
+  }
+  for (int j = 3 * G + threadIdx.x; j < kaug; j += blockDim.x) arow[j] = __float2bfloat16_rn(0.0f);
+}
+
+__global__ void i8_to_f16_kernel(const int8_t* __restrict__ Xq, __half* __restrict__ X16,
+                                 long long count) {
+  const long long i = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) * 4;
+  if (i + 3 < count) {
+    const char4 c = *reinterpret_cast<const char4*>(Xq + i);
+    __half2* o = reinterpret_cast<__half2*>(X16 + i);
+    o[0] = __halves2half2(__int2half_rn(c.x), __int2half_rn(c.y));
+    o[1] = __halves2half2(__int2half_rn(c.z), __int2half_rn(c.w));
+  } else {
+    for (long long j = i; j < count; ++j) X16[j] = __int2half_rn(Xq[j]);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
+                        uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,
+                        cudaStream_t st) {
+  dim3 grid((K / 8 + 31) / 32, (N + 31) / 32);
+  pack_kernel<<<grid, dim3(32, 8), 0, st>>>(q, scale, fold, Bpacked, K, N, group_size);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long count = static_cast<long long>(K / group_size) * N;
+  pack_scales_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(
+      scale, zero, fold, S, zero ? delta : nullptr, count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack(const uint32_t* Bpacked, uint8_t* q, int K, int N, cudaStream_t st) {
+  const long long count = static_cast<long long>(K / 8) * N;
+  unpack_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(Bpacked, q, K, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dequant(const uint32_t* Bpacked, const __half* S, void* W, int w_kind, int K,
+                           int N, int group_size, cudaStream_t st) {
+  const long long count = static_cast<long long>(K / 8) * N;
+  dequant_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(Bpacked, S, W, w_kind,
+                                                                             K, N, group_size);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_per_token(const __half* x, int8_t* Xq, float* x_scale, int M, int K,
+                                      cudaStream_t st) {
+  quantize_per_token_kernel<<<M, 256, 0, st>>>(x, Xq, x_scale, K);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
+                            int kaug, __nv_bfloat16* aug, cudaStream_t st) {
+  if (x_kind == kXBF16) {
+    aug_prep_kernel<kXBF16><<<M, 128, 0, st>>>(X, K, group_size, G, kaug, aug);
+  } else {
+    aug_prep_kernel<kXF16><<<M, 128, 0, st>>>(X, K, group_size, G, kaug, aug);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t st) {
+  const long long threads = (count + 3) / 4;
+  i8_to_f16_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(Xq, X16, count);
+  return cudaGetLastError();
+}
+
+
+}  // namespace wq
