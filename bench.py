@@ -1,0 +1,446 @@
+#!/usr/bin/env python
+"""Benchmark of the W4A16 group-quantized INT4-weight GEMM on GB300.
+
+Default workload: the decode GEMV shapes, M in {1, 4, 16} x N in {4096, 11008},
+K = 4096, group 128, asymmetric weights, fp16 activations and output.  One
+"step" runs all six GEMMs (each on its own resident copy of the packed
+weights); the weight copies rotate over >3x the L2 size so every GEMM reads its
+weights from HBM.  The metric is weight GB/s (codes + fp16 scales + fp32 delta
+per second) for the whole job; TFLOPS is reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wq|reference]
+                    [--workload c1|c0|c2|c3|c4]
+
+--impl reference times the CPU oracle (plain C, fp64, naive loops) on a bounded
+sample of the same workload.  Under torchrun each rank runs an independent
+replica on its own GPU (the GEMM has no exchange step); rank 0 prints one JSON
+line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "W4A16 GEMM TFLOPS & weight GB/s vs M on 1 GB300; % of HBM / tensor-core roofline"
+L2_BYTES = 129 * 2 ** 20
+PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+WORKLOAD_NAMES = {
+    "c0": "W4A16 asym M16 K256 N256 g128 fp16",
+    "c1": "W4A16 asym decode GEMV M{1,4,16} x N{4096,11008} K4096 g128 fp16",
+    "c2": "W4A16 asym batched M{64,128,256} K8192 N8192 g128 and per-channel fp16",
+    "c3": "W4A16 asym prefill M4096 K5120 N17408 + M4096 K17408 N5120 g128 bf16",
+    "c4": "W4A8 sym M{16,256,2048} K5120 N17408 g128 int8 per-token",
+}
+
+
+# ----------------------------------------------------------------------------- helpers
+def weight_bytes(s) -> int:
+    K, N = s["K"], s["N"]
+    G = synth.num_groups(K, s["group_size"])
+    b = K * N // 2 + G * N * 2
+    if s["mode"] == "w4a16":
+        b += G * N * 4
+    return b
+
+
+def io_bytes(s) -> int:
+    xb = 1 if s["mode"] == "w4a8" else 2
+    return s["M"] * s["K"] * xb + s["M"] * s["N"] * 2 + (s["M"] * 4 if s["mode"] == "w4a8" else 0)
+
+
+def flops(s) -> int:
+    return 2 * s["M"] * s["N"] * s["K"]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_init():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample(shapes, budget_s: float, cols: int = 2048):
+    """Time the CPU oracle on column windows of every shape until budget_s has passed."""
+    import oracle
+    probs = []
+    for seed, s in shapes:
+        d = synth.make_inputs(seed, **s)
+        w = min(cols, s["N"])
+        G = synth.num_groups(s["K"], s["group_size"])
+        wb = s["K"] * w // 2 + G * w * 2 + (G * w * 4 if s["mode"] == "w4a16" else 0)
+        probs.append((s, d, w, wb))
+    done_bytes = 0
+    done_flops = 0
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        for s, d, w, wb in probs:
+            if s["mode"] == "w4a8":
+                Xq, xs = oracle.quantize_per_token(d["A"])
+                qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), s["group_size"])
+                oracle.gemm_w4a8(Xq, xs, qf, sf, s["group_size"], cols=(0, w))
+            else:
+                A = oracle.activations_to_double(d["A"], s["a_dtype"])
+                oracle.gemm_asym_plain(A, d["q"], oracle.half_bits(d["scale"]),
+                                       oracle.half_bits(d["zero"]), s["group_size"], cols=(0, w))
+            done_bytes += wb
+            done_flops += 2 * s["M"] * s["K"] * w
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    sample = (f"{passes} pass(es) over the {len(probs)} shapes, columns [0, {cols}) of each, "
+              f"all rows and the full K, fp64 naive loops")
+    return done_bytes / el / 1e9, done_flops / el / 1e12, el, threads, sample
+
+
+def run_reference(args, shapes, ws, rank):
+    if rank != 0:
+        return 0
+    budget = max(2.0, min(20.0, 4.0 * args.steps))
+    steps = []
+    for _ in range(args.warmup and 1):
+        oracle_sample(shapes, 0.5, cols=256)
+    gbs, tfl, el, threads, sample = oracle_sample(shapes, budget)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+        "tflops": round(tfl, 9), "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "sampled": True},
+        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    del steps
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args, shapes, ws, rank, local):
+    import torch
+
+    import weight_only_int4_g128_gb300 as wq
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wq.load_library(build_if_missing=True)
+    if not wq.device_supported(local):
+        raise RuntimeError("not an sm_103 device")
+
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    # --- problems: inputs resident in HBM, weights replicated to rotate past L2
+    probs = []
+    set_bytes = 0
+    for seed, s in shapes:
+        d = synth.make_inputs(seed, **s)
+        gs = s["group_size"]
+        if s["mode"] == "w4a8":
+            Bp, S = wq.pack_w4a8(cu(d["q"]), cu(d["scale"]), gs)
+            dl = None
+            X16 = cu(d["A"])
+            Xq, xs = wq.quantize_per_token(X16)
+            X = (Xq, xs)
+        else:
+            Bp, S, dl = wq.pack_w4a16(cu(d["q"]), cu(d["scale"]), cu(d["zero"]), gs)
+            if s["a_dtype"] == "bf16":
+                X = cu(d["A"].view(np.int16)).view(torch.bfloat16)
+            else:
+                X = cu(d["A"])
+        probs.append({"s": s, "w": [(Bp, S, dl)], "X": X, "A_host": d["A"]})
+        set_bytes += weight_bytes(s)
+        del d
+    reps = max(1, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    for p in probs:
+        Bp, S, dl = p["w"][0]
+        for _ in range(reps - 1):
+            p["w"].append((Bp.clone(), S.clone(), dl.clone() if dl is not None else None))
+    for p in probs:
+        s = p["s"]
+        p["Y"] = torch.empty((s["M"], s["N"]), dtype=torch.float16, device=dev)
+        variant = wq.VARIANT_W4A8 if s["mode"] == "w4a8" else wq.VARIANT_W4A16
+        need = wq.workspace_size(variant, s["M"], s["N"], s["K"], s["group_size"])
+        p["ws"] = torch.zeros(max(need, 4096), dtype=torch.uint8, device=dev)
+
+    def call(p, r, out=None, X=None):
+        s = p["s"]
+        Bp, S, dl = p["w"][r]
+        X = p["X"] if X is None else X
+        if s["mode"] == "w4a8":
+            return wq.gemm_w4a8(X[0], X[1], Bp, S, s["group_size"], out=p["Y"] if out is None else out,
+                                workspace=p["ws"])
+        return wq.gemm_w4a16(X, Bp, S, dl, s["group_size"], out=p["Y"] if out is None else out,
+                             workspace=p["ws"])
+
+    # eager warm-up (sets kernel attributes, checks the calls work)
+    for p in probs:
+        for r in range(reps):
+            call(p, r)
+    torch.cuda.synchronize()
+
+    # --- one CUDA graph per weight replica: a whole step (all shapes)
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for p in probs:
+                    call(p, r)
+            graphs.append(g)
+    torch.cuda.synchronize()
+
+    launches_per_call = {"w4a16": 2, "w4a8": 2}
+    launches_per_step = sum(launches_per_call[p["s"]["mode"]] for p in probs)
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            graphs[i % reps].replay()
+    torch.cuda.synchronize()
+
+    # --- timed region
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(args.steps):
+            graphs[i % reps].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    if ws > 1:
+        t = torch.tensor([ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    step_wbytes = sum(weight_bytes(p["s"]) for p in probs)
+    step_flops = sum(flops(p["s"]) for p in probs)
+    value = ws * step_wbytes / (ms_per_step * 1e-3) / 1e9
+    tflops = ws * step_flops / (ms_per_step * 1e-3) / 1e12
+
+    # --- per-shape launch timing of the GEMM call (graphs of `per` calls on rotating weights)
+    per = 2 * reps
+    shape_rows = []
+    tot_alg = 0
+    tot_ms = 0.0
+    for p in probs:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(per):
+                    call(p, j % reps)
+            for _ in range(3):
+                g.replay()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            nrep = 20
+            for _ in range(nrep):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / (nrep * per)
+        s = p["s"]
+        alg = weight_bytes(s) + io_bytes(s)
+        tot_alg += alg
+        tot_ms += us * 1e-3
+        shape_rows.append({"M": s["M"], "N": s["N"], "K": s["K"], "us": round(us, 3),
+                           "weight_GBps": round(weight_bytes(s) / (us * 1e-6) / 1e9, 1),
+                           "tflops": round(flops(s) / (us * 1e-6) / 1e12, 3)})
+
+    peaks, peaks_src = load_peaks()
+    achieved = tot_alg / (tot_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs, copy)"
+                if peaks_src == "measured" else "fallback 6.8 TB/s",
+                "kernel": "wq::gemm_kernel (one call = group-sum pre-pass + GEMM)",
+                "per_shape": shape_rows}
+
+    # --- end to end through the public API: pinned host X -> device, GEMM, Y -> pinned host
+    e2e_steps = max(20, min(200, args.steps // 50))
+    hx = []
+    hy = []
+    for p in probs:
+        s = p["s"]
+        if s["mode"] == "w4a8":
+            hx.append(None)
+        else:
+            a = p["A_host"]
+            t = torch.from_numpy(a.view(np.int16) if s["a_dtype"] == "bf16" else a)
+            hx.append(t.pin_memory())
+        hy.append(torch.empty((s["M"], s["N"]), dtype=torch.float16).pin_memory())
+    dx = [torch.empty_like(p["X"]) if not isinstance(p["X"], tuple) else None for p in probs]
+    h2d = sum(t.numel() * t.element_size() for t in hx if t is not None)
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(3 + e2e_steps):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            for j, p in enumerate(probs):
+                if hx[j] is not None:
+                    src = hx[j]
+                    if p["X"].dtype == torch.bfloat16:
+                        dx[j].view(torch.int16).copy_(src, non_blocking=True)
+                    else:
+                        dx[j].copy_(src, non_blocking=True)
+                    call(p, i % reps, X=dx[j])
+                else:
+                    call(p, i % reps)
+                hy[j].copy_(p["Y"], non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_val = ws * step_wbytes / e2e_s / 1e9
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "tflops": round(tflops, 3),
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "config": {"workload": WORKLOAD_NAMES[args.workload],
+                   "shapes": [f"M{p['s']['M']} K{p['s']['K']} N{p['s']['N']}" for p in probs],
+                   "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB "
+                         f"> 3x L2); activations resident",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "graph": "one CUDA graph per weight copy holds one step"},
+        "roofline": roofline,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "pinned host X -> device, GEMM via the Python API, Y -> pinned host, "
+                        "synchronised every step"},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, tfl, el, threads, sample = oracle_sample(shapes, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads,
+                                "kind": "oracle", "sample": sample, "seconds": round(el, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
+    ap.add_argument("--workload", choices=list(WORKLOAD_NAMES), default="c1")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    ws, rank, local = dist_init()
+    shapes = synth.shapes(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, shapes, ws, rank)
+    return run_gpu(args, shapes, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
