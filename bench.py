@@ -62,6 +62,14 @@ def io_bytes(s) -> int:
     return s["M"] * s["K"] * xb + s["M"] * s["N"] * 2 + (s["M"] * 4 if s["mode"] == "w4a8" else 0)
 
 
+def kernel_launches(s) -> int:
+    """Kernels one GEMM call enqueues (the decode kernel is a single launch for W4A16;
+    the large-M path adds the group-sum and delta pre-passes, W4A8 an int8->fp16 pass)."""
+    if s["mode"] == "w4a8":
+        return 2
+    return 1 if s["M"] <= 16 else 3
+
+
 def flops(s) -> int:
     return 2 * s["M"] * s["N"] * s["K"]
 
@@ -279,8 +287,7 @@ def run_gpu(args, shapes, ws, rank, local):
             graphs.append(g)
     torch.cuda.synchronize()
 
-    launches_per_call = {"w4a16": 2, "w4a8": 2}
-    launches_per_step = sum(launches_per_call[p["s"]["mode"]] for p in probs)
+    launches_per_step = sum(kernel_launches(p["s"]) for p in probs)
 
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
@@ -316,6 +323,14 @@ def run_gpu(args, shapes, ws, rank, local):
     value = ws * step_wbytes / (ms_per_step * 1e-3) / 1e9
     tflops = ws * step_flops / (ms_per_step * 1e-3) / 1e12
 
+    peaks, peaks_src = load_peaks()
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+                              "tflops": round(tflops, 3), "ms_per_step": round(ms_per_step, 6),
+                              "quick": True, "clocks": clk}), flush=True)
+        return 0
+
     # --- per-shape launch timing of the GEMM call (graphs of `per` calls on rotating weights)
     per = 2 * reps
     shape_rows = []
@@ -346,14 +361,13 @@ def run_gpu(args, shapes, ws, rank, local):
                            "weight_GBps": round(weight_bytes(s) / (us * 1e-6) / 1e9, 1),
                            "tflops": round(flops(s) / (us * 1e-6) / 1e12, 3)})
 
-    peaks, peaks_src = load_peaks()
     achieved = tot_alg / (tot_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1),
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
                 "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs, copy)"
                 if peaks_src == "measured" else "fallback 6.8 TB/s",
-                "kernel": "wq::gemm_kernel (one call = group-sum pre-pass + GEMM)",
+                "kernel": "wq::gemv_kernel (M <= 16) / wq::gemm_kernel; time per GEMM call",
                 "per_shape": shape_rows}
 
     # --- end to end through the public API: pinned host X -> device, GEMM, Y -> pinned host
@@ -432,11 +446,19 @@ def main():
     ap.add_argument("--workload", choices=list(WORKLOAD_NAMES), default="c1")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--shapes", type=str, default=None,
+                    help="comma-separated indices into the workload's shape list (profiling)")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed region only: no per-shape timing, e2e or CPU baseline (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_init()
     shapes = synth.shapes(args.workload)
+    if args.shapes:
+        shapes = [shapes[int(i)] for i in args.shapes.split(",")]
+    if args.quick:
+        args.no_cpu_baseline = True
     if args.impl == "reference":
         return run_reference(args, shapes, ws, rank)
     return run_gpu(args, shapes, ws, rank, local)

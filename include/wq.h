@@ -32,7 +32,7 @@
  *    pages' Marlin preconditions), M >= 0 (M == 0 is a no-op), group_size 128
  *    or K (-1 is accepted as K).  Other shapes return WQ_ERR_UNSUPPORTED_SHAPE.
  *  - Device pointers that a kernel reads with TMA or vector loads must be
- *    16-byte aligned: X, Xq, Bpacked, Y, the workspace.  Otherwise
+ *    16-byte aligned: X, Xq, Bpacked, S, delta, Y, the workspace.  Otherwise
  *    WQ_ERR_INVALID_ARG.
  *  - Only sm_103 devices are supported (WQ_ERR_ARCH otherwise).
  */

@@ -50,11 +50,15 @@ def test_library_links_no_driver_library():
 
 def test_version_and_workspace_queries(lib):
     assert b"sm_103a" in lib.wq_version()
-    # symmetric small-M decode: split-K partials only
+    # decode (M <= 16): split-K partials only, the same for both W4A16 variants
     a = lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 128)
     b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 16, 4096, 4096, 128)
     c = lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
-    assert a > b > 0 and c > b
+    assert a == b > 0 and c > b
+    # large M: the asymmetric variant adds the correction columns
+    a = lib.wq_workspace_size(wq.VARIANT_W4A16, 512, 4096, 4096, 128)
+    b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 512, 4096, 4096, 128)
+    assert a > b
     assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4000, 128) == 0  # K % 128
     assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 64) == 0   # group size
     assert lib.wq_workspace_size(9, 16, 4096, 4096, 128) == 0

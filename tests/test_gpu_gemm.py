@@ -119,7 +119,28 @@ def test_one_hot_rows_give_dequantized_weights_bit_exact(wq, adt, K):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("M,K", [(8, 512), (70, 1024), (257, 256)])
+@pytest.mark.parametrize("adt", ["f16", "bf16"])
+@pytest.mark.parametrize("gs", [128, -1])
+def test_one_hot_decode_path_bit_exact(wq, adt, gs):
+    """M = 16 one-hot rows (the decode kernel): Y[m, :] = RN((q - 8) * scale) of row k_m."""
+    K, N = 2048, 384
+    d = synth.make_inputs(550, 16, K, N, group_size=gs, a_dtype=adt)
+    ks = np.array([0, 1, 7, 8, 127, 128, 129, 511, 640, 1000, 1023, 1024, 1500, 2000, 2046, 2047])
+    eye = np.zeros((16, K), np.float32)
+    eye[np.arange(16), ks] = 1.0
+    if adt == "bf16":
+        d["A"] = (eye.view(np.uint32) >> 16).astype(np.uint16)
+        out, fn = torch.bfloat16, oracle.dequant_sym_bf16
+    else:
+        d["A"] = eye.astype(np.float16)
+        out, fn = torch.float16, oracle.dequant_sym_f16
+    Y, _ = _w4a16(wq, d, out, sym=True)
+    got = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+    want = fn(d["q"], oracle.half_bits(d["scale"]), gs)[ks]
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("M,K", [(8, 512), (70, 1024), (257, 256), (16, 4096)])
 def test_integer_weights_exact(wq, M, K):
     """scale = 1, zero = -8 (so delta = 0): C = X @ (q - 8) is an exact integer matmul."""
     N = 256

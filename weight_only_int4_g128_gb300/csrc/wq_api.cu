@@ -128,45 +128,74 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* p
   return WQ_OK;
 }
 
+// Activations [rows][K] as a 3-D tensor {64 k, rows, K/64 halves-of-k-blocks} so
+// that one box {64, box_rows, 2} fetches a whole 128-k block as two 128-byte
+// swizzled atoms placed one after the other in shared memory.
+int make_map_x3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t rows, uint64_t K,
+                 uint32_t box_rows) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {64, rows, K / 64};
+  cuuint64_t strides[2] = {K * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled (3-D activations) failed (%d)", static_cast<int>(r));
+  return WQ_OK;
+}
+
 // ---------------------------------------------------------------- heuristics
 struct Plan {
-  int bt;
+  bool gemv;      // M <= 16: decode kernel (single launch for W4A16)
+  int bt;         // token tile
   int splits;
   int kb_per_split;
-  int kaug;       // 0 without correction
-  size_t off_aug, off_x16, off_part;  // byte offsets into the workspace
+  int kaug;       // large-M correction length (0 without correction or for the decode kernel)
+  size_t off_aug, off_daug, off_x16, off_part;  // byte offsets into the workspace
   size_t bytes;
 };
 
 constexpr size_t kCounterBytes = 4096;  // split-K tile counters at the start of the workspace
+constexpr int kMaxCounters = static_cast<int>(kCounterBytes / 4);
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 Plan make_plan(int variant, int M, int N, int K, int gs) {
   Plan p{};
-  p.bt = (M <= 16) ? 16 : (M <= 32) ? 32 : (M <= 64) ? 64 : (M <= 128) ? 128 : 256;
   const int G = K / gs;
   const int kb = K / 128;
   const int ntiles = N / 128;
+  p.gemv = (M <= 16);
+  p.bt = p.gemv ? 16 : (M <= 32) ? 32 : (M <= 64) ? 64 : (M <= 128) ? 128 : 256;
   const int mtiles = (M + p.bt - 1) / p.bt;
   const int tiles = ntiles * mtiles;
+  // CTA slots per wave: the decode kernel and the 16/32-token tiles fit two per SM.
   const int slots = (p.bt <= 32) ? 2 * wq::kNumSMs : wq::kNumSMs;
   int splits = 1;
-  if (tiles < slots) {
-    splits = (slots + tiles - 1) / tiles;
+  if (p.gemv) {
+    // K segments of a column tile form one thread-block cluster (<= 8 CTAs)
+    splits = slots / tiles;
+    if (splits < 1) splits = 1;
+    if (splits > wq::gemv_max_splits()) splits = wq::gemv_max_splits();
     if (splits > kb) splits = kb;
-    if (tiles * 1 > static_cast<int>(kCounterBytes / 4)) splits = 1;
+  } else if (tiles < slots && tiles <= kMaxCounters) {
+    splits = slots / tiles;  // as many K segments as still fit in one wave
+    if (splits < 1) splits = 1;
+    if (splits > kb) splits = kb;
   }
   p.kb_per_split = (kb + splits - 1) / splits;
   p.splits = (kb + p.kb_per_split - 1) / p.kb_per_split;
-  p.kaug = (variant == WQ_VARIANT_W4A16) ? ((3 * G + 127) / 128) * 128 : 0;
+  p.kaug = (!p.gemv && variant == WQ_VARIANT_W4A16) ? ((3 * G + 127) / 128) * 128 : 0;
   size_t off = kCounterBytes;
   p.off_aug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(M) * p.kaug * 2);
+  p.off_daug = off;
+  if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
   p.off_x16 = off;
   if (variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(M) * K * 2);
   p.off_part = off;
-  if (p.splits > 1) off = align256(off + static_cast<size_t>(p.splits) * M * N * 4);
+  if (p.splits > 1 && !p.gemv) off = align256(off + static_cast<size_t>(p.splits) * M * N * 4);
   p.bytes = off;
   return p;
 }
@@ -191,14 +220,19 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     xg = x16;
   }
   __nv_bfloat16* aug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_aug);
+  __nv_bfloat16* daug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_daug);
   if (plan.kaug) {
     e = wq::launch_aug_prep(X, x_kind, M, K, gs, G, plan.kaug, aug, st);
     if (e != cudaSuccess) return cuda_fail(e, "group-sum pre-pass");
+    e = wq::launch_delta_aug(delta, G, N, plan.kaug, daug, st);
+    if (e != cudaSuccess) return cuda_fail(e, "delta pre-pass");
   }
 
-  CUtensorMap tm_x, tm_w, tm_aug;
-  int rc = make_map(&tm_x, x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                    2, xg, M, K, plan.bt, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  CUtensorMap tm_x, tm_w, tm_aug, tm_s, tm_d;
+  const CUtensorMapDataType xdt =
+      x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  int rc = plan.gemv ? make_map_x3d(&tm_x, xdt, xg, M, K, plan.bt)
+                     : make_map(&tm_x, xdt, 2, xg, M, K, plan.bt, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc) return rc;
   rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Bpacked, N, K / 8, 128, 16,
                 CU_TENSOR_MAP_SWIZZLE_64B);
@@ -209,6 +243,15 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     if (rc) return rc;
   } else {
     tm_aug = tm_x;  // unused
+  }
+  // scale and delta rows: one group row of 128 columns per pipeline stage
+  rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (rc) return rc;
+  if (delta && variant == WQ_VARIANT_W4A16) {
+    rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+  } else {
+    tm_d = tm_s;  // unused
   }
 
   wq::GemmParams p{};
@@ -223,14 +266,19 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.aug_stages = plan.kaug / 128;
   p.kaug = plan.kaug;
   p.S = static_cast<const __half*>(S);
-  p.delta = plan.kaug ? delta : nullptr;
+  p.delta = (variant == WQ_VARIANT_W4A16) ? delta : nullptr;
+  p.delta_aug = plan.kaug ? daug : nullptr;
   p.x_scale = x_scale;
   p.Y = Y;
   p.y_kind = y_kind;
   p.partials = reinterpret_cast<float*>(wsb + plan.off_part);
   p.counters = reinterpret_cast<int*>(wsb);
   p.timeout_ns = timeout_ns();
-  e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_w, tm_aug, p, st);
+  if (plan.gemv) {
+    e = wq::launch_gemv(x_kind, tm_x, tm_w, tm_s, tm_d, p, st);
+  } else {
+    e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_w, tm_aug, tm_s, p, st);
+  }
   return after_launch(e, name, st);
 }
 
@@ -351,8 +399,8 @@ int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const voi
   if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: bad y_dtype %d", y_dtype);
   if (M == 0) return WQ_OK;
   if (!X || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: null pointer");
-  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y))
-    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: X, Bpacked and Y must be 16-byte aligned");
+  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S) || (delta && !aligned16(delta)))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16: X, Bpacked, S, delta and Y must be 16-byte aligned");
   if ((rc = check_device())) return rc;
   const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
   return gemm_core(X, x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16, Bpacked, S, delta, nullptr, Y, yk, M, N,
@@ -372,8 +420,8 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
   if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: bad y_dtype %d", y_dtype);
   if (M == 0) return WQ_OK;
   if (!Xq || !x_scale || !Bpacked || !S_abs || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: null pointer");
-  if (!aligned16(Xq) || !aligned16(Bpacked) || !aligned16(Y))
-    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: Xq, Bpacked and Y must be 16-byte aligned");
+  if (!aligned16(Xq) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S_abs))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8: Xq, Bpacked, S_abs and Y must be 16-byte aligned");
   if ((rc = check_device())) return rc;
   return gemm_core(Xq, wq::kXF16, Bpacked, S_abs, nullptr, x_scale, Y, yk, M, N, K, gs, WQ_VARIANT_W4A8,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "wq_gemm_w4a8");

@@ -49,9 +49,11 @@ struct Cfg {
   static constexpr int kNSA = (BT <= 32) ? 3 : 4;                     // TMEM A-stages (64 cols each)
   static constexpr int kDCol = (BT <= 32) ? 192 : 256;                // accumulator columns
   static constexpr int kTmemCols = (BT <= 32) ? 256 : 512;
+  static constexpr int kSStageBytes = kTileN * 2;                     // scale row, fp16
   static constexpr int kNumBars = 2 * kNSX + 2 * kNSA + 1;
-  static constexpr int kSmemBytes =
-      1024 /*align slack*/ + kNSX * (kXStageBytes + kWStageBytes) + kNumBars * 8 + 16;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ +
+                                    kNSX * (kXStageBytes + kWStageBytes + kSStageBytes) +
+                                    kNumBars * 8 + 16;
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N for M=128 is 16..256, step 16");
   static_assert(kDCol + BT <= kTmemCols, "TMEM budget");
   static_assert(kNSA * 64 <= kDCol, "TMEM budget");
@@ -68,27 +70,11 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
   return __all_sync(0xffffffffu, ok);
 }
 
-template <int YK>
-__device__ __forceinline__ void store_y(void* Y, size_t idx, float v) {
-  if (YK == kYF16) {
-    reinterpret_cast<__half*>(Y)[idx] = __float2half_rn(v);
-  } else if (YK == kYBF16) {
-    reinterpret_cast<__nv_bfloat16*>(Y)[idx] = __float2bfloat16_rn(v);
-  } else {
-    reinterpret_cast<float*>(Y)[idx] = v;
-  }
-}
-
-__device__ __forceinline__ void store_y_dyn(void* Y, int yk, size_t idx, float v) {
-  if (yk == kYF16) store_y<kYF16>(Y, idx, v);
-  else if (yk == kYBF16) store_y<kYBF16>(Y, idx, v);
-  else store_y<kYF32>(Y, idx, v);
-}
-
 template <int BT, int XK>
 __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_aug, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tm_aug, const __grid_constant__ CUtensorMap tm_s,
+                const GemmParams p) {
   using C = Cfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -96,7 +82,8 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   uint8_t* const gbase = smem_raw + (base - raw);
   const uint32_t sx = base;
   const uint32_t sw = sx + C::kNSX * C::kXStageBytes;
-  const uint32_t sbar = sw + C::kNSX * C::kWStageBytes;
+  const uint32_t ss = sw + C::kNSX * C::kWStageBytes;
+  const uint32_t sbar = ss + C::kNSX * C::kSStageBytes;
   auto full_x = [&](int s) { return sbar + 8u * s; };
   auto empty_x = [&](int s) { return sbar + 8u * (C::kNSX + s); };
   auto full_a = [&](int a) { return sbar + 8u * (2 * C::kNSX + a); };
@@ -135,6 +122,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_w);
+    prefetch_tensormap(&tm_s);
     if (p.aug_stages > 0) prefetch_tensormap(&tm_aug);
   }
   if (warp == 1) {
@@ -146,11 +134,11 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  int issued = 0;  // TMA stages the producer lane has issued
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, &g_status};
-      int issued = 0;
       for (int it = 0; it < n_stages; ++it) {
         const int s = it % C::kNSX;
         const uint32_t ph = (it / C::kNSX) & 1;
@@ -162,19 +150,13 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
           tma_load_2d(xdst + C::kXAtomBytes, &tm_aug, full_x(s), it * kKBlock + 64, m0);
         } else {
           const int kb = kb0 + (it - n_aug);
-          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes);
+          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes + C::kSStageBytes);
           tma_load_2d(xdst, &tm_x, full_x(s), kb * kKBlock, m0);
           tma_load_2d(xdst + C::kXAtomBytes, &tm_x, full_x(s), kb * kKBlock + 64, m0);
           tma_load_2d(sw + s * C::kWStageBytes, &tm_w, full_x(s), kb * kWordsPerKBlock, n0);
+          tma_load_2d(ss + s * C::kSStageBytes, &tm_s, full_x(s), n0, (kb * kKBlock) / p.group_size);
         }
         issued = it + 1;
-      }
-      if (*abort_flag) {
-        // Drain: let every copy this thread issued land before the CTA exits.
-        volatile int never = 0;
-        const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, &g_status};
-        for (int it = max(0, issued - C::kNSX); it < issued; ++it)
-          mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
       }
     }
   } else if (warp == 1) {
@@ -220,25 +202,18 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       const uint32_t pha = (it / C::kNSA) & 1;
       const uint32_t a_tmem = tmem + lane_base + a * 64;
       if (it < n_aug) {
-        // weight-side correction columns: [d_hi | d_hi | d_lo], zero padded
+        // weight-side correction columns [d_hi | d_hi | d_lo | 0...] of this row,
+        // prepared per call in the workspace: 128 bf16 = 64 columns, 16 vector loads.
         uint32_t v[64];
-        const int G = p.G;
-#pragma unroll 4
-        for (int i = 0; i < 64; ++i) {
-          __nv_bfloat16 e[2];
+        const uint4* src = reinterpret_cast<const uint4*>(
+            p.delta_aug + static_cast<size_t>(n) * p.kaug + it * kKBlock);
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int j = it * kKBlock + 2 * i + h;
-            e[h] = __float2bfloat16_rn(0.0f);
-            if (j < 3 * G) {
-              const int t = j / G;
-              const int g = j - t * G;
-              __nv_bfloat16 hi, lo;
-              split_bf16(__ldg(p.delta + static_cast<size_t>(g) * p.N + n), hi, lo);
-              e[h] = (t == 2) ? lo : hi;
-            }
-          }
-          v[i] = pack_bf16x2(e[0], e[1]);
+        for (int i = 0; i < 16; ++i) {
+          const uint4 t = __ldg(src + i);
+          v[4 * i + 0] = t.x;
+          v[4 * i + 1] = t.y;
+          v[4 * i + 2] = t.z;
+          v[4 * i + 3] = t.w;
         }
         if (!warp_wait(full_x(s), ph, wc)) break;
         if (lane == 0) mbar_arrive(empty_x(s));
@@ -246,10 +221,8 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
         tmem_st32(a_tmem, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_st32(a_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       } else {
-        const int kb = kb0 + (it - n_aug);
-        const int g = (kb * kKBlock) / p.group_size;
-        const __half sc = p.S[static_cast<size_t>(g) * p.N + n];
         if (!warp_wait(full_x(s), ph, wc)) break;
+        const __half sc = reinterpret_cast<const __half*>(gbase + (ss - base))[s * kTileN + row];
         uint4 wv[4];
         const uint8_t* wrow = wring + s * C::kWStageBytes + row * 64;
 #pragma unroll
@@ -320,7 +293,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
             float val = __uint_as_float(r[j]);
             if (p.x_scale) val *= __ldg(p.x_scale + m);
             if (direct) {
-              store_y_dyn(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
+              store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
             } else {
               p.partials[(static_cast<size_t>(seg) * p.M + m) * p.N + n] = val;
             }
@@ -343,7 +316,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
             float acc = 0.0f;
             for (int sg = 0; sg < p.splits; ++sg)
               acc += __ldcg(p.partials + (static_cast<size_t>(sg) * p.M + m) * p.N + n);
-            store_y_dyn(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
+            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
           }
           if (threadIdx.x == 64) p.counters[tile] = 0;
         }
@@ -352,6 +325,14 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     tc_fence_before();
   }
 
+  __syncthreads();
+  if (*abort_flag && warp == 0 && lane == 0) {
+    // Let every copy the producer issued land before the CTA exits.
+    volatile int never = 0;
+    const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, &g_status};
+    for (int it = max(0, issued - C::kNSX); it < issued; ++it)
+      mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
+  }
   __syncthreads();
   if (warp == 1) {
     // Every MMA this CTA issued has completed once the final commit arrived.
@@ -366,7 +347,8 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
 
 template <int BT, int XK>
 static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t st) {
+                             const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
+                             cudaStream_t st) {
   using C = Cfg<BT>;
   static unsigned long long attr_mask = 0;  // one bit per device that has the attribute set
   int dev = 0;
@@ -380,27 +362,41 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
     attr_mask |= bit;
   }
   dim3 grid(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
-  gemm_kernel<BT, XK><<<grid, 192, C::kSmemBytes, st>>>(tm_x, tm_w, tm_aug, p);
+  gemm_kernel<BT, XK><<<grid, 192, C::kSmemBytes, st>>>(tm_x, tm_w, tm_aug, tm_s, p);
   return cudaGetLastError();
 }
 
 template <int XK>
 static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t st) {
+                             const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
+                             cudaStream_t st) {
   switch (bt) {
-    case 16: return launch_bt<16, XK>(tm_x, tm_w, tm_aug, p, st);
-    case 32: return launch_bt<32, XK>(tm_x, tm_w, tm_aug, p, st);
-    case 64: return launch_bt<64, XK>(tm_x, tm_w, tm_aug, p, st);
-    case 128: return launch_bt<128, XK>(tm_x, tm_w, tm_aug, p, st);
-    case 256: return launch_bt<256, XK>(tm_x, tm_w, tm_aug, p, st);
+    case 32: return launch_bt<32, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
+    case 64: return launch_bt<64, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
+    case 128: return launch_bt<128, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
+    case 256: return launch_bt<256, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t stream) {
-  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_w, tm_aug, p, stream)
-                          : launch_xk<kXF16>(bt, tm_x, tm_w, tm_aug, p, stream);
+                        const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
+                        cudaStream_t stream) {
+  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_w, tm_aug, tm_s, p, stream)
+                          : launch_xk<kXF16>(bt, tm_x, tm_w, tm_aug, tm_s, p, stream);
+}
+
+// Device address of the status word (host side), looked up once per device.
+unsigned* status_word() {
+  static unsigned* addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<unsigned*>(ptr);
+  }
+  return addr[dev];
 }
 
 // ---------------------------------------------------------------------------
@@ -436,7 +432,6 @@ cudaError_t clear_status() {
 
 size_t gemm_smem_bytes(int bt) {
   switch (bt) {
-    case 16: return Cfg<16>::kSmemBytes;
     case 32: return Cfg<32>::kSmemBytes;
     case 64: return Cfg<64>::kSmemBytes;
     case 128: return Cfg<128>::kSmemBytes;

@@ -26,6 +26,7 @@ constexpr unsigned kDevTimeoutProbe = 1u << 4;
 enum XKind { kXF16 = 0, kXBF16 = 1 };
 enum YKind { kYF16 = 0, kYBF16 = 1, kYF32 = 2 };
 
+
 struct GemmParams {
   int M, N, K;
   int group_size;        // K for one group per column
@@ -37,6 +38,7 @@ struct GemmParams {
   int kaug;              // padded correction length (multiple of 128)
   const __half* S;       // [G][N] group scales
   const float* delta;    // [G][N] zero-point residual, or null
+  const __nv_bfloat16* delta_aug;  // [N][kaug] correction columns (large-M kernel)
   const float* x_scale;  // [M] per-token activation scale (W4A8), or null
   void* Y;               // [M][N]
   int y_kind;
@@ -45,14 +47,22 @@ struct GemmParams {
   unsigned long long timeout_ns;
 };
 
-// Host-side launchers (wq_gemm.cu).
+// Host-side launchers (wq_gemm.cu, wq_gemv.cu).
+cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
+                        const CUtensorMap& tm_s, const CUtensorMap& tm_d, const GemmParams& p,
+                        cudaStream_t stream);
+int gemv_max_splits();
+unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_aug, const GemmParams& p, cudaStream_t stream);
+                        const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
+                        cudaStream_t stream);
 size_t gemm_smem_bytes(int bt);
 
 // Pre-pass kernels (wq_kernels.cu).
 cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
                             int kaug, __nv_bfloat16* aug, cudaStream_t stream);
+cudaError_t launch_delta_aug(const float* delta, int G, int N, int kaug, __nv_bfloat16* delta_aug,
+                             cudaStream_t stream);
 cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t stream);
 cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
                         uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,

@@ -191,6 +191,34 @@ __global__ void aug_prep_kernel(const void* __restrict__ X, int K, int group_siz
   for (int j = 3 * G + threadIdx.x; j < kaug; j += blockDim.x) arow[j] = __float2bfloat16_rn(0.0f);
 }
 
+// Weight-side correction columns: delta_aug[n][j] = [d_hi | d_hi | d_lo | 0...]
+// (j over 3G, padded to kaug) with d_hi = bf16_RN(delta), d_lo = bf16_RN(delta -
+// d_hi).  A block handles 128 columns n and 128 j at a time through shared
+// memory so that the global writes are row-contiguous.
+__global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, int kaug,
+                                 __nv_bfloat16* __restrict__ out) {
+  __shared__ uint16_t tile[128][130];
+  const int nb = blockIdx.x * 128;
+  const int j0 = blockIdx.y * 128;
+  const int t = threadIdx.x;  // 0..127
+  for (int jj = 0; jj < 128; ++jj) {
+    const int j = j0 + jj;
+    uint16_t val = 0;
+    if (j < 3 * G) {
+      const int term = j / G;
+      const int g = j - term * G;
+      __nv_bfloat16 hi, lo;
+      split_bf16(delta[static_cast<size_t>(g) * N + nb + t], hi, lo);
+      val = __bfloat16_as_ushort(term == 2 ? lo : hi);
+    }
+    tile[t][jj] = val;  // coalesced read of delta row g across t
+  }
+  __syncthreads();
+  for (int r = 0; r < 128; ++r) {
+    reinterpret_cast<uint16_t*>(out)[static_cast<size_t>(nb + r) * kaug + j0 + t] = tile[r][t];
+  }
+}
+
 __global__ void i8_to_f16_kernel(const int8_t* __restrict__ Xq, __half* __restrict__ X16,
                                  long long count) {
   const long long i = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) * 4;
@@ -247,6 +275,13 @@ cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_s
   } else {
     aug_prep_kernel<kXF16><<<M, 128, 0, st>>>(X, K, group_size, G, kaug, aug);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_delta_aug(const float* delta, int G, int N, int kaug, __nv_bfloat16* delta_aug,
+                             cudaStream_t st) {
+  dim3 grid(N / 128, kaug / 128);
+  delta_aug_kernel<<<grid, 128, 0, st>>>(delta, G, N, kaug, delta_aug);
   return cudaGetLastError();
 }
 
