@@ -115,10 +115,10 @@ int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, 
  *   delta    [G][N] fp32 device, or NULL for symmetric weights (no correction).
  *   Y        [M][N] device, output, overwritten (y_dtype F16, BF16 or F32).
  *   workspace / workspace_bytes: device scratch of at least
- *            wq_workspace_size(variant, M, N, K, group_size) bytes.  Its first
- *            4096 bytes hold split-K tile counters that must be zero before the
- *            first call that uses this workspace; every call leaves them zero.
- *            Calls that run concurrently must use different workspaces.
+ *            wq_workspace_size(variant, M, N, K, group_size) bytes (may be NULL
+ *            when that is 0; it is 0 for W4A16 with M <= 16).  No
+ *            initialization is needed.  Calls that may run concurrently must
+ *            use different workspaces.
  * Accumulation is fp32.  The weights are dequantized as RN((q-8)*scale) in
  * the activation type; the correction is added in the same accumulator.
  */

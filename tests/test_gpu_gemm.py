@@ -215,7 +215,7 @@ def test_w4a8_gpu_quantizer_end_to_end(wq):
 
 
 def test_empty_and_error_paths(wq):
-    d = synth.make_inputs(960, 4, 256, 256)
+    d = synth.make_inputs(960, 64, 256, 256)
     Y, (Bp, S, dl) = _w4a16(wq, d)
     X0 = torch.empty((0, 256), dtype=torch.float16, device="cuda")
     assert wq.gemm_w4a16(X0, Bp, S, dl, 128).shape == (0, 256)

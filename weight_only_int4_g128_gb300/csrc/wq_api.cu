@@ -152,12 +152,11 @@ struct Plan {
   int splits;
   int kb_per_split;
   int kaug;       // large-M correction length (0 without correction or for the decode kernel)
-  size_t off_aug, off_daug, off_x16, off_part;  // byte offsets into the workspace
+  size_t off_aug, off_daug, off_x16;  // byte offsets into the workspace
   size_t bytes;
 };
 
-constexpr size_t kCounterBytes = 4096;  // split-K tile counters at the start of the workspace
-constexpr int kMaxCounters = static_cast<int>(kCounterBytes / 4);
+constexpr int kMaxClusterSplits = 8;  // K segments of one tile form a portable cluster
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
@@ -172,30 +171,23 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   const int tiles = ntiles * mtiles;
   // CTA slots per wave: the decode kernel and the 16/32-token tiles fit two per SM.
   const int slots = (p.bt <= 32) ? 2 * wq::kNumSMs : wq::kNumSMs;
-  int splits = 1;
-  if (p.gemv) {
-    // K segments of a column tile form one thread-block cluster (<= 8 CTAs)
-    splits = slots / tiles;
-    if (splits < 1) splits = 1;
-    if (splits > wq::gemv_max_splits()) splits = wq::gemv_max_splits();
-    if (splits > kb) splits = kb;
-  } else if (tiles < slots && tiles <= kMaxCounters) {
-    splits = slots / tiles;  // as many K segments as still fit in one wave
-    if (splits < 1) splits = 1;
-    if (splits > kb) splits = kb;
-  }
+  // As many K segments as still fit in one wave; the segments of a tile form
+  // one thread-block cluster and are reduced through distributed shared memory.
+  int splits = slots / tiles;
+  if (splits < 1) splits = 1;
+  const int max_splits = p.gemv ? wq::gemv_max_splits() : kMaxClusterSplits;
+  if (splits > max_splits) splits = max_splits;
+  if (splits > kb) splits = kb;
   p.kb_per_split = (kb + splits - 1) / splits;
   p.splits = (kb + p.kb_per_split - 1) / p.kb_per_split;
   p.kaug = (!p.gemv && variant == WQ_VARIANT_W4A16) ? ((3 * G + 127) / 128) * 128 : 0;
-  size_t off = kCounterBytes;
+  size_t off = 0;
   p.off_aug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(M) * p.kaug * 2);
   p.off_daug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
   p.off_x16 = off;
   if (variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(M) * K * 2);
-  p.off_part = off;
-  if (p.splits > 1 && !p.gemv) off = align256(off + static_cast<size_t>(p.splits) * M * N * 4);
   p.bytes = off;
   return p;
 }
@@ -205,9 +197,9 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
               const float* x_scale, void* Y, int y_kind, int M, int N, int K, int gs, int variant,
               void* ws, size_t ws_bytes, cudaStream_t st, const char* name) {
   const Plan plan = make_plan(variant, M, N, K, gs);
-  if (!ws || ws_bytes < plan.bytes)
+  if (plan.bytes > 0 && (!ws || ws_bytes < plan.bytes))
     return fail(WQ_ERR_WORKSPACE, "%s: workspace of %zu bytes given, %zu needed", name, ws_bytes, plan.bytes);
-  if (!aligned16(ws)) return fail(WQ_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
+  if (ws && !aligned16(ws)) return fail(WQ_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   const int G = K / gs;
   cudaError_t e;
@@ -231,15 +223,13 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   CUtensorMap tm_x, tm_w, tm_aug, tm_s, tm_d;
   const CUtensorMapDataType xdt =
       x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  int rc = plan.gemv ? make_map_x3d(&tm_x, xdt, xg, M, K, plan.bt)
-                     : make_map(&tm_x, xdt, 2, xg, M, K, plan.bt, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  int rc = make_map_x3d(&tm_x, xdt, xg, M, K, plan.bt);
   if (rc) return rc;
   rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Bpacked, N, K / 8, 128, 16,
                 CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
   if (plan.kaug) {
-    rc = make_map(&tm_aug, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, aug, M, plan.kaug, plan.bt, 64,
-                  CU_TENSOR_MAP_SWIZZLE_128B);
+    rc = make_map_x3d(&tm_aug, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, aug, M, plan.kaug, plan.bt);
     if (rc) return rc;
   } else {
     tm_aug = tm_x;  // unused
@@ -271,8 +261,6 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.x_scale = x_scale;
   p.Y = Y;
   p.y_kind = y_kind;
-  p.partials = reinterpret_cast<float*>(wsb + plan.off_part);
-  p.counters = reinterpret_cast<int*>(wsb);
   p.timeout_ns = timeout_ns();
   if (plan.gemv) {
     e = wq::launch_gemv(x_kind, tm_x, tm_w, tm_s, tm_d, p, st);

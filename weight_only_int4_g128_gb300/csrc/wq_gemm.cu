@@ -27,9 +27,9 @@
 // columns [d_hi | d_hi | d_lo] (delta split the same way).  Their bf16 MMAs add
 // a_hi*d_hi + a_lo*d_hi + a_hi*d_lo, which is a_sum*delta up to ~2^-16
 // relative.
-// Split-K: gridDim.z segments of k-blocks; each writes an fp32 partial and
-// the last CTA to arrive on a per-tile counter sums the partials in segment
-// order (deterministic) and writes Y.
+// Split-K: gridDim.z segments of k-blocks form a thread-block cluster; the
+// partials are reduced through distributed shared memory in rank order
+// (deterministic) and written to Y.
 //
 // Every wait is bounded; on expiry the CTA records a status bit, drains what
 // it issued, frees its TMEM and returns.
@@ -46,17 +46,22 @@ struct Cfg {
   static constexpr int kXAtomBytes = BT * 128;                        // one box of 64 k
   static constexpr int kWStageBytes = kTileN * kWordsPerKBlock * 4;  // 8 KB
   static constexpr int kNSX = (BT >= 256) ? 3 : (BT >= 128) ? 5 : (BT >= 64) ? 8 : (BT >= 32) ? 6 : 8;
-  static constexpr int kNSA = (BT <= 32) ? 3 : 4;                     // TMEM A-stages (64 cols each)
+  // TMEM A-stages (64 columns each); at most kNSX so that the per-stage
+  // mma_done barrier also tells when an A-stage is free again
+  static constexpr int kNSA = (BT <= 32) ? 3 : (kNSX < 4 ? kNSX : 4);
   static constexpr int kDCol = (BT <= 32) ? 192 : 256;                // accumulator columns
   static constexpr int kTmemCols = (BT <= 32) ? 256 : 512;
   static constexpr int kSStageBytes = kTileN * 2;                     // scale row, fp16
-  static constexpr int kNumBars = 2 * kNSX + 2 * kNSA + 1;
+  static constexpr int kNumBars = 3 * kNSX + kNSA + 1;
   static constexpr int kSmemBytes = 1024 /*align slack*/ +
                                     kNSX * (kXStageBytes + kWStageBytes + kSStageBytes) +
                                     kNumBars * 8 + 16;
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N for M=128 is 16..256, step 16");
   static_assert(kDCol + BT <= kTmemCols, "TMEM budget");
   static_assert(kNSA * 64 <= kDCol, "TMEM budget");
+  static_assert(kNSA <= kNSX, "mma_done is indexed by stage");
+  static_assert((BT + 8) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
+                "split-K reduction buffer reuses the stage ring");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -84,11 +89,15 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   const uint32_t sw = sx + C::kNSX * C::kXStageBytes;
   const uint32_t ss = sw + C::kNSX * C::kWStageBytes;
   const uint32_t sbar = ss + C::kNSX * C::kSStageBytes;
+  // full_x: TMA bytes of stage s landed; empty_x: the dequant warps have read
+  // it; mma_done: the k-block's MMAs completed (one tcgen05.commit per
+  // k-block; frees the activation tile and the TMEM A-stage); full_a: the
+  // A-stage holds dequantized weights.
   auto full_x = [&](int s) { return sbar + 8u * s; };
   auto empty_x = [&](int s) { return sbar + 8u * (C::kNSX + s); };
-  auto full_a = [&](int a) { return sbar + 8u * (2 * C::kNSX + a); };
-  auto empty_a = [&](int a) { return sbar + 8u * (2 * C::kNSX + C::kNSA + a); };
-  const uint32_t done_bar = sbar + 8u * (2 * C::kNSX + 2 * C::kNSA);
+  auto mma_done = [&](int s) { return sbar + 8u * (2 * C::kNSX + s); };
+  auto full_a = [&](int a) { return sbar + 8u * (3 * C::kNSX + a); };
+  const uint32_t done_bar = sbar + 8u * (3 * C::kNSX + C::kNSA);
   const uint32_t misc = sbar + 8u * C::kNumBars;
   uint8_t* const gmisc = gbase + (misc - base);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gmisc);
@@ -108,11 +117,11 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kNSX; ++s) {
       mbar_init(full_x(s), 1);
-      mbar_init(empty_x(s), 1 + 4);  // MMA commit + one arrive per dequant warp
+      mbar_init(empty_x(s), 4);  // one arrive per dequant warp
+      mbar_init(mma_done(s), 1);
     }
     for (int a = 0; a < C::kNSA; ++a) {
       mbar_init(full_a(a), 4);
-      mbar_init(empty_a(a), 1);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -143,16 +152,16 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
         const int s = it % C::kNSX;
         const uint32_t ph = (it / C::kNSX) & 1;
         if (!mbar_wait(empty_x(s), ph ^ 1, wc)) break;
+        if (!mbar_wait(mma_done(s), ph ^ 1, wc)) break;
         const uint32_t xdst = sx + s * C::kXStageBytes;
+        // activation tile [BT x 128 k]: one 3-D box {64 k, BT rows, 2 halves}
         if (it < n_aug) {
           mbar_arrive_expect_tx(full_x(s), C::kXStageBytes);
-          tma_load_2d(xdst, &tm_aug, full_x(s), it * kKBlock, m0);
-          tma_load_2d(xdst + C::kXAtomBytes, &tm_aug, full_x(s), it * kKBlock + 64, m0);
+          tma_load_3d(xdst, &tm_aug, full_x(s), 0, m0, 2 * it);
         } else {
           const int kb = kb0 + (it - n_aug);
           mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes + C::kSStageBytes);
-          tma_load_2d(xdst, &tm_x, full_x(s), kb * kKBlock, m0);
-          tma_load_2d(xdst + C::kXAtomBytes, &tm_x, full_x(s), kb * kKBlock + 64, m0);
+          tma_load_3d(xdst, &tm_x, full_x(s), 0, m0, 2 * kb);
           tma_load_2d(sw + s * C::kWStageBytes, &tm_w, full_x(s), kb * kWordsPerKBlock, n0);
           tma_load_2d(ss + s * C::kSStageBytes, &tm_s, full_x(s), n0, (kb * kKBlock) / p.group_size);
         }
@@ -164,25 +173,23 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMma, &g_status};
       const uint32_t d_tmem = tmem + C::kDCol;
-      const uint32_t id_x = idesc_f16(XK, 128, BT);
-      const uint32_t id_aug = idesc_f16(1, 128, BT);
+      constexpr uint32_t id_x = idesc_f16(XK, 128, BT);
+      constexpr uint32_t id_aug = idesc_f16(1, 128, BT);
+      const uint64_t desc0 = desc_kmajor_sw128(sx);
       for (int it = 0; it < n_stages; ++it) {
         const int s = it % C::kNSX;
-        const uint32_t ph = (it / C::kNSX) & 1;
         const int a = it % C::kNSA;
-        const uint32_t pha = (it / C::kNSA) & 1;
-        if (!mbar_wait(full_x(s), ph, wc)) break;
-        if (!mbar_wait(full_a(a), pha, wc)) break;
+        // full_a implies the stage's TMA bytes landed: the dequant warps waited on full_x
+        if (!mbar_wait(full_a(a), (it / C::kNSA) & 1, wc)) break;
         tc_fence_after();
-        const uint32_t xs = sx + s * C::kXStageBytes;
+        const uint64_t ds = desc0 + static_cast<uint64_t>((s * C::kXStageBytes) >> 4);
         const uint32_t id = (it < n_aug) ? id_aug : id_x;
+        const uint32_t at = tmem + a * 64;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint64_t bd = desc_kmajor_sw128(xs + (i >> 2) * C::kXAtomBytes + (i & 3) * 32);
-          mma_ts(d_tmem, tmem + a * 64 + i * 8, bd, id, (it > 0 || i > 0) ? 1u : 0u);
-        }
-        mma_commit(empty_x(s));
-        mma_commit(empty_a(a));
+        for (int i = 0; i < 8; ++i)
+          mma_ts(d_tmem, at + i * 8, ds + (((i >> 2) * C::kXAtomBytes + (i & 3) * 32) >> 4), id,
+                 (it > 0 || i > 0) ? 1u : 0u);
+        mma_commit(mma_done(s));
       }
       mma_commit(done_bar);
     }
@@ -199,7 +206,6 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       const int s = it % C::kNSX;
       const uint32_t ph = (it / C::kNSX) & 1;
       const int a = it % C::kNSA;
-      const uint32_t pha = (it / C::kNSA) & 1;
       const uint32_t a_tmem = tmem + lane_base + a * 64;
       if (it < n_aug) {
         // weight-side correction columns [d_hi | d_hi | d_lo | 0...] of this row,
@@ -217,7 +223,11 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
         }
         if (!warp_wait(full_x(s), ph, wc)) break;
         if (lane == 0) mbar_arrive(empty_x(s));
-        if (!warp_wait(empty_a(a), pha ^ 1, wc)) break;
+        if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
+          const int pk = it - C::kNSA;
+          if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
+          tc_fence_after();
+        }
         tmem_st32(a_tmem, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
         tmem_st32(a_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       } else {
@@ -261,7 +271,11 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
             }
           }
         }
-        if (!warp_wait(empty_a(a), pha ^ 1, wc)) break;
+        if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
+          const int pk = it - C::kNSA;
+          if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
+          tc_fence_after();
+        }
         tmem_st32(a_tmem, v0);
         tmem_st32(a_tmem + 32, v1);
       }
@@ -271,14 +285,12 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       if (lane == 0) mbar_arrive(full_a(a));
     }
 
-    // ---- epilogue: accumulator -> Y (or fp32 partial)
+    // ---- epilogue (single K segment): accumulator -> Y
     warp_wait(done_bar, 0, wc);
     named_bar_sync(1, 128);
-    const bool ok = !*abort_flag;  // uniform: no wait can set the flag past this point
     tc_fence_after();
-    if (ok) {
+    if (!*abort_flag && p.splits == 1) {  // uniform: no wait can set the flag past this point
       const uint32_t dt = tmem + lane_base + C::kDCol;
-      const bool direct = (p.splits == 1);
       const int mlim = min(BT, p.M - m0);
       for (int c = 0; c < BT / 16; ++c) {
         if (16 * c >= mlim) break;
@@ -292,33 +304,8 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
             const int m = m0 + ml;
             float val = __uint_as_float(r[j]);
             if (p.x_scale) val *= __ldg(p.x_scale + m);
-            if (direct) {
-              store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
-            } else {
-              p.partials[(static_cast<size_t>(seg) * p.M + m) * p.N + n] = val;
-            }
+            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
           }
-        }
-      }
-      if (!direct) {
-        __threadfence();
-        named_bar_sync(1, 128);
-        const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-        if (threadIdx.x == 64) {
-          const int old = atomicAdd(p.counters + tile, 1);
-          *last_flag = (old == p.splits - 1) ? 1 : 0;
-        }
-        named_bar_sync(1, 128);
-        if (*last_flag) {
-          __threadfence();
-          for (int ml = 0; ml < mlim; ++ml) {
-            const int m = m0 + ml;
-            float acc = 0.0f;
-            for (int sg = 0; sg < p.splits; ++sg)
-              acc += __ldcg(p.partials + (static_cast<size_t>(sg) * p.M + m) * p.N + n);
-            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
-          }
-          if (threadIdx.x == 64) p.counters[tile] = 0;
         }
       }
     }
@@ -334,6 +321,59 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
   }
   __syncthreads();
+
+  // ---- split-K over a thread-block cluster (the K segments of one output tile).
+  // Every CTA pushes its fp32 partial rows into the shared memory of the rank
+  // that owns them (rows [r*rpr, (r+1)*rpr) belong to rank r); the owner sums
+  // the partials in rank order (deterministic) and writes Y.
+  if (p.splits > 1) {
+    const int splits = p.splits;
+    const int rpr = (BT + splits - 1) / splits;
+    const int mlim = min(BT, p.M - m0);
+    const bool math = warp >= 2;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int n = n0 + row;
+    float* const red = reinterpret_cast<float*>(gbase);  // [splits][rpr][128], over the ring
+    cluster_sync_all();  // every CTA of the cluster is past its mainloop: rings are free
+    if (math) {
+      tc_fence_after();
+      const bool aborted = *abort_flag != 0;
+      const uint32_t dt = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDCol;
+      const uint32_t red_base = smem_u32(red);
+      for (int c = 0; c < BT / 16; ++c) {
+        if (16 * c >= mlim) break;
+        uint32_t r[16];
+        tmem_ld16(dt + 16 * c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int ml = 16 * c + j;
+          if (ml < mlim) {
+            const int owner = ml / rpr;
+            const int local = ml - owner * rpr;
+            const uint32_t addr =
+                red_base + static_cast<uint32_t>(((seg * rpr + local) * kTileN + row) * 4);
+            st_dsmem_f32(mapa_shared(addr, owner), aborted ? __int_as_float(0x7fc00000) : __uint_as_float(r[j]));
+          }
+        }
+      }
+      tc_fence_before();
+    }
+    cluster_sync_all();  // all pushes landed
+    if (math) {
+      const int hi = min(mlim, (seg + 1) * rpr);
+      for (int ml = seg * rpr; ml < hi; ++ml) {
+        const int local = ml - seg * rpr;
+        float acc = 0.0f;
+        for (int src = 0; src < splits; ++src) acc += red[(src * rpr + local) * kTileN + row];
+        const int m = m0 + ml;
+        if (p.x_scale) acc *= __ldg(p.x_scale + m);
+        store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
+      }
+    }
+  }
+
   if (warp == 1) {
     // Every MMA this CTA issued has completed once the final commit arrived.
     volatile int never = 0;
@@ -361,9 +401,19 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
     if (e != cudaSuccess) return e;
     attr_mask |= bit;
   }
-  dim3 grid(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
-  gemm_kernel<BT, XK><<<grid, 192, C::kSmemBytes, st>>>(tm_x, tm_w, tm_aug, tm_s, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;  // the K segments of a tile form a cluster
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = p.splits;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_w, tm_aug, tm_s, p);
 }
 
 template <int XK>

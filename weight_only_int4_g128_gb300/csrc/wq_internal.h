@@ -33,7 +33,7 @@ struct GemmParams {
   int G;                 // number of groups
   int kb_total;          // K / 128
   int kb_per_split;      // k-blocks per split segment
-  int splits;            // number of K segments (gridDim.z)
+  int splits;            // number of K segments (one thread-block cluster per tile)
   int aug_stages;        // correction stages (Kaug / 128), 0 when there is no correction
   int kaug;              // padded correction length (multiple of 128)
   const __half* S;       // [G][N] group scales
@@ -42,8 +42,6 @@ struct GemmParams {
   const float* x_scale;  // [M] per-token activation scale (W4A8), or null
   void* Y;               // [M][N]
   int y_kind;
-  float* partials;       // [splits][M][N] fp32 (split-K only)
-  int* counters;         // one per output tile (split-K only)
   unsigned long long timeout_ns;
 };
 

@@ -148,74 +148,121 @@ __global__ void quantize_per_token_kernel(const __half* __restrict__ x, int8_t* 
 // Correction pre-pass: a_sum[m][g] = sum_{k in g} X[m][k] in fp32 ("Marlin
 // INT4 on Ada", section "The core mismatch"), written as the activation-side
 // correction columns aug[m][0..kaug) = [a_hi | a_lo | a_hi | 0...] in bf16.
-// One block per row m; warp w sums groups w, w+4, ...
+// Groups of <= 1024 elements: one thread per (m, g), 16-byte loads issued
+// back to back.  Longer groups (one group per column): one warp per (m, g).
 // ---------------------------------------------------------------------------
 template <int XK>
-__global__ void aug_prep_kernel(const void* __restrict__ X, int K, int group_size, int G, int kaug,
-                                __nv_bfloat16* __restrict__ aug) {
-  const int m = blockIdx.x;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const uint16_t* row = reinterpret_cast<const uint16_t*>(X) + static_cast<size_t>(m) * K;
-  __nv_bfloat16* arow = aug + static_cast<size_t>(m) * kaug;
-  for (int g = warp; g < G; g += blockDim.x >> 5) {
-    float acc = 0.0f;
-    const uint16_t* gp = row + static_cast<size_t>(g) * group_size;
-    for (int k = lane * 8; k < group_size; k += 256) {
-      const uint4 v = *reinterpret_cast<const uint4*>(gp + k);
-      const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+__device__ __forceinline__ float sum8(const uint4 v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float acc = 0.0f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        float lo, hi;
-        if (XK == kXF16) {
-          lo = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu)));
-          hi = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
-        } else {
-          lo = __uint_as_float(u[i] << 16);
-          hi = __uint_as_float(u[i] & 0xFFFF0000u);
-        }
-        acc += lo;
-        acc += hi;
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      __nv_bfloat16 h, l;
-      split_bf16(acc, h, l);
-      arow[g] = h;
-      arow[G + g] = l;
-      arow[2 * G + g] = h;
+  for (int i = 0; i < 4; ++i) {
+    if (XK == kXF16) {
+      acc += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu)));
+      acc += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
+    } else {
+      acc += __uint_as_float(u[i] << 16);
+      acc += __uint_as_float(u[i] & 0xFFFF0000u);
     }
   }
-  for (int j = 3 * G + threadIdx.x; j < kaug; j += blockDim.x) arow[j] = __float2bfloat16_rn(0.0f);
+  return acc;
+}
+
+__device__ __forceinline__ void write_aug(__nv_bfloat16* arow, int G, int g, float a) {
+  __nv_bfloat16 h, l;
+  split_bf16(a, h, l);
+  arow[g] = h;
+  arow[G + g] = l;
+  arow[2 * G + g] = h;
+}
+
+template <int XK>
+__global__ void aug_prep_kernel(const void* __restrict__ X, int M, int K, int group_size, int G,
+                                int kaug, __nv_bfloat16* __restrict__ aug) {
+  const uint16_t* Xh = reinterpret_cast<const uint16_t*>(X);
+  if (group_size <= 1024) {
+    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+    if (idx >= static_cast<long long>(M) * G) return;
+    const int m = static_cast<int>(idx / G);
+    const int g = static_cast<int>(idx - static_cast<long long>(m) * G);
+    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * K +
+                                                     static_cast<size_t>(g) * group_size);
+    float acc = 0.0f;
+    const int nv = group_size / 8;
+#pragma unroll 16
+    for (int i = 0; i < nv; ++i) acc += sum8<XK>(__ldg(gp + i));
+    write_aug(aug + static_cast<size_t>(m) * kaug, G, g, acc);
+  } else {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (warp >= M * G) return;
+    const int m = warp / G;
+    const int g = warp - m * G;
+    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * K +
+                                                     static_cast<size_t>(g) * group_size);
+    float acc = 0.0f;
+    const int nv = group_size / 8;
+#pragma unroll 8
+    for (int i = lane; i < nv; i += 32) acc += sum8<XK>(__ldg(gp + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) write_aug(aug + static_cast<size_t>(m) * kaug, G, g, acc);
+  }
+}
+
+// Zero the padding columns [3G, kaug) of every aug row.
+__global__ void aug_pad_kernel(int M, int G, int kaug, __nv_bfloat16* __restrict__ aug) {
+  const int pad = kaug - 3 * G;
+  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<long long>(M) * pad) return;
+  const int m = static_cast<int>(idx / pad);
+  const int j = 3 * G + static_cast<int>(idx - static_cast<long long>(m) * pad);
+  aug[static_cast<size_t>(m) * kaug + j] = __float2bfloat16_rn(0.0f);
 }
 
 // Weight-side correction columns: delta_aug[n][j] = [d_hi | d_hi | d_lo | 0...]
 // (j over 3G, padded to kaug) with d_hi = bf16_RN(delta), d_lo = bf16_RN(delta -
-// d_hi).  A block handles 128 columns n and 128 j at a time through shared
-// memory so that the global writes are row-contiguous.
+// d_hi).  A tiled transpose: a 32 (g) x 32 (n) tile of delta is read with
+// coalesced rows, split in shared memory, and written as 32 consecutive j of
+// each of the 32 rows n, three times (one per term).
 __global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, int kaug,
                                  __nv_bfloat16* __restrict__ out) {
-  __shared__ uint16_t tile[128][130];
-  const int nb = blockIdx.x * 128;
-  const int j0 = blockIdx.y * 128;
-  const int t = threadIdx.x;  // 0..127
-  for (int jj = 0; jj < 128; ++jj) {
-    const int j = j0 + jj;
-    uint16_t val = 0;
-    if (j < 3 * G) {
-      const int term = j / G;
-      const int g = j - term * G;
-      __nv_bfloat16 hi, lo;
-      split_bf16(delta[static_cast<size_t>(g) * N + nb + t], hi, lo);
-      val = __bfloat16_as_ushort(term == 2 ? lo : hi);
+  __shared__ uint16_t hi_t[32][33];
+  __shared__ uint16_t lo_t[32][33];
+  const int g0 = blockIdx.x * 32;
+  const int n0 = blockIdx.y * 32;
+  const int tx = threadIdx.x;  // 0..31
+  const int ty = threadIdx.y;  // 0..7
+  for (int r = ty; r < 32; r += 8) {
+    const int g = g0 + r;
+    uint16_t h = 0, l = 0;
+    if (g < G) {
+      __nv_bfloat16 bh, bl;
+      split_bf16(delta[static_cast<size_t>(g) * N + n0 + tx], bh, bl);
+      h = __bfloat16_as_ushort(bh);
+      l = __bfloat16_as_ushort(bl);
     }
-    tile[t][jj] = val;  // coalesced read of delta row g across t
+    hi_t[r][tx] = h;
+    lo_t[r][tx] = l;
   }
   __syncthreads();
-  for (int r = 0; r < 128; ++r) {
-    reinterpret_cast<uint16_t*>(out)[static_cast<size_t>(nb + r) * kaug + j0 + t] = tile[r][t];
+  uint16_t* o = reinterpret_cast<uint16_t*>(out);
+  for (int r = ty; r < 32; r += 8) {
+    const int n = n0 + r;
+    const int g = g0 + tx;
+    if (g < G) {
+      uint16_t* row = o + static_cast<size_t>(n) * kaug;
+      row[g] = hi_t[tx][r];
+      row[G + g] = hi_t[tx][r];
+      row[2 * G + g] = lo_t[tx][r];
+    }
+  }
+  // padding columns, written by the blocks of the first g tile
+  if (blockIdx.x == 0) {
+    for (int r = ty; r < 32; r += 8) {
+      uint16_t* row = o + static_cast<size_t>(n0 + r) * kaug;
+      for (int j = 3 * G + tx; j < kaug; j += 32) row[j] = 0;
+    }
   }
 }
 
@@ -270,18 +317,28 @@ cudaError_t launch_quantize_per_token(const __half* x, int8_t* Xq, float* x_scal
 
 cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
                             int kaug, __nv_bfloat16* aug, cudaStream_t st) {
+  const long long work = (group_size <= 1024) ? static_cast<long long>(M) * G
+                                              : static_cast<long long>(M) * G * 32;
+  const unsigned blocks = static_cast<unsigned>((work + 127) / 128);
   if (x_kind == kXBF16) {
-    aug_prep_kernel<kXBF16><<<M, 128, 0, st>>>(X, K, group_size, G, kaug, aug);
+    aug_prep_kernel<kXBF16><<<blocks, 128, 0, st>>>(X, M, K, group_size, G, kaug, aug);
   } else {
-    aug_prep_kernel<kXF16><<<M, 128, 0, st>>>(X, K, group_size, G, kaug, aug);
+    aug_prep_kernel<kXF16><<<blocks, 128, 0, st>>>(X, M, K, group_size, G, kaug, aug);
   }
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long pad = static_cast<long long>(M) * (kaug - 3 * G);
+  if (pad > 0) {
+    aug_pad_kernel<<<static_cast<unsigned>((pad + 255) / 256), 256, 0, st>>>(M, G, kaug, aug);
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 cudaError_t launch_delta_aug(const float* delta, int G, int N, int kaug, __nv_bfloat16* delta_aug,
                              cudaStream_t st) {
-  dim3 grid(N / 128, kaug / 128);
-  delta_aug_kernel<<<grid, 128, 0, st>>>(delta, G, N, kaug, delta_aug);
+  dim3 grid((G + 31) / 32, N / 32);
+  delta_aug_kernel<<<grid, dim3(32, 8), 0, st>>>(delta, G, N, kaug, delta_aug);
   return cudaGetLastError();
 }
 
