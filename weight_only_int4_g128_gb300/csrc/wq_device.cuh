@@ -275,25 +275,54 @@ __device__ __forceinline__ void dq8_f16_scaled(uint32_t w, uint32_t s2, uint32_t
   for (int i = 0; i < 4; ++i) o[i] = hmul2_rn(o[i], s2);
 }
 
-// 8 codes -> bfloat16_RN((v - 8) * s): (v - 8) made exact in fp32 (nibble
-// OR-ed into the mantissa of 2^23, then 2^23 + 8 subtracted), the product with
-// the fp32 value of the fp16 scale is exact, and cvt.rn.bf16x2 rounds once.
-__device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
+// 8 codes -> 4 bf16x2 registers holding (v - 8) exactly: OR-ing a nibble into
+// the mantissa of 128.0 (0x4300) gives 128 + v exactly; subtract 136.
+__device__ __forceinline__ uint32_t bsub2_rn(uint32_t a, uint32_t b) {
   uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
-__device__ __forceinline__ void dq8_bf16_scaled(uint32_t w, float s, uint32_t (&o)[4]) {
-  constexpr uint32_t kMagic = 0x4B000000u;  // 2^23
-  constexpr float kSub = 8388616.0f;        // 2^23 + 8
+__device__ __forceinline__ uint32_t bmul2_rn(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bfma2_rn(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ void dq8_bf16_exact(uint32_t w, uint32_t (&o)[4]) {
+  constexpr uint32_t kMagic = 0x43004300u;  // (128.0, 128.0)
+  constexpr uint32_t kSub = 0x43084308u;    // (136.0, 136.0)
 #pragma unroll
-  for (int p = 0; p < 4; ++p) {
-    const uint32_t lo = (w >> (4 * p)) & 0xFu;
-    const uint32_t hi = (w >> (16 + 4 * p)) & 0xFu;
-    const float flo = __fsub_rn(__uint_as_float(lo | kMagic), kSub);
-    const float fhi = __fsub_rn(__uint_as_float(hi | kMagic), kSub);
-    o[p] = cvt_bf16x2(__fmul_rn(flo, s), __fmul_rn(fhi, s));
-  }
+  for (int p = 0; p < 4; ++p) o[p] = bsub2_rn(lop_and_or(w >> (4 * p), 0x000F000Fu, kMagic), kSub);
+}
+
+// Split an fp16 scale into bf16 s_hi = RN(s) and s_lo = s - s_hi, each
+// broadcast to both halves of a bf16x2.  s_lo is exact in bf16: an fp16
+// significand has 11 bits, s_hi keeps the top 8, the remainder needs <= 3.
+struct ScaleBf16 {
+  uint32_t hi2, lo2;
+};
+__device__ __forceinline__ ScaleBf16 split_scale_bf16(__half s) {
+  const float f = __half2float(s);
+  const __nv_bfloat16 hi = __float2bfloat16_rn(f);
+  const __nv_bfloat16 lo = __float2bfloat16_rn(__fsub_rn(f, __bfloat162float(hi)));
+  ScaleBf16 r;
+  r.hi2 = static_cast<uint32_t>(__bfloat16_as_ushort(hi)) * 0x00010001u;
+  r.lo2 = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) * 0x00010001u;
+  return r;
+}
+
+// 8 codes -> bfloat16_RN((v - 8) * s) with one rounding.  x = v - 8 has <= 3
+// significant bits, so x * s_lo (<= 6 bits) is exact in bf16; the fused
+// x * s_hi + x * s_lo is then rounded once, which is RN(x * s) because
+// s_hi + s_lo == s exactly.
+__device__ __forceinline__ void dq8_bf16_scaled(uint32_t w, const ScaleBf16& s, uint32_t (&o)[4]) {
+  dq8_bf16_exact(w, o);
+#pragma unroll
+  for (int p = 0; p < 4; ++p) o[p] = bfma2_rn(o[p], s.hi2, bmul2_rn(o[p], s.lo2));
 }
 
 // fp32 -> (hi, lo) bfloat16 split: hi = bf16_RN(x), lo = bf16_RN(x - hi).

@@ -17,8 +17,9 @@
 //               (64-byte swizzle) into a shared-memory ring.
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM,
 //               B = activations from shared memory) and tcgen05.commit.
-//   warps 2..5  dequant: each thread owns one weight row, turns 128 codes into
-//               128 scaled fp16/bf16 values in registers and stores them into
+//   warps 2..9  dequant: two warps per TMEM lane quarter, each thread owns one
+//               weight row and one 64-k half of the k-block, turns its codes
+//               into scaled fp16/bf16 values in registers and stores them into
 //               a TMEM A-stage with tcgen05.st (the weights never pass through
 //               shared memory once dequantized); then the epilogue.
 // Correction as K-augmentation: a_sum (fp32, computed once by a pre-pass) is
@@ -39,6 +40,9 @@ namespace wq {
 
 // Device status word: bounded waits that expire OR a code into it.
 static __device__ unsigned int g_status = 0;
+
+constexpr int kGemmThreads = 320;  // producer, MMA issuer, 8 dequant/epilogue warps
+constexpr int kDqWarps = 8;
 
 template <int BT>
 struct Cfg {
@@ -76,7 +80,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 }
 
 template <int BT, int XK>
-__global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
+__global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_aug, const __grid_constant__ CUtensorMap tm_s,
                 const GemmParams p) {
@@ -117,11 +121,11 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kNSX; ++s) {
       mbar_init(full_x(s), 1);
-      mbar_init(empty_x(s), 4);  // one arrive per dequant warp
+      mbar_init(empty_x(s), kDqWarps);  // one arrive per dequant warp
       mbar_init(mma_done(s), 1);
     }
     for (int a = 0; a < C::kNSA; ++a) {
-      mbar_init(full_a(a), 4);
+      mbar_init(full_a(a), kDqWarps);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
@@ -195,8 +199,12 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     }
   } else {
     // ------------------------------------------------------------ dequant + epilogue
+    // Two warps per TMEM lane quarter: warp half h owns words [8h, 8h + 8) of
+    // each weight row (A-stage columns [32h, 32h + 32)) and, in the epilogue,
+    // the 16-column chunks c with c % 2 == h.
     const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, &g_status};
     const int q = warp & 3;               // TMEM lane quarter this warp may access
+    const int h = (warp - 2) >> 2;        // 0 or 1
     const int row = q * 32 + lane;        // weight row of the tile = TMEM lane
     const int n = n0 + row;
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -206,15 +214,15 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       const int s = it % C::kNSX;
       const uint32_t ph = (it / C::kNSX) & 1;
       const int a = it % C::kNSA;
-      const uint32_t a_tmem = tmem + lane_base + a * 64;
+      const uint32_t a_tmem = tmem + lane_base + a * 64 + 32 * h;
+      uint32_t v[32];
       if (it < n_aug) {
         // weight-side correction columns [d_hi | d_hi | d_lo | 0...] of this row,
-        // prepared per call in the workspace: 128 bf16 = 64 columns, 16 vector loads.
-        uint32_t v[64];
+        // prepared per call in the workspace: 64 bf16 = 32 columns, 8 vector loads.
         const uint4* src = reinterpret_cast<const uint4*>(
-            p.delta_aug + static_cast<size_t>(n) * p.kaug + it * kKBlock);
+            p.delta_aug + static_cast<size_t>(n) * p.kaug + it * kKBlock + 64 * h);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
           const uint4 t = __ldg(src + i);
           v[4 * i + 0] = t.x;
           v[4 * i + 1] = t.y;
@@ -223,62 +231,41 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
         }
         if (!warp_wait(full_x(s), ph, wc)) break;
         if (lane == 0) mbar_arrive(empty_x(s));
-        if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
-          const int pk = it - C::kNSA;
-          if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
-          tc_fence_after();
-        }
-        tmem_st32(a_tmem, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-        tmem_st32(a_tmem + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       } else {
         if (!warp_wait(full_x(s), ph, wc)) break;
         const __half sc = reinterpret_cast<const __half*>(gbase + (ss - base))[s * kTileN + row];
-        uint4 wv[4];
         const uint8_t* wrow = wring + s * C::kWStageBytes + row * 64;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          wv[c] = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ ((row >> 1) & 3)));
+        const uint4 w0 = *reinterpret_cast<const uint4*>(wrow + 16 * ((2 * h) ^ ((row >> 1) & 3)));
+        const uint4 w1 = *reinterpret_cast<const uint4*>(wrow + 16 * ((2 * h + 1) ^ ((row >> 1) & 3)));
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_x(s));
-        const uint32_t words[16] = {wv[0].x, wv[0].y, wv[0].z, wv[0].w, wv[1].x, wv[1].y,
-                                    wv[1].z, wv[1].w, wv[2].x, wv[2].y, wv[2].z, wv[2].w,
-                                    wv[3].x, wv[3].y, wv[3].z, wv[3].w};
-        uint32_t v0[32], v1[32];
+        const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         if (XK == kXF16) {
           const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
-            uint32_t o[4], o2[4];
+            uint32_t o[4];
             dq8_f16_scaled(words[w], s2, o);
-            dq8_f16_scaled(words[w + 8], s2, o2);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v0[4 * w + e] = o[e];
-              v1[4 * w + e] = o2[e];
-            }
+            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
           }
         } else {
-          const float sf = __half2float(sc);
+          const ScaleBf16 sb = split_scale_bf16(sc);
 #pragma unroll
           for (int w = 0; w < 8; ++w) {
-            uint32_t o[4], o2[4];
-            dq8_bf16_scaled(words[w], sf, o);
-            dq8_bf16_scaled(words[w + 8], sf, o2);
+            uint32_t o[4];
+            dq8_bf16_scaled(words[w], sb, o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v0[4 * w + e] = o[e];
-              v1[4 * w + e] = o2[e];
-            }
+            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
           }
         }
-        if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
-          const int pk = it - C::kNSA;
-          if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
-          tc_fence_after();
-        }
-        tmem_st32(a_tmem, v0);
-        tmem_st32(a_tmem + 32, v1);
       }
+      if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
+        const int pk = it - C::kNSA;
+        if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
+        tc_fence_after();
+      }
+      tmem_st32(a_tmem, v);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -287,12 +274,12 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
 
     // ---- epilogue (single K segment): accumulator -> Y
     warp_wait(done_bar, 0, wc);
-    named_bar_sync(1, 128);
+    named_bar_sync(1, 32 * kDqWarps);
     tc_fence_after();
     if (!*abort_flag && p.splits == 1) {  // uniform: no wait can set the flag past this point
       const uint32_t dt = tmem + lane_base + C::kDCol;
       const int mlim = min(BT, p.M - m0);
-      for (int c = 0; c < BT / 16; ++c) {
+      for (int c = h; c < BT / 16; c += 2) {
         if (16 * c >= mlim) break;
         uint32_t r[16];
         tmem_ld16(dt + 16 * c, r);
@@ -332,6 +319,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     const int mlim = min(BT, p.M - m0);
     const bool math = warp >= 2;
     const int q = warp & 3;
+    const int h = math ? (warp - 2) >> 2 : 0;
     const int row = q * 32 + lane;
     const int n = n0 + row;
     float* const red = reinterpret_cast<float*>(gbase);  // [splits][rpr][128], over the ring
@@ -341,7 +329,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
       const bool aborted = *abort_flag != 0;
       const uint32_t dt = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDCol;
       const uint32_t red_base = smem_u32(red);
-      for (int c = 0; c < BT / 16; ++c) {
+      for (int c = h; c < BT / 16; c += 2) {
         if (16 * c >= mlim) break;
         uint32_t r[16];
         tmem_ld16(dt + 16 * c, r);
@@ -363,7 +351,7 @@ __global__ void __launch_bounds__(192, (BT <= 32) ? 2 : 1)
     cluster_sync_all();  // all pushes landed
     if (math) {
       const int hi = min(mlim, (seg + 1) * rpr);
-      for (int ml = seg * rpr; ml < hi; ++ml) {
+      for (int ml = seg * rpr + h; ml < hi; ml += 2) {
         const int local = ml - seg * rpr;
         float acc = 0.0f;
         for (int src = 0; src < splits; ++src) acc += red[(src * rpr + local) * kTileN + row];
@@ -403,7 +391,7 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

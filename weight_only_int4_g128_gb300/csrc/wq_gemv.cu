@@ -66,20 +66,6 @@ __device__ __forceinline__ void named_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// 8 codes -> 4 bf16x2 registers holding (v - 8) exactly: OR-ing a nibble into
-// the mantissa of 128.0 (0x4300) gives 128 + v exactly; subtract 136.
-__device__ __forceinline__ uint32_t bsub2_rn(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ void dq8_bf16_exact(uint32_t w, uint32_t (&o)[4]) {
-  constexpr uint32_t kMagic = 0x43004300u;  // (128.0, 128.0)
-  constexpr uint32_t kSub = 0x43084308u;    // (136.0, 136.0)
-#pragma unroll
-  for (int p = 0; p < 4; ++p) o[p] = bsub2_rn(lop_and_or(w >> (4 * p), 0x000F000Fu, kMagic), kSub);
-}
-
 __device__ __forceinline__ float lo_to_f32(uint32_t u, int xk) {
   return xk == kXF16 ? __half2float(__ushort_as_half(static_cast<uint16_t>(u & 0xFFFFu)))
                      : __uint_as_float(u << 16);

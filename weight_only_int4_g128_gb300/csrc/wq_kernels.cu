@@ -96,7 +96,7 @@ __global__ void dequant_kernel(const uint32_t* __restrict__ Bpacked, const __hal
   if (w_kind == kXF16) {
     dq8_f16_scaled(word, static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u, o);
   } else {
-    dq8_bf16_scaled(word, __half2float(sc), o);
+    dq8_bf16_scaled(word, split_scale_bf16(sc), o);
   }
   uint16_t* out = reinterpret_cast<uint16_t*>(W);
 #pragma unroll
