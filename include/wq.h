@@ -60,6 +60,9 @@ extern "C" {
 #define WQ_DTYPE_BF16 1
 #define WQ_DTYPE_F32 2
 
+/* options for wq_set_option / wq_get_option */
+#define WQ_OPTION_WEIGHT_PREFETCH 1 /* 0 (default) or 1, see wq_set_option */
+
 /* workspace variants for wq_workspace_size */
 #define WQ_VARIANT_W4A16 0      /* wq_gemm_w4a16 with delta (asymmetric) */
 #define WQ_VARIANT_W4A16_SYM 1  /* wq_gemm_w4a16 with delta == NULL */
@@ -72,8 +75,14 @@ extern "C" {
  *   q        [K][N] uint8 device, one code 0..15 per byte (row k, column n).
  *   scale    [G][N] fp16 device, G = K / group_size.
  *   zero     [G][N] fp16 device.
- *   Bpacked  [N][K/8] uint32 device, output.  Word (n, w) holds q[8w + j][n]
- *            for j = 0..7, code j in bits [4*(j/2) + 16*(j%2), +4).
+ *   Bpacked  K*N/8 uint32 device, output, in this library's blocked layout:
+ *            the word for column n and codes k = 8w..8w+7 holds q[8w + j][n],
+ *            code j in bits [4*(j/2) + 16*(j%2), +4); words are grouped in
+ *            blocks of 128 columns x 128 k (2048 words), block index
+ *            (n/128)*(K/128) + 8w/128, and inside a block row r = n%128 holds
+ *            its 16 words as four 16-byte chunks, chunk c = (w%16)/4 stored at
+ *            word offset r*16 + 4*(c ^ ((r/2)%4)) + w%4.  Each block is the
+ *            weight tile one GEMM pipeline stage copies in a single transfer.
  *   S        [G][N] fp16 device, output: a copy of scale.
  *   delta    [G][N] fp32 device, output: fp32(zero) + 8*fp32(scale), rounded
  *            once (exact for operands of similar magnitude).
@@ -89,13 +98,13 @@ int wq_pack_w4a16(const uint8_t* q, const void* scale, const void* zero, uint32_
  * (value -8), which becomes +7 instead of +8.
  *   q             [K][N] uint8 device, uint4b8 codes (value = v - 8).
  *   scale_signed  [G][N] fp16 device.
- *   Bpacked       [N][K/8] uint32 device, output (layout as wq_pack_w4a16).
+ *   Bpacked       K*N/8 uint32 device, output (layout as wq_pack_w4a16).
  *   S_abs         [G][N] fp16 device, output: the folded (non-negative) scales.
  */
 int wq_pack_w4a8(const uint8_t* q, const void* scale_signed, uint32_t* Bpacked, void* S_abs,
                  int K, int N, int group_size, void* stream);
 
-/* Inverse of the packing: Bpacked [N][K/8] -> q [K][N] uint8 codes. */
+/* Inverse of the packing: Bpacked (blocked layout) -> q [K][N] uint8 codes. */
 int wq_unpack_w4(const uint32_t* Bpacked, uint8_t* q, int K, int N, void* stream);
 
 /*
@@ -110,7 +119,7 @@ int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, 
  * W4A16 GEMM with the fused zero-point correction:
  *   Y[m][n] = sum_k X[m][k] * W_sym[k][n] + (A_group_sum @ delta)[m][n]
  *   X        [M][K] device, fp16 or bf16 (x_dtype), row-major.
- *   Bpacked  [N][K/8] uint32 device (from wq_pack_w4a16).
+ *   Bpacked  K*N/8 uint32 device (from wq_pack_w4a16).
  *   S        [G][N] fp16 device.
  *   delta    [G][N] fp32 device, or NULL for symmetric weights (no correction).
  *   Y        [M][N] device, output, overwritten (y_dtype F16, BF16 or F32).
@@ -148,6 +157,20 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
  * An all-zero row gives x_scale = 0 and zero codes.  Any K >= 1.
  */
 int wq_quantize_per_token(const void* x, int8_t* Xq, float* x_scale, int M, int K, void* stream);
+
+/*
+ * Process-wide launch options.
+ *   WQ_OPTION_WEIGHT_PREFETCH: the decode kernel (M <= 16) is launched with
+ *   programmatic dependent launch, so its setup overlaps the tail of the
+ *   preceding kernel in the stream; it waits for that kernel before touching
+ *   X or Y.  With this option set to 1 it also starts copying its first weight
+ *   tiles (Bpacked, S, delta) before that wait.  Only enable it when the
+ *   kernel launched just before each GEMM on the stream does not write the
+ *   weights (the usual serving loop, where weights are packed once).
+ * Returns WQ_ERR_INVALID_ARG for an unknown option or value.
+ */
+int wq_set_option(int option, long long value);
+int wq_get_option(int option, long long* value);
 
 /* Bytes of workspace the GEMM needs for this problem (0 if none). */
 size_t wq_workspace_size(int variant, int M, int N, int K, int group_size);

@@ -147,18 +147,19 @@ def double_to_bf16(x: np.ndarray) -> np.ndarray:
 # -- pack / fold / delta -----------------------------------------------------------
 
 def pack(q: np.ndarray) -> np.ndarray:
-    """codes q [K, N] (0..15) -> packed words [N, K/8] uint32 (the library layout)."""
+    """codes q [K, N] (0..15) -> packed words [N/128, K/128, 128, 16] uint32 (the library's
+    blocked layout; see wq_oracle.c).  K and N must be multiples of 128."""
     lib = _load()
     q = _c(q, np.uint8)
     K, N = q.shape
-    out = np.empty((N, K // 8), np.uint32)
+    out = np.empty((N // 128, K // 128, 128, 16), np.uint32)
     lib.wq_o_pack(_p(q), K, N, _p(out))
     return out
 
 
 def unpack(words: np.ndarray, K: int, N: int) -> np.ndarray:
     lib = _load()
-    w = _c(words, np.uint32).reshape(N, K // 8)
+    w = _c(words, np.uint32).reshape(-1)
     q = np.empty((K, N), np.uint8)
     lib.wq_o_unpack(_p(w), K, N, _p(q))
     return q

@@ -33,9 +33,14 @@
  * folded).
  *
  * Packed layout (this library's own; the pages fix only "8 x int4 -> uint32"):
- *   words[n * (K/8) + w] holds the codes q[8w + j][n], j = 0..7; code j sits
- *   in bits [b_j, b_j + 4) with b_j = 4*(j/2) + 16*(j%2), i.e. even j fill the
- *   low 16 bits and odd j the high 16 bits, in increasing j.
+ *   The word for column n and codes k = 8w .. 8w+7 holds q[8w + j][n], j = 0..7;
+ *   code j sits in bits [b_j, b_j + 4) with b_j = 4*(j/2) + 16*(j%2), i.e. even
+ *   j fill the low 16 bits and odd j the high 16 bits, in increasing j.
+ *   Words are grouped in blocks of 128 columns x 128 k (2048 words, 8 KB):
+ *     block   = (n / 128) * (K / 128) + (8w) / 128
+ *     r       = n % 128,  u = w % 16 (word of the row inside the block),
+ *     c       = u / 4 (16-byte chunk), e = u % 4
+ *     index   = block * 2048 + r * 16 + 4 * (c XOR ((r / 2) % 4)) + e
  */
 #include <math.h>
 #include <stdint.h>
@@ -145,7 +150,17 @@ WQ_O_API void wq_o_double_to_bf16_array(const double* x, int64_t n, uint16_t* ou
 
 static int nibble_shift(int j) { return 4 * (j / 2) + 16 * (j % 2); }
 
-/* q: [K][N] codes 0..15, one per byte.  words: [N][K/8]. */
+/* Position of the word holding codes 8w..8w+7 of column n (see the header). */
+static int64_t word_index(int n, int w, int K) {
+  int64_t block = (int64_t)(n / 128) * (K / 128) + (8 * w) / 128;
+  int r = n % 128;
+  int u = w % 16;
+  int c = u / 4;
+  int e = u % 4;
+  return block * 2048 + (int64_t)r * 16 + 4 * (c ^ ((r / 2) % 4)) + e;
+}
+
+/* q: [K][N] codes 0..15, one per byte.  words: K*N/8 words in the blocked layout. */
 WQ_O_API void wq_o_pack(const uint8_t* q, int K, int N, uint32_t* words) {
   int KW = K / 8;
   for (int n = 0; n < N; ++n) {
@@ -155,7 +170,7 @@ WQ_O_API void wq_o_pack(const uint8_t* q, int K, int N, uint32_t* words) {
         uint32_t v = q[(int64_t)(8 * w + j) * N + n] & 0xfu;
         word |= v << nibble_shift(j);
       }
-      words[(int64_t)n * KW + w] = word;
+      words[word_index(n, w, K)] = word;
     }
   }
 }
@@ -164,7 +179,7 @@ WQ_O_API void wq_o_unpack(const uint32_t* words, int K, int N, uint8_t* q) {
   int KW = K / 8;
   for (int n = 0; n < N; ++n) {
     for (int w = 0; w < KW; ++w) {
-      uint32_t word = words[(int64_t)n * KW + w];
+      uint32_t word = words[word_index(n, w, K)];
       for (int j = 0; j < 8; ++j) {
         q[(int64_t)(8 * w + j) * N + n] = (uint8_t)((word >> nibble_shift(j)) & 0xfu);
       }

@@ -97,6 +97,13 @@ def test_shape_and_argument_errors_before_device_work(lib):
     assert lib.wq_pack_w4a16(None, fake, fake, fake, fake, fake, 256, 256, 128, None) == 1
     assert lib.wq_dequant_w4(fake, fake, fake, 2, 256, 256, 128, None) == 1
     assert lib.wq_debug_wait_probe(0, None) == 1
+    assert lib.wq_set_option(99, 1) == 1
+    assert lib.wq_set_option(wq.OPTION_WEIGHT_PREFETCH, 2) == 1
+    v = ctypes.c_longlong(-1)
+    assert lib.wq_get_option(wq.OPTION_WEIGHT_PREFETCH, ctypes.byref(v)) == 0 and v.value == 0
+    assert lib.wq_set_option(wq.OPTION_WEIGHT_PREFETCH, 1) == 0
+    assert lib.wq_get_option(wq.OPTION_WEIGHT_PREFETCH, ctypes.byref(v)) == 0 and v.value == 1
+    assert lib.wq_set_option(wq.OPTION_WEIGHT_PREFETCH, 0) == 0
 
 
 def test_no_device_means_an_error_not_a_fallback(lib):

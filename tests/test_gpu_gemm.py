@@ -278,3 +278,42 @@ def test_full_size_workloads_sampled(wq, workload, idx):
             got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
             err = oracle.rel_fro(got, ref)
             assert err <= TOL_W4A16, (c, err)
+
+
+@pytest.mark.parametrize("prefetch", [False, True])
+def test_back_to_back_launches_see_their_inputs(wq, prefetch):
+    """Decode GEMMs launched back to back (programmatic dependent launch) read activations
+    written by the kernel launched just before them, eagerly and inside a CUDA graph, and
+    match synchronised runs bit for bit."""
+    M, K, N = 4, 2048, 512
+    d = synth.make_inputs(980, M, K, N)
+    Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
+    X = _cuda(d["A"])
+    refs = []
+    for i in range(4):
+        Xi = X * (i + 1)
+        torch.cuda.synchronize()
+        refs.append(wq.gemm_w4a16(Xi, Bp, S, dl, 128))
+        torch.cuda.synchronize()
+    wq.set_weight_prefetch(prefetch)
+    try:
+        outs = [wq.gemm_w4a16(X * (i + 1), Bp, S, dl, 128) for i in range(4)]
+        torch.cuda.synchronize()
+        for Y, R in zip(outs, refs):
+            assert torch.equal(Y, R)
+        Ys = [torch.empty_like(refs[0]) for _ in range(4)]
+        s = torch.cuda.Stream()
+        with torch.cuda.stream(s):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                for i in range(4):
+                    wq.gemm_w4a16(X * (i + 1), Bp, S, dl, 128, out=Ys[i])
+            for _ in range(3):
+                for Y in Ys:
+                    Y.zero_()
+                g.replay()
+        torch.cuda.synchronize()
+        for Y, R in zip(Ys, refs):
+            assert torch.equal(Y, R)
+    finally:
+        wq.set_weight_prefetch(False)

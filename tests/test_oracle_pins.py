@@ -77,41 +77,60 @@ def test_bf16_rounding_matches_torch():
 
 # --------------------------------------------------------------------------- pack layout
 
+def _word_position(n, w, K):
+    """The blocked layout's word position, written out independently of the oracle:
+    8 KB blocks of 128 columns x 128 k, row r = n % 128 holds 16 words as four
+    16-byte chunks, chunk c stored at slot c ^ ((r // 2) % 4)."""
+    block = (n // 128) * (K // 128) + (8 * w) // 128
+    r, u = n % 128, w % 16
+    c, e = u // 4, u % 4
+    return block * 2048 + r * 16 + 4 * (c ^ ((r // 2) % 4)) + e
+
+
 def test_pack_golden_words():
+    """Each golden line: the 8 codes of column 0, k = 0..7 -> their word (the first word)."""
     for row in _golden_rows("pack_layout.txt"):
         codes, word = row.split("->")
         codes = [int(c) for c in codes.split()]
-        q = np.array(codes, np.uint8).reshape(8, 1)
-        assert int(oracle.pack(q)[0, 0]) == int(word, 16), row
+        q = np.zeros((128, 128), np.uint8)
+        q[:8, 0] = codes
+        assert int(oracle.pack(q).reshape(-1)[_word_position(0, 0, 128)]) == int(word, 16), row
 
 
 def test_pack_unpack_roundtrip_exhaustive():
-    """Every code 0..15 at every nibble position, several columns, round trip."""
-    K, N = 16 * 8, 24
+    """Every code 0..15 at every nibble position, several column tiles, round trip."""
+    K, N = 16 * 8, 256
     q = np.zeros((K, N), np.uint8)
     for k in range(K):
         for n in range(N):
             q[k, n] = (k // 8 + 3 * n + (k % 8)) % 16
     w = oracle.pack(q)
-    assert w.shape == (N, K // 8)
+    assert w.shape == (N // 128, K // 128, 128, 16)
     assert np.array_equal(oracle.unpack(w, K, N), q)
     rng = _rng(3)
-    q2 = rng.integers(0, 16, (256, 40), dtype=np.uint8)
-    assert np.array_equal(oracle.unpack(oracle.pack(q2), 256, 40), q2)
+    q2 = rng.integers(0, 16, (384, 256), dtype=np.uint8)
+    assert np.array_equal(oracle.unpack(oracle.pack(q2), 384, 256), q2)
 
 
 def test_pack_matches_bitwise_definition():
-    """Pack == the layout rule written with numpy shifts (brute force)."""
+    """Pack == the layout rule written with numpy shifts and the position formula (brute force)."""
     rng = _rng(4)
-    K, N = 64, 9
+    K, N = 256, 256
     q = rng.integers(0, 16, (K, N), dtype=np.uint8)
-    w = oracle.pack(q)
-    for n in range(N):
+    w = oracle.pack(q).reshape(-1)
+    for n in list(range(0, N, 7)) + [1, 2, 3, 127, 128, 255]:
         for kw in range(K // 8):
             word = 0
             for j in range(8):
                 word |= int(q[8 * kw + j, n]) << (4 * (j // 2) + 16 * (j % 2))
-            assert int(w[n, kw]) == word
+            assert int(w[_word_position(n, kw, K)]) == word
+
+
+def test_pack_positions_are_a_permutation():
+    """Every (column, word) pair lands on a distinct slot (the layout is a bijection)."""
+    K, N = 384, 256
+    pos = {_word_position(n, w, K) for n in range(N) for w in range(K // 8)}
+    assert len(pos) == N * K // 8 and min(pos) == 0 and max(pos) == N * K // 8 - 1
 
 
 # --------------------------------------------------------------------------- delta

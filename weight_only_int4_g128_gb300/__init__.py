@@ -24,7 +24,8 @@ __all__ = [
     "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a8", "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
-    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8",
+    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "set_weight_prefetch",
+    "OPTION_WEIGHT_PREFETCH",
 ]
 
 DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
@@ -48,7 +49,10 @@ EXPORTS = {
     "wq_version": (ctypes.c_char_p, []),
     "wq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint), _I, _P]),
     "wq_debug_wait_probe": (_I, [ctypes.c_ulonglong, _P]),
+    "wq_set_option": (_I, [_I, ctypes.c_longlong]),
+    "wq_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
 }
+OPTION_WEIGHT_PREFETCH = 1
 
 _lib = None
 _lock = threading.Lock()
@@ -121,12 +125,14 @@ def _require_cuda(*ts):
 # -- packing -------------------------------------------------------------------------
 
 def pack_w4a16(q, scale, zero, group_size: int = 128):
-    """q [K,N] uint8 codes, scale/zero [G,N] fp16 -> (Bpacked [N,K/8] int32, S, delta fp32)."""
+    """q [K,N] uint8 codes, scale/zero [G,N] fp16 -> (Bpacked, S, delta fp32).
+
+    Bpacked is int32 [N/128, K/128, 128, 16] holding the library's blocked layout."""
     torch = _torch()
     _require_cuda(q, scale, zero)
     K, N = q.shape
     G = K // _gs(K, group_size)
-    Bp = torch.empty((N, K // 8), dtype=torch.int32, device=q.device)
+    Bp = torch.empty((N // 128, K // 128, 128, 16), dtype=torch.int32, device=q.device)
     S = torch.empty((G, N), dtype=torch.float16, device=q.device)
     d = torch.empty((G, N), dtype=torch.float32, device=q.device)
     _check(load_library().wq_pack_w4a16(_ptr(q), _ptr(scale), _ptr(zero), _ptr(Bp), _ptr(S),
@@ -140,7 +146,7 @@ def pack_w4a8(q, scale_signed, group_size: int = 128):
     _require_cuda(q, scale_signed)
     K, N = q.shape
     G = K // _gs(K, group_size)
-    Bp = torch.empty((N, K // 8), dtype=torch.int32, device=q.device)
+    Bp = torch.empty((N // 128, K // 128, 128, 16), dtype=torch.int32, device=q.device)
     S = torch.empty((G, N), dtype=torch.float16, device=q.device)
     _check(load_library().wq_pack_w4a8(_ptr(q), _ptr(scale_signed), _ptr(Bp), _ptr(S), K, N,
                                        group_size, _stream()), "wq_pack_w4a8")
@@ -217,7 +223,7 @@ def gemm_w4a16(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=
     out_dtype = out_dtype or torch.float16
     _require_cuda(X, Bpacked, S, delta, out)
     M, K = X.shape
-    N = Bpacked.shape[0]
+    N = Bpacked.numel() * 8 // K
     Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=X.device)
     variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
     need = workspace_size(variant, M, N, K, group_size) if M > 0 else 0
@@ -236,7 +242,7 @@ def gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size: int = 128, out_dtype=None
     out_dtype = out_dtype or torch.float16
     _require_cuda(Xq, x_scale, Bpacked, S_abs, out)
     M, K = Xq.shape
-    N = Bpacked.shape[0]
+    N = Bpacked.numel() * 8 // K
     Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=Xq.device)
     need = workspace_size(VARIANT_W4A8, M, N, K, group_size) if M > 0 else 0
     ws = workspace if workspace is not None else (_workspace(Xq.device, need) if need else None)
@@ -261,6 +267,13 @@ def device_status(reset: bool = True) -> int:
 
 def debug_wait_probe(limit_ns: int):
     _check(load_library().wq_debug_wait_probe(limit_ns, _stream()), "wq_debug_wait_probe")
+
+
+def set_weight_prefetch(enabled: bool):
+    """Let the decode kernel start copying weights before the preceding kernel in the
+    stream finishes (only valid when that kernel does not write the weights)."""
+    _check(load_library().wq_set_option(OPTION_WEIGHT_PREFETCH, 1 if enabled else 0),
+           "wq_set_option")
 
 
 def version() -> str:

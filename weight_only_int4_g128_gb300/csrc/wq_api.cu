@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -15,6 +16,7 @@
 namespace {
 
 thread_local char t_err[512] = "";
+std::atomic<int> g_weight_prefetch{0};
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -170,7 +172,7 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   const int mtiles = (M + p.bt - 1) / p.bt;
   const int tiles = ntiles * mtiles;
   // CTA slots per wave: the decode kernel and the 16/32-token tiles fit two per SM.
-  const int slots = (p.bt <= 32) ? 2 * wq::kNumSMs : wq::kNumSMs;
+  const int slots = (p.bt <= 64) ? 2 * wq::kNumSMs : wq::kNumSMs;
   // As many K segments as still fit in one wave; the segments of a tile form
   // one thread-block cluster and are reduced through distributed shared memory.
   int splits = slots / tiles;
@@ -220,13 +222,10 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     if (e != cudaSuccess) return cuda_fail(e, "delta pre-pass");
   }
 
-  CUtensorMap tm_x, tm_w, tm_aug, tm_s, tm_d;
+  CUtensorMap tm_x, tm_aug, tm_s, tm_d;
   const CUtensorMapDataType xdt =
       x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   int rc = make_map_x3d(&tm_x, xdt, xg, M, K, plan.bt);
-  if (rc) return rc;
-  rc = make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, Bpacked, N, K / 8, 128, 16,
-                CU_TENSOR_MAP_SWIZZLE_64B);
   if (rc) return rc;
   if (plan.kaug) {
     rc = make_map_x3d(&tm_aug, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, aug, M, plan.kaug, plan.bt);
@@ -234,11 +233,11 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   } else {
     tm_aug = tm_x;  // unused
   }
-  // scale and delta rows: one group row of 128 columns per pipeline stage
-  rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  // scale and delta rows: 8 group rows of 128 columns per copy (rows past G read as zero)
+  rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
   if (delta && variant == WQ_VARIANT_W4A16) {
-    rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 1, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
   } else {
     tm_d = tm_s;  // unused
@@ -255,6 +254,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.splits = plan.splits;
   p.aug_stages = plan.kaug / 128;
   p.kaug = plan.kaug;
+  p.B = Bpacked;
   p.S = static_cast<const __half*>(S);
   p.delta = (variant == WQ_VARIANT_W4A16) ? delta : nullptr;
   p.delta_aug = plan.kaug ? daug : nullptr;
@@ -262,10 +262,11 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.Y = Y;
   p.y_kind = y_kind;
   p.timeout_ns = timeout_ns();
+  p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
   if (plan.gemv) {
-    e = wq::launch_gemv(x_kind, tm_x, tm_w, tm_s, tm_d, p, st);
+    e = wq::launch_gemv(x_kind, tm_x, tm_s, tm_d, p, st);
   } else {
-    e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_w, tm_aug, tm_s, p, st);
+    e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_aug, tm_s, p, st);
   }
   return after_launch(e, name, st);
 }
@@ -297,6 +298,24 @@ int wq_device_supported(int device) {
 }
 
 const char* wq_last_error(void) { return t_err; }
+
+int wq_set_option(int option, long long value) {
+  if (option == WQ_OPTION_WEIGHT_PREFETCH) {
+    if (value != 0 && value != 1) return fail(WQ_ERR_INVALID_ARG, "wq_set_option: value must be 0 or 1");
+    g_weight_prefetch.store(static_cast<int>(value), std::memory_order_relaxed);
+    return WQ_OK;
+  }
+  return fail(WQ_ERR_INVALID_ARG, "wq_set_option: unknown option %d", option);
+}
+
+int wq_get_option(int option, long long* value) {
+  if (!value) return fail(WQ_ERR_INVALID_ARG, "wq_get_option: null pointer");
+  if (option == WQ_OPTION_WEIGHT_PREFETCH) {
+    *value = g_weight_prefetch.load(std::memory_order_relaxed);
+    return WQ_OK;
+  }
+  return fail(WQ_ERR_INVALID_ARG, "wq_get_option: unknown option %d", option);
+}
 
 const char* wq_version(void) { return "wq 0.1.0 (sm_103a, tcgen05)"; }
 

@@ -12,9 +12,9 @@
 //
 // Tiling (swap-AB): one CTA owns 128 output columns n (the MMA's M = 128,
 // i.e. 128 TMEM lanes, one weight row per lane) and BT tokens (the MMA's N).
-//   warp 0      TMA producer: activation tile [BT x 128 k] (two 128-byte
-//               swizzled boxes) and the packed weight tile [128 n x 16 words]
-//               (64-byte swizzle) into a shared-memory ring.
+//   warp 0      TMA producer: activation tile [BT x 128 k] (one 3-D box = two
+//               128-byte swizzled atoms), the packed weight tile (one
+//               contiguous 8 KB block, bulk copy) and the scale row.
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM,
 //               B = activations from shared memory) and tcgen05.commit.
 //   warps 2..9  dequant: two warps per TMEM lane quarter, each thread owns one
@@ -49,22 +49,27 @@ struct Cfg {
   static constexpr int kXStageBytes = BT * kKBlock * 2;              // two SW128 atoms
   static constexpr int kXAtomBytes = BT * 128;                        // one box of 64 k
   static constexpr int kWStageBytes = kTileN * kWordsPerKBlock * 4;  // 8 KB
-  static constexpr int kNSX = (BT >= 256) ? 3 : (BT >= 128) ? 5 : (BT >= 64) ? 8 : (BT >= 32) ? 6 : 8;
+  // tiles of <= 64 tokens run two CTAs per SM (<= 113 KB shared memory, 256 TMEM columns)
+  static constexpr bool kTwoPerSM = BT <= 64;
+  static constexpr int kNSX = (BT >= 256) ? 3 : (BT >= 128) ? 5 : (BT >= 64) ? 4 : 6;
   // TMEM A-stages (64 columns each); at most kNSX so that the per-stage
   // mma_done barrier also tells when an A-stage is free again
-  static constexpr int kNSA = (BT <= 32) ? 3 : (kNSX < 4 ? kNSX : 4);
-  static constexpr int kDCol = (BT <= 32) ? 192 : 256;                // accumulator columns
-  static constexpr int kTmemCols = (BT <= 32) ? 256 : 512;
-  static constexpr int kSStageBytes = kTileN * 2;                     // scale row, fp16
-  static constexpr int kNumBars = 3 * kNSX + kNSA + 1;
-  static constexpr int kSmemBytes = 1024 /*align slack*/ +
-                                    kNSX * (kXStageBytes + kWStageBytes + kSStageBytes) +
-                                    kNumBars * 8 + 16;
+  static constexpr int kNSA = kTwoPerSM ? 3 : (kNSX < 4 ? kNSX : 4);
+  static constexpr int kDCol = kTwoPerSM ? 192 : 256;                // accumulator columns
+  static constexpr int kTmemCols = kTwoPerSM ? 256 : 512;
+  static constexpr int kChunk = 8;  // groups per scale chunk (the index math below uses >> 3)
+  static constexpr int kSChunkBytes = kChunk * kTileN * 2;            // 2 KB of fp16 scale rows
+  static constexpr int kChunkSlots = 2;
+  static constexpr int kNumBars = 3 * kNSX + kNSA + 1 + 2 * kChunkSlots;
+  static constexpr int kSmemBytes = 1024 /*align slack*/ + kNSX * (kXStageBytes + kWStageBytes) +
+                                    kChunkSlots * kSChunkBytes + kNumBars * 8 + 16;
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N for M=128 is 16..256, step 16");
   static_assert(kDCol + BT <= kTmemCols, "TMEM budget");
+  static_assert(!kTwoPerSM || kSmemBytes + 1024 <= 116 * 1024, "two CTAs per SM");
   static_assert(kNSA * 64 <= kDCol, "TMEM budget");
   static_assert(kNSA <= kNSX, "mma_done is indexed by stage");
-  static_assert((BT + 8) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
+  // split-K reduction buffer red[splits][128][rpr + 4] (rpr <= BT/splits + 3, splits <= 8)
+  static_assert((BT + 64) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
                 "split-K reduction buffer reuses the stage ring");
 };
 
@@ -80,10 +85,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 }
 
 template <int BT, int XK>
-__global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
-    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_aug, const __grid_constant__ CUtensorMap tm_s,
-                const GemmParams p) {
+__global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_aug,
+                const __grid_constant__ CUtensorMap tm_s, const GemmParams p) {
   using C = Cfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -91,8 +95,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
   uint8_t* const gbase = smem_raw + (base - raw);
   const uint32_t sx = base;
   const uint32_t sw = sx + C::kNSX * C::kXStageBytes;
-  const uint32_t ss = sw + C::kNSX * C::kWStageBytes;
-  const uint32_t sbar = ss + C::kNSX * C::kSStageBytes;
+  const uint32_t sch = sw + C::kNSX * C::kWStageBytes;  // scale chunk slots
+  const uint32_t sbar = sch + C::kChunkSlots * C::kSChunkBytes;
   // full_x: TMA bytes of stage s landed; empty_x: the dequant warps have read
   // it; mma_done: the k-block's MMAs completed (one tcgen05.commit per
   // k-block; frees the activation tile and the TMEM A-stage); full_a: the
@@ -102,6 +106,10 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
   auto mma_done = [&](int s) { return sbar + 8u * (2 * C::kNSX + s); };
   auto full_a = [&](int a) { return sbar + 8u * (3 * C::kNSX + a); };
   const uint32_t done_bar = sbar + 8u * (3 * C::kNSX + C::kNSA);
+  // full_c / empty_c: scale rows of 8 consecutive groups (one chunk) landed /
+  // released by the dequant warps.
+  auto full_c = [&](int c) { return sbar + 8u * (3 * C::kNSX + C::kNSA + 1 + c); };
+  auto empty_c = [&](int c) { return sbar + 8u * (3 * C::kNSX + C::kNSA + 1 + C::kChunkSlots + c); };
   const uint32_t misc = sbar + 8u * C::kNumBars;
   uint8_t* const gmisc = gbase + (misc - base);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gmisc);
@@ -117,6 +125,12 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
   const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
   const int n_aug = (seg == 0) ? p.aug_stages : 0;
   const int n_stages = n_aug + max(0, kb1 - kb0);
+  // group size is 128 (group = k-block) or K (one group per column)
+  const bool per_channel = p.group_size != kKBlock;
+  const int g_first = per_channel ? 0 : kb0;  // first group of this K segment
+  // chunk ordinal (0, 1, ...) and row of the k-block `kb` (chunks of 8 groups)
+  auto chunk_of = [&](int kb) { return per_channel ? 0 : (kb >> 3) - (g_first >> 3); };
+  auto chunk_row = [&](int kb) { return per_channel ? 0 : (kb & 7); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kNSX; ++s) {
@@ -127,6 +141,10 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
     for (int a = 0; a < C::kNSA; ++a) {
       mbar_init(full_a(a), kDqWarps);
     }
+    for (int c = 0; c < C::kChunkSlots; ++c) {
+      mbar_init(full_c(c), 1);
+      mbar_init(empty_c(c), kDqWarps);
+    }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     *last_flag = 0;
@@ -134,7 +152,6 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tm_x);
-    prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_s);
     if (p.aug_stages > 0) prefetch_tensormap(&tm_aug);
   }
@@ -147,7 +164,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int issued = 0;  // TMA stages the producer lane has issued
+  int issued = 0;         // TMA stages the producer lane has issued
+  int chunks_loaded = 0;  // producer lane: scale chunks [0, chunks_loaded) issued
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -164,10 +182,21 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
           tma_load_3d(xdst, &tm_aug, full_x(s), 0, m0, 2 * it);
         } else {
           const int kb = kb0 + (it - n_aug);
-          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes + C::kSStageBytes);
+          const int o = chunk_of(kb);
+          if (o >= chunks_loaded) {
+            const int slot = o % C::kChunkSlots;
+            if (!mbar_wait(empty_c(slot), ((o / C::kChunkSlots) & 1) ^ 1, wc)) break;
+            mbar_arrive_expect_tx(full_c(slot), C::kSChunkBytes);
+            tma_load_2d(sch + slot * C::kSChunkBytes, &tm_s, full_c(slot), n0,
+                        ((g_first >> 3) + o) * C::kChunk);
+            chunks_loaded = o + 1;
+          }
+          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes);
           tma_load_3d(xdst, &tm_x, full_x(s), 0, m0, 2 * kb);
-          tma_load_2d(sw + s * C::kWStageBytes, &tm_w, full_x(s), kb * kWordsPerKBlock, n0);
-          tma_load_2d(ss + s * C::kSStageBytes, &tm_s, full_x(s), n0, (kb * kKBlock) / p.group_size);
+          // packed weight tile: one contiguous 8 KB block of the blocked layout
+          bulk_load(sw + s * C::kWStageBytes,
+                    p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb) * 2048, C::kWStageBytes,
+                    full_x(s));
         }
         issued = it + 1;
       }
@@ -233,12 +262,20 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
         if (lane == 0) mbar_arrive(empty_x(s));
       } else {
         if (!warp_wait(full_x(s), ph, wc)) break;
-        const __half sc = reinterpret_cast<const __half*>(gbase + (ss - base))[s * kTileN + row];
+        const int kb = kb0 + (it - n_aug);
+        const int o = chunk_of(kb);
+        const int slot = o % C::kChunkSlots;
+        if (!warp_wait(full_c(slot), (o / C::kChunkSlots) & 1, wc)) break;
+        const __half sc = reinterpret_cast<const __half*>(
+            gbase + (sch - base) + slot * C::kSChunkBytes)[chunk_row(kb) * kTileN + row];
         const uint8_t* wrow = wring + s * C::kWStageBytes + row * 64;
         const uint4 w0 = *reinterpret_cast<const uint4*>(wrow + 16 * ((2 * h) ^ ((row >> 1) & 3)));
         const uint4 w1 = *reinterpret_cast<const uint4*>(wrow + 16 * ((2 * h + 1) ^ ((row >> 1) & 3)));
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_x(s));
+        if (lane == 0) {
+          mbar_arrive(empty_x(s));
+          if (kb + 1 == kb1 || chunk_of(kb + 1) != o) mbar_arrive(empty_c(slot));  // chunk done
+        }
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
         if (XK == kXF16) {
           const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
@@ -306,43 +343,53 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
     const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, &g_status};
     for (int it = max(0, issued - C::kNSX); it < issued; ++it)
       mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
+    for (int o = max(0, chunks_loaded - C::kChunkSlots); o < chunks_loaded; ++o)
+      mbar_wait(full_c(o % C::kChunkSlots), (o / C::kChunkSlots) & 1, drain);
   }
   __syncthreads();
 
   // ---- split-K over a thread-block cluster (the K segments of one output tile).
-  // Every CTA pushes its fp32 partial rows into the shared memory of the rank
-  // that owns them (rows [r*rpr, (r+1)*rpr) belong to rank r); the owner sums
-  // the partials in rank order (deterministic) and writes Y.
+  // Rows (tokens) [r*rpr, (r+1)*rpr) of the tile belong to rank r (rpr a multiple
+  // of 4).  Every CTA pushes its fp32 partial of those rows into rank r's shared
+  // memory with 16-byte remote stores, laid out red[src][row][rpr_pad] (rows are
+  // the 128 weight rows of the tile); the owner sums the partials in rank order
+  // (deterministic) and writes Y.
   if (p.splits > 1) {
     const int splits = p.splits;
-    const int rpr = (BT + splits - 1) / splits;
+    const int rpr = ((BT + splits - 1) / splits + 3) & ~3;
+    const int rpr_pad = rpr + 4;  // breaks shared-memory bank conflicts between rows
     const int mlim = min(BT, p.M - m0);
     const bool math = warp >= 2;
     const int q = warp & 3;
     const int h = math ? (warp - 2) >> 2 : 0;
     const int row = q * 32 + lane;
     const int n = n0 + row;
-    float* const red = reinterpret_cast<float*>(gbase);  // [splits][rpr][128], over the ring
+    float* const red = reinterpret_cast<float*>(gbase);  // over the (now idle) stage ring
     cluster_sync_all();  // every CTA of the cluster is past its mainloop: rings are free
     if (math) {
       tc_fence_after();
       const bool aborted = *abort_flag != 0;
       const uint32_t dt = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDCol;
-      const uint32_t red_base = smem_u32(red);
+      const uint32_t red_row = smem_u32(red) + static_cast<uint32_t>((seg * kTileN + row) * rpr_pad * 4);
       for (int c = h; c < BT / 16; c += 2) {
         if (16 * c >= mlim) break;
         uint32_t r[16];
         tmem_ld16(dt + 16 * c, r);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int ml = 16 * c + j;
+        for (int j = 0; j < 16; j += 4) {
+          const int ml = 16 * c + j;  // 4 consecutive rows, same owner (rpr % 4 == 0)
           if (ml < mlim) {
             const int owner = ml / rpr;
             const int local = ml - owner * rpr;
-            const uint32_t addr =
-                red_base + static_cast<uint32_t>(((seg * rpr + local) * kTileN + row) * 4);
-            st_dsmem_f32(mapa_shared(addr, owner), aborted ? __int_as_float(0x7fc00000) : __uint_as_float(r[j]));
+            const uint32_t addr = mapa_shared(red_row + static_cast<uint32_t>(local * 4), owner);
+            if (aborted) {
+              const float nanv = __int_as_float(0x7fc00000);
+              st_dsmem_v4(addr, nanv, nanv, nanv, nanv);
+            } else {
+              st_dsmem_v4(addr, __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+            }
           }
         }
       }
@@ -350,14 +397,28 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
     }
     cluster_sync_all();  // all pushes landed
     if (math) {
-      const int hi = min(mlim, (seg + 1) * rpr);
-      for (int ml = seg * rpr + h; ml < hi; ml += 2) {
-        const int local = ml - seg * rpr;
-        float acc = 0.0f;
-        for (int src = 0; src < splits; ++src) acc += red[(src * rpr + local) * kTileN + row];
-        const int m = m0 + ml;
-        if (p.x_scale) acc *= __ldg(p.x_scale + m);
-        store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, acc);
+      const int lo = seg * rpr;
+      const int hi = min(mlim, lo + rpr);
+      for (int l4 = 4 * h; lo + l4 < hi; l4 += 8) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int src = 0; src < splits; ++src) {
+          const float4 v = *reinterpret_cast<const float4*>(red + (src * kTileN + row) * rpr_pad + l4);
+          acc.x += v.x;
+          acc.y += v.y;
+          acc.z += v.z;
+          acc.w += v.w;
+        }
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int ml = lo + l4 + e;
+          if (ml < hi) {
+            const int m = m0 + ml;
+            float val = a4[e];
+            if (p.x_scale) val *= __ldg(p.x_scale + m);
+            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
+          }
+        }
       }
     }
   }
@@ -374,9 +435,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 32) ? 2 : 1)
 }
 
 template <int BT, int XK>
-static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
-                             cudaStream_t st) {
+static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
+                             const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t st) {
   using C = Cfg<BT>;
   static unsigned long long attr_mask = 0;  // one bit per device that has the attribute set
   int dev = 0;
@@ -401,27 +461,25 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
   attr[0].val.clusterDim.z = p.splits;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_w, tm_aug, tm_s, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_aug, tm_s, p);
 }
 
 template <int XK>
-static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                             const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
-                             cudaStream_t st) {
+static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
+                             const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t st) {
   switch (bt) {
-    case 32: return launch_bt<32, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
-    case 64: return launch_bt<64, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
-    case 128: return launch_bt<128, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
-    case 256: return launch_bt<256, XK>(tm_x, tm_w, tm_aug, tm_s, p, st);
+    case 32: return launch_bt<32, XK>(tm_x, tm_aug, tm_s, p, st);
+    case 64: return launch_bt<64, XK>(tm_x, tm_aug, tm_s, p, st);
+    case 128: return launch_bt<128, XK>(tm_x, tm_aug, tm_s, p, st);
+    case 256: return launch_bt<256, XK>(tm_x, tm_aug, tm_s, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
-                        cudaStream_t stream) {
-  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_w, tm_aug, tm_s, p, stream)
-                          : launch_xk<kXF16>(bt, tm_x, tm_w, tm_aug, tm_s, p, stream);
+cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
+                        const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t stream) {
+  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_aug, tm_s, p, stream)
+                          : launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, p, stream);
 }
 
 // Device address of the status word (host side), looked up once per device.

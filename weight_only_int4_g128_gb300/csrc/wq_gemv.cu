@@ -15,9 +15,9 @@
 // row are scalars, so promotion costs 32 FMAs per 128 weights.
 //
 //   warp 0      TMA producer, per 128-k block: activation tile [16 x 128 k]
-//               (two 128-byte swizzled boxes), packed weight tile [128 n x 16
-//               words] (64-byte swizzle), and the scale and delta rows of the
-//               block's group for the tile's 128 columns
+//               (one 3-D box = two 128-byte swizzled atoms) and the packed
+//               weight tile (one contiguous 8 KB block, bulk copy); per 8
+//               groups: the scale and delta rows of the tile's 128 columns
 //   warp 1      TMEM owner; lane 0 issues tcgen05.mma into a ring of 4 D buffers
 //   warp 2      group sums of the activation tile
 //   warps 3..6  dequant: each thread one weight row, 16 words -> 64 exact
@@ -42,13 +42,15 @@ constexpr int kBT = 16;
 constexpr int kXStage = kBT * kKBlock * 2;              // 4 KB
 constexpr int kXAtom = kBT * 128;                       // 2 KB
 constexpr int kWStage = kTileN * kWordsPerKBlock * 4;   // 8 KB
-constexpr int kSStage = kTileN * 2;                     // scale row, fp16
-constexpr int kDStage = kTileN * 4;                     // delta row, fp32
+constexpr int kChunk = 8;  // groups per scale/delta chunk (the index math uses >> 3)
+constexpr int kSChunk = kChunk * kTileN * 2;            // scale rows of a chunk, fp16 (2 KB)
+constexpr int kDChunk = kChunk * kTileN * 4;            // delta rows of a chunk, fp32 (4 KB)
+constexpr int kChunkSlots = 2;
 constexpr int kDCol = kNSA * 64;                        // 192
 constexpr int kTmemCols = 256;
 constexpr int kThreads = 352;  // 11 warps
-constexpr int kNumBars = 4 * kNSX + kNSA + kNB + 1;
-constexpr int kSmemBytes = 1024 + kNSX * (kXStage + kWStage + kSStage + kDStage) +
+constexpr int kNumBars = 4 * kNSX + kNSA + kNB + 1 + 2 * kChunkSlots;
+constexpr int kSmemBytes = 1024 + kNSX * (kXStage + kWStage) + kChunkSlots * (kSChunk + kDChunk) +
                            kNSX * kBT * 4 + kNumBars * 8 + 16;
 constexpr int kMaxSplits = 8;  // portable cluster size
 static_assert(kNB + kNSA < kNSX, "stages are released after promotion");
@@ -77,9 +79,8 @@ __device__ __forceinline__ float hi_to_f32(uint32_t u, int xk) {
 
 template <int XK>
 __global__ void __launch_bounds__(gemv::kThreads, 2)
-    gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_d,
-                const GemmParams p, unsigned* status) {
+    gemv_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_s,
+                const __grid_constant__ CUtensorMap tm_d, const GemmParams p, unsigned* status) {
   using namespace gemv;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -87,9 +88,8 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
   uint8_t* const gbase = smem_raw + (base - raw);
   const uint32_t sx = base;
   const uint32_t sw = sx + kNSX * kXStage;
-  const uint32_t ss = sw + kNSX * kWStage;
-  const uint32_t sd = ss + kNSX * kSStage;
-  const uint32_t sasum = sd + kNSX * kDStage;
+  const uint32_t sch = sw + kNSX * kWStage;  // scale/delta chunk slots: [slot][S 2 KB | delta 4 KB]
+  const uint32_t sasum = sch + kChunkSlots * (kSChunk + kDChunk);
   const uint32_t sbar = sasum + kNSX * kBT * 4;
   // Barriers.  Per stage s (k-block it, s = it % kNSX):
   //   full_x    TMA bytes of the stage landed
@@ -106,12 +106,15 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
   auto full_a = [&](int a) { return sbar + 8u * (4 * kNSX + a); };
   auto empty_d = [&](int b) { return sbar + 8u * (4 * kNSX + kNSA + b); };
   const uint32_t done_bar = sbar + 8u * (4 * kNSX + kNSA + kNB);
+  // full_c / empty_c: scale+delta rows of 8 consecutive groups (one chunk) landed /
+  // released by the promotion warps.
+  auto full_c = [&](int c) { return sbar + 8u * (4 * kNSX + kNSA + kNB + 1 + c); };
+  auto empty_c = [&](int c) { return sbar + 8u * (4 * kNSX + kNSA + kNB + 1 + kChunkSlots + c); };
   uint8_t* const gmisc = gbase + (sbar + 8u * kNumBars - base);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gmisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gmisc + 4);
   float* const asum_ring = reinterpret_cast<float*>(gbase + (sasum - base));
-  const __half* const s_ring = reinterpret_cast<const __half*>(gbase + (ss - base));
-  const float* const d_ring = reinterpret_cast<const float*>(gbase + (sd - base));
+  const uint8_t* const chunk_smem = gbase + (sch - base);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -120,11 +123,40 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
   const int kb0 = seg * p.kb_per_split;
   const int nkb = max(0, min(p.kb_total, kb0 + p.kb_per_split) - kb0);
   const bool has_delta = p.delta != nullptr;
-  const uint32_t stage_tx = kXStage + kWStage + kSStage + (has_delta ? kDStage : 0);
+  const uint32_t stage_tx = kXStage + kWStage;
+  const uint32_t chunk_tx = kSChunk + (has_delta ? kDChunk : 0);
+  // group size is 128 (group = k-block) or K (one group per column)
+  const bool per_channel = p.group_size != kKBlock;
+  const int g_first = per_channel ? 0 : kb0;  // first group of this K segment
+  // chunk ordinal (0, 1, ...) of the k-block `it` of this segment, and its row (chunks of 8 groups)
+  auto chunk_of = [&](int it) { return per_channel ? 0 : ((kb0 + it) >> 3) - (g_first >> 3); };
+  auto chunk_row = [&](int it) { return per_channel ? 0 : ((kb0 + it) & 7); };
+  int chunks_loaded = 0;  // producer lane: chunk ordinals [0, chunks_loaded) are issued
+  // Weight-side copies of k-block `it` (producer lane only): the packed tile, and the
+  // scale/delta chunk when the k-block starts a new one.
+  auto weight_copies = [&](int it, const WaitCtx& wc) -> bool {
+    const int o = chunk_of(it);
+    if (o >= chunks_loaded) {
+      const int slot = o % kChunkSlots;
+      if (!mbar_wait(empty_c(slot), ((o / kChunkSlots) & 1) ^ 1, wc)) return false;
+      const int grow = ((g_first >> 3) + o) * kChunk;
+      const uint32_t dst = sch + slot * (kSChunk + kDChunk);
+      mbar_arrive_expect_tx(full_c(slot), chunk_tx);
+      tma_load_2d(dst, &tm_s, full_c(slot), n0, grow);
+      if (has_delta) tma_load_2d(dst + kSChunk, &tm_d, full_c(slot), n0, grow);
+      chunks_loaded = o + 1;
+    }
+    const int s = it % kNSX;
+    mbar_arrive_expect_tx(full_x(s), stage_tx);
+    // packed weight tile: one contiguous 8 KB block of the blocked layout
+    bulk_load(sw + s * kWStage, p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb0 + it) * 2048,
+              kWStage, full_x(s));
+    return true;
+  };
+  const int pre = p.weight_prefetch ? min(kNSX, nkb) : 0;
 
   if (threadIdx.x == 0) {
     prefetch_tensormap(&tm_x);
-    prefetch_tensormap(&tm_w);
     prefetch_tensormap(&tm_s);
     if (has_delta) prefetch_tensormap(&tm_d);
     for (int s = 0; s < kNSX; ++s) {
@@ -135,9 +167,18 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
     }
     for (int a = 0; a < kNSA; ++a) mbar_init(full_a(a), 4);
     for (int b = 0; b < kNB; ++b) mbar_init(empty_d(b), 4);  // promotion warps
+    for (int c = 0; c < kChunkSlots; ++c) {
+      mbar_init(full_c(c), 1);
+      mbar_init(empty_c(c), 4);  // promotion warps
+    }
     mbar_init(done_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // Weight-side copies of the first stages go out before anything else (fresh
+    // stages and chunk slots: nothing to wait for); see the note below.
+    volatile int never = 0;
+    const WaitCtx nowait{&never, 1000000ull, kDevTimeoutProducer, status};
+    for (int it = 0; it < pre; ++it) weight_copies(it, nowait);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(gmisc), kTmemCols);
@@ -148,28 +189,36 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Programmatic dependent launch: nothing before griddep_wait() touches memory
+  // the preceding grid may write (X, Y).  Only the weight-side copies (packed
+  // codes, scales, delta) of the first stages may be issued earlier, and only
+  // when the caller enabled it (the weights must not be written by the
+  // preceding kernel).
   int issued = 0;  // TMA stages the producer lane has issued
   if (warp == 0) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, status};
+      griddep_wait();
       for (int it = 0; it < nkb; ++it) {
         const int s = it % kNSX;
-        const uint32_t prev = ((it / kNSX) & 1) ^ 1;  // phase of k-block it - kNSX
-        if (!mbar_wait(empty_x(s), prev, wc)) break;
-        if (!mbar_wait(mma_done(s), prev, wc)) break;
-        const int kb = kb0 + it;
-        const int g = (kb * kKBlock) / p.group_size;
-        mbar_arrive_expect_tx(full_x(s), stage_tx);
+        if (it >= pre) {
+          const uint32_t prev = ((it / kNSX) & 1) ^ 1;  // phase of k-block it - kNSX
+          if (!mbar_wait(empty_x(s), prev, wc)) break;
+          if (!mbar_wait(mma_done(s), prev, wc)) break;
+          if (!weight_copies(it, wc)) break;
+        }
         // activation tile [16 x 128 k]: one 3-D box {64 k, 16 rows, 2 halves of the k-block}
-        tma_load_3d(sx + s * kXStage, &tm_x, full_x(s), 0, 0, 2 * kb);
-        tma_load_2d(sw + s * kWStage, &tm_w, full_x(s), kb * kWordsPerKBlock, n0);
-        tma_load_2d(ss + s * kSStage, &tm_s, full_x(s), n0, g);
-        if (has_delta) tma_load_2d(sd + s * kDStage, &tm_d, full_x(s), n0, g);
+        tma_load_3d(sx + s * kXStage, &tm_x, full_x(s), 0, 0, 2 * (kb0 + it));
         issued = it + 1;
       }
+    } else {
+      griddep_wait();
     }
-  } else if (warp == 1) {
+  } else {
+    griddep_wait();
+  }
+  if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMma, status};
@@ -287,12 +336,17 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_d(b));
-      const float sc = __half2float(s_ring[sj * kTileN + row]);
+      const int o = chunk_of(j);
+      const int slot = o % kChunkSlots;
+      if (!warp_wait_g(full_c(slot), (o / kChunkSlots) & 1, wc)) break;
+      const uint8_t* chunk = chunk_smem + slot * (kSChunk + kDChunk);
+      const int gr = chunk_row(j);
+      const float sc = __half2float(reinterpret_cast<const __half*>(chunk)[gr * kTileN + row]);
 #pragma unroll
       for (int m = 0; m < kBT; ++m) acc[m] = fmaf(sc, __uint_as_float(r[m]), acc[m]);
       if (has_delta) {
         if (!warp_wait_g(asum_full(sj), (j / kNSX) & 1, wc)) break;
-        const float dl = d_ring[sj * kTileN + row];
+        const float dl = reinterpret_cast<const float*>(chunk + kSChunk)[gr * kTileN + row];
         const float4* a4 = reinterpret_cast<const float4*>(asum_ring + sj * kBT);
 #pragma unroll
         for (int v = 0; v < kBT / 4; ++v) {
@@ -304,7 +358,10 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty_x(sj));
+      if (lane == 0) {
+        mbar_arrive(empty_x(sj));
+        if (j + 1 == nkb || chunk_of(j + 1) != o) mbar_arrive(empty_c(slot));  // chunk done
+      }
     }
     tc_fence_before();
   }
@@ -312,6 +369,7 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
 
   // ---------------------------------------------------------------- split-K reduction + store
   __syncthreads();  // every role is past its loop
+  griddep_launch_dependents();  // the next grid in the stream may start its setup
   const bool aborted = *abort_flag != 0;
   if (aborted && warp == 0 && lane == 0) {
     // Let every copy the producer issued land before the shared memory is reused.
@@ -319,6 +377,8 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
     const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, status};
     for (int it = max(0, issued - kNSX); it < issued; ++it)
       mbar_wait(full_x(it % kNSX), (it / kNSX) & 1, drain);
+    for (int o = max(0, chunks_loaded - kChunkSlots); o < chunks_loaded; ++o)
+      mbar_wait(full_c(o % kChunkSlots), (o / kChunkSlots) & 1, drain);
   }
   __syncthreads();
   float* const red = reinterpret_cast<float*>(gbase + (sw - base));  // [16][128] fp32
@@ -352,9 +412,9 @@ __global__ void __launch_bounds__(gemv::kThreads, 2)
 }
 
 template <int XK>
-static cudaError_t launch_gemv_xk(const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                                  const CUtensorMap& tm_s, const CUtensorMap& tm_d,
-                                  const GemmParams& p, unsigned* status, cudaStream_t st) {
+static cudaError_t launch_gemv_xk(const CUtensorMap& tm_x, const CUtensorMap& tm_s,
+                                  const CUtensorMap& tm_d, const GemmParams& p, unsigned* status,
+                                  cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -371,26 +431,27 @@ static cudaError_t launch_gemv_xk(const CUtensorMap& tm_x, const CUtensorMap& tm
   cfg.blockDim = dim3(gemv::kThreads, 1, 1);
   cfg.dynamicSmemBytes = gemv::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = p.splits;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK>, tm_x, tm_w, tm_s, tm_d, p, status);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK>, tm_x, tm_s, tm_d, p, status);
 }
 
 int gemv_max_splits() { return gemv::kMaxSplits; }
 
-cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_s, const CUtensorMap& tm_d, const GemmParams& p,
-                        cudaStream_t stream) {
+cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s,
+                        const CUtensorMap& tm_d, const GemmParams& p, cudaStream_t stream) {
   unsigned* status = status_word();
   if (!status) return cudaErrorInvalidSymbol;
   if (p.splits < 1 || p.splits > gemv::kMaxSplits) return cudaErrorInvalidValue;
-  return x_kind == kXBF16 ? launch_gemv_xk<kXBF16>(tm_x, tm_w, tm_s, tm_d, p, status, stream)
-                          : launch_gemv_xk<kXF16>(tm_x, tm_w, tm_s, tm_d, p, status, stream);
+  return x_kind == kXBF16 ? launch_gemv_xk<kXBF16>(tm_x, tm_s, tm_d, p, status, stream)
+                          : launch_gemv_xk<kXF16>(tm_x, tm_s, tm_d, p, status, stream);
 }
 
 }  // namespace wq

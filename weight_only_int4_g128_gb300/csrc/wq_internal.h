@@ -36,6 +36,7 @@ struct GemmParams {
   int splits;            // number of K segments (one thread-block cluster per tile)
   int aug_stages;        // correction stages (Kaug / 128), 0 when there is no correction
   int kaug;              // padded correction length (multiple of 128)
+  const uint32_t* B;     // packed weights, blocked layout (one 8 KB block per tile, k-block)
   const __half* S;       // [G][N] group scales
   const float* delta;    // [G][N] zero-point residual, or null
   const __nv_bfloat16* delta_aug;  // [N][kaug] correction columns (large-M kernel)
@@ -43,17 +44,16 @@ struct GemmParams {
   void* Y;               // [M][N]
   int y_kind;
   unsigned long long timeout_ns;
+  int weight_prefetch;   // issue weight copies before waiting on the preceding grid
 };
 
 // Host-side launchers (wq_gemm.cu, wq_gemv.cu).
-cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_s, const CUtensorMap& tm_d, const GemmParams& p,
-                        cudaStream_t stream);
+cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s,
+                        const CUtensorMap& tm_d, const GemmParams& p, cudaStream_t stream);
 int gemv_max_splits();
 unsigned* status_word();
-cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_w,
-                        const CUtensorMap& tm_aug, const CUtensorMap& tm_s, const GemmParams& p,
-                        cudaStream_t stream);
+cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
+                        const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes(int bt);
 
 // Pre-pass kernels (wq_kernels.cu).

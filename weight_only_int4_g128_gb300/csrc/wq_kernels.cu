@@ -12,44 +12,51 @@ namespace wq {
 // HyperQwen W4A8 article, section "hidden mine": negative group scales fold
 // into the codes, s -> -s, v -> 16 - v clamped to 15).
 //
-// Layout: Bpacked[n][K/8]; word (n, w) holds codes q[8w + j][n] with code j at
-// bit 4*(j/2) + 16*(j%2).  A 32 (n) x 32 (word) tile goes through shared
-// memory so that both the code reads and the word writes are coalesced.
+// Layout (this library's own): the word for column n and codes k = 8w..8w+7
+// holds q[8w + j][n] with code j at bit 4*(j/2) + 16*(j%2).  Words are grouped
+// in blocks of 128 columns x 128 k (2048 words = 8 KB), one block per GEMM
+// weight tile, blocks ordered column-tile major then k-block; inside a block
+// row r = n % 128 holds its 16 words as four 16-byte chunks, chunk c stored in
+// slot c ^ ((r / 2) % 4) so that rows can be read from shared memory without
+// bank conflicts after a plain bulk copy.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ int code_shift(int j) { return 4 * (j >> 1) + 16 * (j & 1); }
+
+// word index (blocked layout) -> (column n, word w along K)
+__device__ __forceinline__ void word_coords(long long idx, int K, int& n, int& w) {
+  const int KB = K / kKBlock;
+  const long long block = idx >> 11;          // 2048 words per block
+  const int within = static_cast<int>(idx & 2047);
+  const int r = within >> 4;
+  const int slot = within & 15;
+  const int c = (slot >> 2) ^ ((r >> 1) & 3);
+  const int u = 4 * c + (slot & 3);
+  const int tile_n = static_cast<int>(block / KB);
+  const int kb = static_cast<int>(block - static_cast<long long>(tile_n) * KB);
+  n = tile_n * kTileN + r;
+  w = kb * kWordsPerKBlock + u;
+}
+
 __global__ void pack_kernel(const uint8_t* __restrict__ q, const __half* __restrict__ scale,
                             int fold, uint32_t* __restrict__ Bpacked, int K, int N,
                             int group_size) {
-  __shared__ uint32_t tile[32][33];
-  const int KW = K / 8;
-  const int w0 = blockIdx.x * 32;
-  const int nb = blockIdx.y * 32;
-  const int tx = threadIdx.x;  // 0..31
-  const int ty = threadIdx.y;  // 0..7
-  const int n = nb + tx;
-  for (int r = ty; r < 32; r += 8) {
-    const int w = w0 + r;
-    uint32_t word = 0;
-    if (w < KW && n < N) {
-      bool neg = false;
-      if (fold) {
-        const int g = (8 * w) / group_size;
-        neg = __half2float(scale[static_cast<size_t>(g) * N + n]) < 0.0f;
-      }
+  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<long long>(K / 8) * N) return;
+  int n, w;
+  word_coords(idx, K, n, w);
+  bool neg = false;
+  if (fold) {
+    const int g = (8 * w) / group_size;
+    neg = __half2float(scale[static_cast<size_t>(g) * N + n]) < 0.0f;
+  }
+  uint32_t word = 0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        uint32_t v = q[static_cast<size_t>(8 * w + j) * N + n] & 0xFu;
-        if (neg) v = min(16u - v, 15u);
-        word |= v << (4 * (j >> 1) + 16 * (j & 1));
-      }
-    }
-    tile[r][tx] = word;
+  for (int j = 0; j < 8; ++j) {
+    uint32_t v = q[static_cast<size_t>(8 * w + j) * N + n] & 0xFu;
+    if (neg) v = min(16u - v, 15u);
+    word |= v << code_shift(j);
   }
-  __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int nn = nb + r;
-    const int w = w0 + tx;
-    if (nn < N && w < KW) Bpacked[static_cast<size_t>(nn) * KW + w] = tile[tx][r];
-  }
+  Bpacked[idx] = word;
 }
 
 // S = |scale| (fold) or scale; delta = fp32(zero) + 8 * fp32(scale) rounded once.
@@ -69,27 +76,25 @@ __global__ void pack_scales_kernel(const __half* __restrict__ scale, const __hal
 
 __global__ void unpack_kernel(const uint32_t* __restrict__ Bpacked, uint8_t* __restrict__ q, int K,
                               int N) {
-  const int KW = K / 8;
-  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (i >= static_cast<long long>(KW) * N) return;
-  const int n = static_cast<int>(i % N);  // n fastest: coalesced code writes
-  const int w = static_cast<int>(i / N);
-  const uint32_t word = Bpacked[static_cast<size_t>(n) * KW + w];
+  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<long long>(K / 8) * N) return;
+  int n, w;
+  word_coords(idx, K, n, w);
+  const uint32_t word = Bpacked[idx];
 #pragma unroll
   for (int j = 0; j < 8; ++j)
-    q[static_cast<size_t>(8 * w + j) * N + n] = (word >> (4 * (j >> 1) + 16 * (j & 1))) & 0xFu;
+    q[static_cast<size_t>(8 * w + j) * N + n] = (word >> code_shift(j)) & 0xFu;
 }
 
 // W[k][n] = RN((v - 8) * s) in fp16 or bf16: the same dequant routines the
 // GEMM uses, exposed so the dequantized weights can be checked bit for bit.
 __global__ void dequant_kernel(const uint32_t* __restrict__ Bpacked, const __half* __restrict__ S,
                                void* __restrict__ W, int w_kind, int K, int N, int group_size) {
-  const int KW = K / 8;
-  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (i >= static_cast<long long>(KW) * N) return;
-  const int n = static_cast<int>(i % N);
-  const int w = static_cast<int>(i / N);
-  const uint32_t word = Bpacked[static_cast<size_t>(n) * KW + w];
+  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<long long>(K / 8) * N) return;
+  int n, w;
+  word_coords(idx, K, n, w);
+  const uint32_t word = Bpacked[idx];
   const int g = (8 * w) / group_size;
   const __half sc = S[static_cast<size_t>(g) * N + n];
   uint32_t o[4];
@@ -285,8 +290,9 @@ __global__ void i8_to_f16_kernel(const int8_t* __restrict__ Xq, __half* __restri
 cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
                         uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,
                         cudaStream_t st) {
-  dim3 grid((K / 8 + 31) / 32, (N + 31) / 32);
-  pack_kernel<<<grid, dim3(32, 8), 0, st>>>(q, scale, fold, Bpacked, K, N, group_size);
+  const long long words = static_cast<long long>(K / 8) * N;
+  pack_kernel<<<static_cast<unsigned>((words + 255) / 256), 256, 0, st>>>(q, scale, fold, Bpacked, K,
+                                                                          N, group_size);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const long long count = static_cast<long long>(K / group_size) * N;
