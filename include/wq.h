@@ -172,6 +172,25 @@ int wq_quantize_per_token(const void* x, int8_t* Xq, float* x_scale, int M, int 
 int wq_set_option(int option, long long value);
 int wq_get_option(int option, long long* value);
 
+/*
+ * wq_gemm_w4a16 without a workspace argument, for callers that cannot
+ * allocate device memory where they make the call (inside a framework that
+ * forbids allocations outside its own allocator, host code that runs during
+ * CUDA stream capture, latency-critical loops where cudaMalloc could
+ * synchronize).  The pages have no counterpart to this entry point.
+ *   Arguments and result as wq_gemm_w4a16.  The scratch comes from a 16 MiB
+ *   array of device memory inside the library image (held by every GPU that
+ *   loads the library until the process exits); problems that need more
+ *   (wq_workspace_size > 16 MiB) return WQ_ERR_WORKSPACE without launching.
+ *   Nothing is allocated or freed.  The first call on a device looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before capturing a stream.  All calls on a device share the array, so
+ *   calls whose kernels may overlap on the GPU (different streams) race on it.
+ */
+int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S,
+                          const float* delta, void* Y, int y_dtype, int M, int N, int K,
+                          int group_size, void* stream);
+
 /* Bytes of workspace the GEMM needs for this problem (0 if none). */
 size_t wq_workspace_size(int variant, int M, int N, int K, int group_size);
 

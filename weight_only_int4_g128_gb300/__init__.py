@@ -50,6 +50,7 @@ EXPORTS = {
     "wq_device_status": (_I, [ctypes.POINTER(ctypes.c_uint), _I, _P]),
     "wq_debug_wait_probe": (_I, [ctypes.c_ulonglong, _P]),
     "wq_set_option": (_I, [_I, ctypes.c_longlong]),
+    "wq_gemm_w4a16_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wq_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
 }
 OPTION_WEIGHT_PREFETCH = 1

@@ -282,6 +282,16 @@ int y_kind_of(int y_dtype) {
 
 }  // namespace
 
+namespace wq {
+int set_last_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_err, sizeof(t_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+}  // namespace wq
+
 extern "C" {
 
 int wq_device_supported(int device) {

@@ -47,6 +47,9 @@ struct GemmParams {
   int weight_prefetch;   // issue weight copies before waiting on the preceding grid
 };
 
+// Record the message for wq_last_error() on this thread and return `code`.
+int set_last_error(int code, const char* fmt, ...);
+
 // Host-side launchers (wq_gemm.cu, wq_gemv.cu).
 cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s,
                         const CUtensorMap& tm_d, const GemmParams& p, cudaStream_t stream);
