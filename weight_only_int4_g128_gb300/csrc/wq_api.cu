@@ -147,14 +147,32 @@ int make_map_x3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64
   return WQ_OK;
 }
 
+// Decode activation components [rows][K] bytes as a 3-D tensor {128 bytes of a
+// k-block, rows, K/128 k-blocks}: one box {128, rows, 2} fetches two k-blocks'
+// tiles, each rows x 128 B with 128-byte swizzling, one after the other.
+int make_map_b3d(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t K) {
+  EncodeFn enc = get_encode();
+  if (!enc) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  cuuint64_t dims[3] = {128, rows, K / 128};
+  cuuint64_t strides[2] = {K, 128};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled (decode components) failed (%d)", static_cast<int>(r));
+  return WQ_OK;
+}
+
 // ---------------------------------------------------------------- heuristics
 struct Plan {
-  bool gemv;      // M <= 16: decode kernel (single launch for W4A16)
+  bool gemv;      // M <= 16: decode pre-pass + decode kernel
   int bt;         // token tile
   int splits;
   int kb_per_split;
   int kaug;       // large-M correction length (0 without correction or for the decode kernel)
-  size_t off_aug, off_daug, off_x16;  // byte offsets into the workspace
+  size_t off_aug, off_daug, off_x16;  // byte offsets into the workspace (large M)
+  size_t off_x8;                      // byte offset into the workspace (decode)
   size_t bytes;
 };
 
@@ -177,7 +195,7 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   // one thread-block cluster and are reduced through distributed shared memory.
   int splits = slots / tiles;
   if (splits < 1) splits = 1;
-  const int max_splits = p.gemv ? wq::gemv_max_splits() : kMaxClusterSplits;
+  const int max_splits = p.gemv ? wq::decode_max_splits() : kMaxClusterSplits;
   if (splits > max_splits) splits = max_splits;
   if (splits > kb) splits = kb;
   p.kb_per_split = (kb + splits - 1) / splits;
@@ -189,7 +207,10 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   p.off_daug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
   p.off_x16 = off;
-  if (variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(M) * K * 2);
+  if (variant == WQ_VARIANT_W4A8 && !p.gemv) off = align256(off + static_cast<size_t>(M) * K * 2);
+  // decode: e4m3 activation components + per-block sums/factors row, padded: [56][K] bytes
+  p.off_x8 = off;
+  if (p.gemv) off = align256(off + static_cast<size_t>(wq::decode_b_rows()) * K);
   p.bytes = off;
   return p;
 }
@@ -205,6 +226,44 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   uint8_t* wsb = static_cast<uint8_t*>(ws);
   const int G = K / gs;
   cudaError_t e;
+
+  if (plan.gemv) {
+    // decode: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
+    uint8_t* x8 = wsb + plan.off_x8;
+    const int pk = (variant == WQ_VARIANT_W4A8) ? wq::kXI8 : x_kind;
+    e = wq::launch_decode_prep(X, pk, M, K, x_scale, x8, st);
+    if (e != cudaSuccess) return cuda_fail(e, "decode activation pre-pass");
+    CUtensorMap tm_b, tm_s, tm_d;
+    int rc = make_map_b3d(&tm_b, x8, wq::decode_b_rows(), K);
+    if (rc) return rc;
+    rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+    if (delta && variant == WQ_VARIANT_W4A16) {
+      rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc) return rc;
+    } else {
+      tm_d = tm_s;  // unused
+    }
+    wq::GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.group_size = gs;
+    p.G = G;
+    p.kb_total = K / 128;
+    p.kb_per_split = plan.kb_per_split;
+    p.splits = plan.splits;
+    p.B = Bpacked;
+    p.S = static_cast<const __half*>(S);
+    p.delta = (variant == WQ_VARIANT_W4A16) ? delta : nullptr;
+    p.Y = Y;
+    p.y_kind = y_kind;
+    p.timeout_ns = timeout_ns();
+    p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+    p.x_scale = nullptr;  // folded into the pre-pass factors
+    e = wq::launch_decode(tm_b, tm_s, tm_d, p, st);
+    return after_launch(e, name, st);
+  }
 
   const void* xg = X;
   if (variant == WQ_VARIANT_W4A8) {
@@ -263,11 +322,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.y_kind = y_kind;
   p.timeout_ns = timeout_ns();
   p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
-  if (plan.gemv) {
-    e = wq::launch_gemv(x_kind, tm_x, tm_s, tm_d, p, st);
-  } else {
-    e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_aug, tm_s, p, st);
-  }
+  e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_aug, tm_s, p, st);
   return after_launch(e, name, st);
 }
 

@@ -23,7 +23,7 @@ constexpr unsigned kDevTimeoutMath = 1u << 2;
 constexpr unsigned kDevTimeoutFixup = 1u << 3;
 constexpr unsigned kDevTimeoutProbe = 1u << 4;
 
-enum XKind { kXF16 = 0, kXBF16 = 1 };
+enum XKind { kXF16 = 0, kXBF16 = 1, kXI8 = 2 };
 enum YKind { kYF16 = 0, kYBF16 = 1, kYF32 = 2 };
 
 
@@ -50,10 +50,13 @@ struct GemmParams {
 // Record the message for wq_last_error() on this thread and return `code`.
 int set_last_error(int code, const char* fmt, ...);
 
-// Host-side launchers (wq_gemm.cu, wq_gemv.cu).
-cudaError_t launch_gemv(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s,
-                        const CUtensorMap& tm_d, const GemmParams& p, cudaStream_t stream);
-int gemv_max_splits();
+// Host-side launchers (wq_gemm.cu, wq_decode.cu).
+cudaError_t launch_decode_prep(const void* X, int x_kind, int M, int K, const float* x_scale, uint8_t* X8,
+                               cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& tm_b, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
+                          const GemmParams& p, cudaStream_t stream);
+int decode_max_splits();
+int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
                         const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t stream);
