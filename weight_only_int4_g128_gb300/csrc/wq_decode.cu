@@ -16,7 +16,7 @@
 //    x / sigma = c1 + c2/16 + c3/256 up to 2^-12 relative (about one bit finer
 //    than fp16), and stores the block's fp32 sum of x and the factor
 //    f = sigma * 2^9.  The 48 = 3 x 16 component rows are the MMA's N.
-//  * Per 128-k block (group g) the kernel has D[n][c*16+m] = sum_k v[k][n] *
+//  * Per 128-k block (group g) the kernel has D[n][3m+c] = sum_k v[k][n] *
 //    c_c[m][k] * 2^-9 in TMEM, and the promotion warps accumulate in fp32
 //        acc[n][m] += s[g][n] * f[m] * (D1 + D2/16 + D3/256) + zero[g][n] * asum[m]
 //    with zero = delta - 8 s ("Marlin INT4 on Ada -- how it works", section "The
@@ -111,8 +111,9 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 // ---------------------------------------------------------------------------
 // Pre-pass: one warp per (token row m < 16, 128-k block kb); lane l holds
 // k = 128 kb + 4 l .. + 3.
-//   X8 rows c*16 + m (c = 0, 1, 2), bytes [128 kb, 128 kb + 128): e4m3
+//   X8 rows 3 m + c (c = 0, 1, 2), bytes [128 kb, 128 kb + 128): e4m3
 //       components of x[m][k] / sigma, sigma = 2^(e - 8) with max |x| < 2^e
+//       (token-major, so that M tokens occupy the first 3 M rows)
 //   X8 row 48, bytes [128 kb, 128 kb + 128): fp32 asum[16] = xs[m] * sum x,
 //       then fp32 f[16] = xs[m] * sigma * 2^9 (xs = W4A8 token scale, else 1;
 //       f = NaN when the block holds inf or NaN)
@@ -162,9 +163,9 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const void* X, int M, 
   griddep_wait();
   if (kb >= nkb) return;
   const size_t o = static_cast<size_t>(kb) * kKBlock + lane * 4;
-  uint32_t* const r1 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(m) * K + o);
-  uint32_t* const r2 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(dec::kMT + m) * K + o);
-  uint32_t* const r3 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(2 * dec::kMT + m) * K + o);
+  uint32_t* const r1 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m) * K + o);
+  uint32_t* const r2 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m + 1) * K + o);
+  uint32_t* const r3 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m + 2) * K + o);
   float* const srow = reinterpret_cast<float*>(X8 + static_cast<size_t>(dec::kBN) * K + static_cast<size_t>(kb) * kKBlock);
   if (m >= M) {
     *r1 = 0u;
@@ -221,6 +222,72 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const void* X, int M, 
     const float xs = x_scale ? x_scale[m] : 1.0f;
     srow[m] = sum * xs;
     srow[dec::kMT + m] = bad ? __int_as_float(0x7fc00000) : f * xs;
+  }
+}
+
+// Promotion loop of the decode kernel (warps 6..9): per 128-k block, read the
+// block's D (G groups of 16 fp32 columns: tokens 0 .. 16 G / 3), combine the
+// three components, and accumulate s * f * D + zero * asum in fp32.  Barrier
+// addresses follow the kernel's layout (see decode_kernel).
+template <int G>
+__device__ __forceinline__ void promote_loop(const GemmParams& p, uint32_t tmem_lane, const uint8_t* bring,
+                                             const uint8_t* chunk_smem, uint32_t sbar, int nkb, int kb0, int row,
+                                             volatile int* abort_flag, unsigned* status, float (&acc)[dec::kMT]) {
+  using namespace dec;
+  constexpr int T = (16 * G) / 3;  // tokens whose three columns are loaded
+  auto full_g = [&](int g) { return sbar + 8u * g; };
+  auto mma_done = [&](int s) { return sbar + 8u * (kNG + s); };
+  auto pdone = [&](int s) { return sbar + 8u * (kNG + kNSX + s); };
+  auto full_c = [&](int c) { return sbar + 8u * (kNG + 2 * kNSX + kNSA + c); };
+  auto empty_c = [&](int c) { return sbar + 8u * (kNG + 2 * kNSX + kNSA + kChunkSlots + c); };
+  const bool per_channel = p.group_size != kKBlock;
+  const int g_first = per_channel ? 0 : kb0;
+  auto chunk_of = [&](int it) { return per_channel ? 0 : ((kb0 + it) >> 3) - (g_first >> 3); };
+  auto chunk_row = [&](int it) { return per_channel ? 0 : ((kb0 + it) & 7); };
+  const bool has_delta = p.delta != nullptr;
+  const int lane = threadIdx.x & 31;
+  const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, status};
+  for (int j = 0; j < nkb; ++j) {
+    const int s = j % kNSX;
+    const int b = j % kNB;
+    // operands that do not depend on the MMAs first: the block's sums and factors
+    // (the TMA copy that wrote them completed full_g) and the row's scale and delta
+    if (!warp_wait(full_g(s / kPair), (j / kNSX) & 1, wc)) break;
+    float as[kMT], fs[kMT];
+    const float4* srow = reinterpret_cast<const float4*>(bring + s * kBStage + kBN * 128);
+#pragma unroll
+    for (int v4 = 0; v4 < (T + 3) / 4; ++v4) {
+      const float4 t = srow[v4];
+      const float4 u = srow[kMT / 4 + v4];
+      as[4 * v4] = t.x; as[4 * v4 + 1] = t.y; as[4 * v4 + 2] = t.z; as[4 * v4 + 3] = t.w;
+      fs[4 * v4] = u.x; fs[4 * v4 + 1] = u.y; fs[4 * v4 + 2] = u.z; fs[4 * v4 + 3] = u.w;
+    }
+    const int o = chunk_of(j);
+    const int slot = o % kChunkSlots;
+    if (!warp_wait(full_c(slot), (o / kChunkSlots) & 1, wc)) break;
+    const uint8_t* chunk = chunk_smem + slot * (kSChunk + kDChunk);
+    const int gr = chunk_row(j);
+    const float sc = __half2float(reinterpret_cast<const __half*>(chunk)[gr * kTileN + row]);
+    const float dl = has_delta ? reinterpret_cast<const float*>(chunk + kSChunk)[gr * kTileN + row] : 0.0f;
+    const float zero = fmaf(-8.0f, sc, dl);  // delta - 8 s: the zero point
+    __syncwarp();
+    if (lane == 0 && (j + 1 == nkb || chunk_of(j + 1) != o)) mbar_arrive(empty_c(slot));
+    if (!warp_wait(mma_done(s), (j / kNSX) & 1, wc)) break;
+    tc_fence_after();
+    uint32_t d[16 * G];
+    const uint32_t dcol = tmem_lane + kDCol0 + b * kBN;
+#pragma unroll
+    for (int g = 0; g < G; ++g) tmem_ld16(dcol + 16 * g, *reinterpret_cast<uint32_t(*)[16]>(d + 16 * g));
+    tmem_wait_ld();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(pdone(s));
+#pragma unroll
+    for (int m = 0; m < T; ++m) {
+      const float val = fmaf(__uint_as_float(d[3 * m + 2]), 1.0f / 256.0f,
+                             fmaf(__uint_as_float(d[3 * m + 1]), 1.0f / 16.0f, __uint_as_float(d[3 * m])));
+      acc[m] = fmaf(zero, as[m], fmaf(sc * fs[m], val, acc[m]));
+    }
   }
 }
 
@@ -418,14 +485,19 @@ __global__ void __launch_bounds__(dec::kThreads, 2)
     // ---------------------------------------------------------------- dequant
     const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, status};
     const uint8_t* wring = gbase + (sw - base);
-    for (int it = 0; it < nkb; ++it) {
+    // the weight words of k-block it: 16 words of this thread's row (swizzled 16-byte chunks)
+    auto load_words = [&](int it, uint4 (&wv)[4]) -> bool {
       const int s = it % kNSX;
-      const int a = it % kNSA;
-      if (!warp_wait(full_g(s / kPair), (it / kNSX) & 1, wc)) break;
-      uint4 wv[4];
+      if (!warp_wait(full_g(s / kPair), (it / kNSX) & 1, wc)) return false;
       const uint8_t* wrow = wring + s * kWStage + row * 64;
 #pragma unroll
       for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ ((row >> 1) & 3)));
+      return true;
+    };
+    uint4 wv[4];
+    bool ok = nkb > 0 && load_words(0, wv);
+    for (int it = 0; ok && it < nkb; ++it) {
+      const int a = it % kNSA;
       // code j of a word sits at bit 4*(j/2) + 16*(j%2): t holds codes 0,4,1,5 and
       // u codes 2,6,3,7 in its bytes; two permutes restore k order.
       uint32_t v[32];
@@ -444,6 +516,8 @@ __global__ void __launch_bounds__(dec::kThreads, 2)
         tc_fence_after();
       }
       tmem_st32(tmem + lane_base + a * kACol, v);
+      // the next k-block's words load while the store completes
+      if (it + 1 < nkb) ok = load_words(it + 1, wv);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
@@ -451,57 +525,14 @@ __global__ void __launch_bounds__(dec::kThreads, 2)
     }
   } else {
     // ---------------------------------------------------------------- promotion
-    const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, status};
-    const uint8_t* bring = gbase + (sb - base);
-    for (int j = 0; j < nkb; ++j) {
-      const int s = j % kNSX;
-      const int b = j % kNB;
-      if (!warp_wait(mma_done(s), (j / kNSX) & 1, wc)) break;
-      tc_fence_after();
-      uint32_t d1[16], d2[16], d3[16];
-      const uint32_t dcol = tmem + lane_base + kDCol0 + b * kBN;
-      tmem_ld16(dcol, d1);
-      tmem_ld16(dcol + 16, d2);
-      tmem_ld16(dcol + 32, d3);
-      // the stage's sums/factors row (the TMA copy that wrote it completed full_g)
-      if (!warp_wait(full_g(s / kPair), (j / kNSX) & 1, wc)) break;
-      float as[kMT], fs[kMT];
-      const float4* a4 = reinterpret_cast<const float4*>(bring + s * kBStage + kBN * 128);
-#pragma unroll
-      for (int v4 = 0; v4 < kMT / 4; ++v4) {
-        const float4 t = a4[v4];
-        const float4 u = a4[kMT / 4 + v4];
-        as[4 * v4] = t.x;
-        as[4 * v4 + 1] = t.y;
-        as[4 * v4 + 2] = t.z;
-        as[4 * v4 + 3] = t.w;
-        fs[4 * v4] = u.x;
-        fs[4 * v4 + 1] = u.y;
-        fs[4 * v4 + 2] = u.z;
-        fs[4 * v4 + 3] = u.w;
-      }
-      tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pdone(s));
-      float val[kMT];
-#pragma unroll
-      for (int m = 0; m < kMT; ++m)
-        val[m] = fmaf(__uint_as_float(d3[m]), 1.0f / 256.0f,
-                      fmaf(__uint_as_float(d2[m]), 1.0f / 16.0f, __uint_as_float(d1[m])));
-      const int o = chunk_of(j);
-      const int slot = o % kChunkSlots;
-      if (!warp_wait(full_c(slot), (o / kChunkSlots) & 1, wc)) break;
-      const uint8_t* chunk = chunk_smem + slot * (kSChunk + kDChunk);
-      const int gr = chunk_row(j);
-      const float sc = __half2float(reinterpret_cast<const __half*>(chunk)[gr * kTileN + row]);
-      const float dl = has_delta ? reinterpret_cast<const float*>(chunk + kSChunk)[gr * kTileN + row] : 0.0f;
-      const float zero = fmaf(-8.0f, sc, dl);  // delta - 8 s: the zero point
-#pragma unroll
-      for (int m = 0; m < kMT; ++m) acc[m] = fmaf(zero, as[m], fmaf(sc * fs[m], val[m], acc[m]));
-      __syncwarp();
-      if (lane == 0 && (j + 1 == nkb || chunk_of(j + 1) != o)) mbar_arrive(empty_c(slot));
-    }
+    // Only the first 3 M columns of D are live: load and combine 16, 32 or 48.
+    const int groups = (3 * p.M + 15) / 16;
+    if (groups == 1)
+      promote_loop<1>(p, tmem + lane_base, gbase + (sb - base), chunk_smem, sbar, nkb, kb0, row, abort_flag, status, acc);
+    else if (groups == 2)
+      promote_loop<2>(p, tmem + lane_base, gbase + (sb - base), chunk_smem, sbar, nkb, kb0, row, abort_flag, status, acc);
+    else
+      promote_loop<3>(p, tmem + lane_base, gbase + (sb - base), chunk_smem, sbar, nkb, kb0, row, abort_flag, status, acc);
     tc_fence_before();
   }
 
