@@ -50,12 +50,13 @@ def test_library_links_no_driver_library():
 
 def test_version_and_workspace_queries(lib):
     assert b"sm_103a" in lib.wq_version()
-    # decode (M <= 16), every variant: the e4m3 activation components plus one row of
-    # per-block sums and factors, padded to [56][K] bytes (split-K reduces in shared memory)
+    # decode (M <= 16): W4A16 reads the activations directly and reduces split-K in
+    # shared memory (no scratch); W4A8 needs the e4m3 activation components plus one
+    # row of per-block sums and factors, padded to [56][K] bytes
     a = lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 128)
     b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 1, 4096, 4096, 128)
     c = lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
-    assert a == b == c == 56 * 4096
+    assert a == b == 0 and c == 56 * 4096
     # large M: the asymmetric variant needs the correction columns, [M + N][kaug] bf16
     a = lib.wq_workspace_size(wq.VARIANT_W4A16, 512, 4096, 4096, 128)
     b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 512, 4096, 4096, 128)

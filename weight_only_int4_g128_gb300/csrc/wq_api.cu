@@ -132,14 +132,15 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, size_t esize, const void* p
 
 // Activations [rows][K] as a 3-D tensor {64 k, rows, K/64 halves-of-k-blocks} so
 // that one box {64, box_rows, 2} fetches a whole 128-k block as two 128-byte
-// swizzled atoms placed one after the other in shared memory.
+// swizzled atoms placed one after the other in shared memory (box_atoms = 4:
+// two consecutive 128-k blocks).
 int make_map_x3d(CUtensorMap* m, CUtensorMapDataType dt, const void* ptr, uint64_t rows, uint64_t K,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, uint32_t box_atoms = 2) {
   EncodeFn enc = get_encode();
   if (!enc) return fail(WQ_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   cuuint64_t dims[3] = {64, rows, K / 64};
   cuuint64_t strides[2] = {K * 2, 128};
-  cuuint32_t box[3] = {64, box_rows, 2};
+  cuuint32_t box[3] = {64, box_rows, box_atoms};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -208,9 +209,10 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
   p.off_x16 = off;
   if (variant == WQ_VARIANT_W4A8 && !p.gemv) off = align256(off + static_cast<size_t>(M) * K * 2);
-  // decode: e4m3 activation components + per-block sums/factors row, padded: [56][K] bytes
+  // decode W4A8: e4m3 activation components + per-block sums/factors row, padded: [56][K]
+  // bytes (the W4A16 decode kernel reads the activations directly)
   p.off_x8 = off;
-  if (p.gemv) off = align256(off + static_cast<size_t>(wq::decode_b_rows()) * K);
+  if (p.gemv && variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(wq::decode_b_rows()) * K);
   p.bytes = off;
   return p;
 }
@@ -227,8 +229,42 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   const int G = K / gs;
   cudaError_t e;
 
+  if (plan.gemv && variant != WQ_VARIANT_W4A8) {
+    // decode W4A16: one launch, activations read directly
+    CUtensorMap tm_x, tm_s, tm_d;
+    const CUtensorMapDataType xdt =
+        x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    int rc = make_map_x3d(&tm_x, xdt, X, M, K, 16, 4);
+    if (rc) return rc;
+    rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc) return rc;
+    if (delta) {
+      rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+      if (rc) return rc;
+    } else {
+      tm_d = tm_s;  // unused
+    }
+    wq::GemmParams p{};
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.group_size = gs;
+    p.G = G;
+    p.kb_total = K / 128;
+    p.kb_per_split = plan.kb_per_split;
+    p.splits = plan.splits;
+    p.B = Bpacked;
+    p.S = static_cast<const __half*>(S);
+    p.delta = delta;
+    p.Y = Y;
+    p.y_kind = y_kind;
+    p.timeout_ns = timeout_ns();
+    p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+    e = wq::launch_decode16(x_kind, tm_x, tm_s, tm_d, p, st);
+    return after_launch(e, name, st);
+  }
   if (plan.gemv) {
-    // decode: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
+    // decode W4A8: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
     uint8_t* x8 = wsb + plan.off_x8;
     const int pk = (variant == WQ_VARIANT_W4A8) ? wq::kXI8 : x_kind;
     e = wq::launch_decode_prep(X, pk, M, K, x_scale, x8, st);

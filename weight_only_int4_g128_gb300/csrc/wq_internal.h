@@ -56,6 +56,9 @@ cudaError_t launch_decode_prep(const void* X, int x_kind, int M, int K, const fl
 cudaError_t launch_decode(const CUtensorMap& tm_b, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
                           const GemmParams& p, cudaStream_t stream);
 int decode_max_splits();
+cudaError_t launch_decode16(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
+                            const GemmParams& p, cudaStream_t stream);
+int decode16_max_splits();
 int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
