@@ -74,6 +74,29 @@ def flops(s) -> int:
     return 2 * s["M"] * s["N"] * s["K"]
 
 
+def load_traffic(shapes):
+    """DRAM bytes of one launch of the decode kernel from the committed ncu capture
+    (profiles/traffic.json), or None when the kernel's sources changed since the
+    capture or the captured shape is not part of this workload."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f)
+    h = hashlib.sha256()
+    for src in rec["sources"]:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != rec["source_sha256"]:
+        return None
+    sh = rec["shape"]
+    if not any(s["M"] == sh["M"] and s["K"] == sh["K"] and s["N"] == sh["N"] and s["group_size"] == sh["group_size"]
+               and s["mode"] == "w4a16" for _, s in shapes):
+        return None
+    return rec
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -364,14 +387,34 @@ def run_gpu(args, shapes, ws, rank, local):
                            "weight_GBps": round(weight_bytes(s) / (us * 1e-6) / 1e9, 1),
                            "tflops": round(flops(s) / (us * 1e-6) / 1e12, 3)})
 
-    achieved = tot_alg / (tot_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1),
-                "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs, copy)"
-                if peaks_src == "measured" else "fallback 6.8 TB/s",
-                "kernel": "wq::gemv_kernel (M <= 16) / wq::gemm_kernel; time per GEMM call",
-                "per_shape": shape_rows}
+    traffic = load_traffic(shapes)
+    tot_flops = sum(flops(p["s"]) for p in probs)
+    # Which roofline bounds the workload: its bytes at the measured HBM copy rate
+    # against its FLOPs at the measured dense bf16/fp16 rate (fp16 runs at the bf16
+    # rate on this part; W4A8 is computed in fp16 or e4m3, never at an int8 rate).
+    # The per-shape loops run for seconds, so the sustained tensor figure applies.
+    t_hbm = tot_alg / (peaks["hbm_gbs"] * 1e9)
+    t_tc = tot_flops / (peaks["bf16_tflops_sustained"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved = tot_alg / (tot_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(achieved / peaks["hbm_gbs"], 4),
+                    "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs, copy)"
+                    if peaks_src == "measured" else "fallback 6.8 TB/s"}
+    else:
+        achieved = tot_flops / (tot_ms * 1e-3) / 1e12
+        pk = peaks["bf16_tflops_sustained"]
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
+                    "frac": round(achieved / pk, 4),
+                    "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
+                    "peak_source": f"{peaks_src} (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS bf16)"
+                    if peaks_src == "measured" else "fallback 1.7 PFLOP/s sustained"}
+    roofline.update({
+        "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
+        "kernel": "wq::decode16_kernel (W4A16, M <= 16) / wq::gemm_kernel; time per GEMM call",
+        "traffic_launch": ({"shape": traffic["shape"], "algorithmic_bytes": traffic["algorithmic_bytes_per_launch"],
+                            "source": traffic["capture"]} if traffic else None),
+        "per_shape": shape_rows})
 
     # --- end to end through the public API: pinned host X -> device, GEMM, Y -> pinned host
     e2e_steps = max(20, min(200, args.steps // 50))
