@@ -64,10 +64,11 @@ def io_bytes(s) -> int:
 
 def kernel_launches(s) -> int:
     """Kernels one GEMM call enqueues (the decode kernel is a single launch for W4A16;
-    the large-M path adds the group-sum and delta pre-passes, W4A8 an int8->fp16 pass)."""
+    the large-M path adds one correction pre-pass (group sums and delta columns), W4A8
+    an activation pre-pass)."""
     if s["mode"] == "w4a8":
         return 2
-    return 1 if s["M"] <= 16 else 3
+    return 1 if s["M"] <= 16 else 2
 
 
 def flops(s) -> int:

@@ -311,10 +311,8 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   __nv_bfloat16* aug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_aug);
   __nv_bfloat16* daug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_daug);
   if (plan.kaug) {
-    e = wq::launch_aug_prep(X, x_kind, M, K, gs, G, plan.kaug, aug, st);
-    if (e != cudaSuccess) return cuda_fail(e, "group-sum pre-pass");
-    e = wq::launch_delta_aug(delta, G, N, plan.kaug, daug, st);
-    if (e != cudaSuccess) return cuda_fail(e, "delta pre-pass");
+    e = wq::launch_corr_prep(X, x_kind, delta, M, K, N, gs, G, plan.kaug, aug, daug, st);
+    if (e != cudaSuccess) return cuda_fail(e, "correction pre-pass");
   }
 
   CUtensorMap tm_x, tm_aug, tm_s, tm_d;

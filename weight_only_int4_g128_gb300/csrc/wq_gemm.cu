@@ -60,7 +60,7 @@ struct Cfg {
   static constexpr int kChunk = 8;  // groups per scale chunk (the index math below uses >> 3)
   static constexpr int kSChunkBytes = kChunk * kTileN * 2;            // 2 KB of fp16 scale rows
   static constexpr int kChunkSlots = 2;
-  static constexpr int kNumBars = 3 * kNSX + kNSA + 1 + 2 * kChunkSlots;
+  static constexpr int kNumBars = 4 * kNSX + kNSA + 1 + 2 * kChunkSlots;
   static constexpr int kSmemBytes = 1024 /*align slack*/ + kNSX * (kXStageBytes + kWStageBytes) +
                                     kChunkSlots * kSChunkBytes + kNumBars * 8 + 16;
   static_assert(BT % 16 == 0 && BT >= 16 && BT <= 256, "MMA N for M=128 is 16..256, step 16");
@@ -97,19 +97,25 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
   const uint32_t sw = sx + C::kNSX * C::kXStageBytes;
   const uint32_t sch = sw + C::kNSX * C::kWStageBytes;  // scale chunk slots
   const uint32_t sbar = sch + C::kChunkSlots * C::kSChunkBytes;
-  // full_x: TMA bytes of stage s landed; empty_x: the dequant warps have read
-  // it; mma_done: the k-block's MMAs completed (one tcgen05.commit per
-  // k-block; frees the activation tile and the TMEM A-stage); full_a: the
-  // A-stage holds dequantized weights.
+  // The packed weight tile of a stage travels on its own barrier and is copied
+  // one stage ahead of the stage's activation tile, so the dequant of a stage
+  // overlaps the copy of its (much larger) activation tile.
+  // full_x: activation tile of stage s landed; full_w: weight tile landed (a
+  // correction stage has none: the producer only completes the phase);
+  // empty_w: the dequant warps have read the weight tile; mma_done: the
+  // k-block's MMAs completed (one tcgen05.commit per k-block; frees the
+  // activation tile and the TMEM A-stage); full_a: the A-stage holds
+  // dequantized weights.
   auto full_x = [&](int s) { return sbar + 8u * s; };
-  auto empty_x = [&](int s) { return sbar + 8u * (C::kNSX + s); };
+  auto empty_w = [&](int s) { return sbar + 8u * (C::kNSX + s); };
   auto mma_done = [&](int s) { return sbar + 8u * (2 * C::kNSX + s); };
-  auto full_a = [&](int a) { return sbar + 8u * (3 * C::kNSX + a); };
-  const uint32_t done_bar = sbar + 8u * (3 * C::kNSX + C::kNSA);
+  auto full_w = [&](int s) { return sbar + 8u * (3 * C::kNSX + s); };
+  auto full_a = [&](int a) { return sbar + 8u * (4 * C::kNSX + a); };
+  const uint32_t done_bar = sbar + 8u * (4 * C::kNSX + C::kNSA);
   // full_c / empty_c: scale rows of 8 consecutive groups (one chunk) landed /
   // released by the dequant warps.
-  auto full_c = [&](int c) { return sbar + 8u * (3 * C::kNSX + C::kNSA + 1 + c); };
-  auto empty_c = [&](int c) { return sbar + 8u * (3 * C::kNSX + C::kNSA + 1 + C::kChunkSlots + c); };
+  auto full_c = [&](int c) { return sbar + 8u * (4 * C::kNSX + C::kNSA + 1 + c); };
+  auto empty_c = [&](int c) { return sbar + 8u * (4 * C::kNSX + C::kNSA + 1 + C::kChunkSlots + c); };
   const uint32_t misc = sbar + 8u * C::kNumBars;
   uint8_t* const gmisc = gbase + (misc - base);
   volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gmisc);
@@ -135,7 +141,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kNSX; ++s) {
       mbar_init(full_x(s), 1);
-      mbar_init(empty_x(s), kDqWarps);  // one arrive per dequant warp
+      mbar_init(full_w(s), 1);
+      mbar_init(empty_w(s), kDqWarps);  // one arrive per dequant warp
       mbar_init(mma_done(s), 1);
     }
     for (int a = 0; a < C::kNSA; ++a) {
@@ -163,41 +170,60 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Programmatic dependent launch: the next grid in the stream may be scheduled
+  // now (a grid of this library waits for this one to complete before it touches
+  // memory this one uses); nothing here reads or writes memory a preceding grid
+  // may write (X, the correction columns of the pre-pass, Y) before the wait.
+  griddep_launch_dependents();
+  griddep_wait();
 
-  int issued = 0;         // TMA stages the producer lane has issued
+  int issued = 0;         // stages whose activation tile the producer lane has issued
+  int w_issued = 0;       // stages whose weight side the producer lane has issued
   int chunks_loaded = 0;  // producer lane: scale chunks [0, chunks_loaded) issued
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, &g_status};
-      for (int it = 0; it < n_stages; ++it) {
-        const int s = it % C::kNSX;
-        const uint32_t ph = (it / C::kNSX) & 1;
-        if (!mbar_wait(empty_x(s), ph ^ 1, wc)) break;
-        if (!mbar_wait(mma_done(s), ph ^ 1, wc)) break;
-        const uint32_t xdst = sx + s * C::kXStageBytes;
-        // activation tile [BT x 128 k]: one 3-D box {64 k, BT rows, 2 halves}
-        if (it < n_aug) {
-          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes);
-          tma_load_3d(xdst, &tm_aug, full_x(s), 0, m0, 2 * it);
-        } else {
-          const int kb = kb0 + (it - n_aug);
-          const int o = chunk_of(kb);
-          if (o >= chunks_loaded) {
-            const int slot = o % C::kChunkSlots;
-            if (!mbar_wait(empty_c(slot), ((o / C::kChunkSlots) & 1) ^ 1, wc)) break;
-            mbar_arrive_expect_tx(full_c(slot), C::kSChunkBytes);
-            tma_load_2d(sch + slot * C::kSChunkBytes, &tm_s, full_c(slot), n0,
-                        ((g_first >> 3) + o) * C::kChunk);
-            chunks_loaded = o + 1;
-          }
-          mbar_arrive_expect_tx(full_x(s), C::kXStageBytes + C::kWStageBytes);
-          tma_load_3d(xdst, &tm_x, full_x(s), 0, m0, 2 * kb);
-          // packed weight tile: one contiguous 8 KB block of the blocked layout
-          bulk_load(sw + s * C::kWStageBytes,
-                    p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb) * 2048, C::kWStageBytes,
-                    full_x(s));
+      // Weight side of stage it2: the packed tile (+ a scale chunk when its k-block
+      // starts one); a correction stage has no weight tile and only completes the
+      // phase.  Every wait comes before the first copy of the stage.
+      auto issue_w = [&](int it2) -> bool {
+        const int s2 = it2 % C::kNSX;
+        if (!mbar_wait(empty_w(s2), ((it2 / C::kNSX) & 1) ^ 1, wc)) return false;
+        if (it2 < n_aug) {
+          mbar_arrive(full_w(s2));
+          return true;
         }
+        const int kb = kb0 + (it2 - n_aug);
+        const int o = chunk_of(kb);
+        if (o >= chunks_loaded) {
+          const int slot = o % C::kChunkSlots;
+          if (!mbar_wait(empty_c(slot), ((o / C::kChunkSlots) & 1) ^ 1, wc)) return false;
+          mbar_arrive_expect_tx(full_c(slot), C::kSChunkBytes);
+          tma_load_2d(sch + slot * C::kSChunkBytes, &tm_s, full_c(slot), n0, ((g_first >> 3) + o) * C::kChunk);
+          chunks_loaded = o + 1;
+        }
+        mbar_arrive_expect_tx(full_w(s2), C::kWStageBytes);
+        // packed weight tile: one contiguous 8 KB block of the blocked layout
+        bulk_load(sw + s2 * C::kWStageBytes, p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb) * 2048,
+                  C::kWStageBytes, full_w(s2));
+        return true;
+      };
+      bool ok = n_stages == 0 || issue_w(0);
+      if (ok) w_issued = n_stages > 0 ? 1 : 0;
+      for (int it = 0; ok && it < n_stages; ++it) {
+        // weight side one stage ahead
+        if (it + 1 < n_stages) {
+          if (!issue_w(it + 1)) break;
+          w_issued = it + 2;
+        }
+        // activation tile [BT x 128 k]: one 3-D box {64 k, BT rows, 2 halves}
+        const int s = it % C::kNSX;
+        if (!mbar_wait(mma_done(s), ((it / C::kNSX) & 1) ^ 1, wc)) break;
+        const uint32_t xdst = sx + s * C::kXStageBytes;
+        mbar_arrive_expect_tx(full_x(s), C::kXStageBytes);
+        if (it < n_aug) tma_load_3d(xdst, &tm_aug, full_x(s), 0, m0, 2 * it);
+        else tma_load_3d(xdst, &tm_x, full_x(s), 0, m0, 2 * (kb0 + (it - n_aug)));
         issued = it + 1;
       }
     }
@@ -212,8 +238,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
       for (int it = 0; it < n_stages; ++it) {
         const int s = it % C::kNSX;
         const int a = it % C::kNSA;
-        // full_a implies the stage's TMA bytes landed: the dequant warps waited on full_x
         if (!mbar_wait(full_a(a), (it / C::kNSA) & 1, wc)) break;
+        if (!mbar_wait(full_x(s), (it / C::kNSX) & 1, wc)) break;  // activation tile landed
         tc_fence_after();
         const uint64_t ds = desc0 + static_cast<uint64_t>((s * C::kXStageBytes) >> 4);
         const uint32_t id = (it < n_aug) ? id_aug : id_x;
@@ -258,10 +284,10 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
           v[4 * i + 2] = t.z;
           v[4 * i + 3] = t.w;
         }
-        if (!warp_wait(full_x(s), ph, wc)) break;
-        if (lane == 0) mbar_arrive(empty_x(s));
+        if (!warp_wait(full_w(s), ph, wc)) break;  // the producer's (empty) weight side of the stage
+        if (lane == 0) mbar_arrive(empty_w(s));
       } else {
-        if (!warp_wait(full_x(s), ph, wc)) break;
+        if (!warp_wait(full_w(s), ph, wc)) break;
         const int kb = kb0 + (it - n_aug);
         const int o = chunk_of(kb);
         const int slot = o % C::kChunkSlots;
@@ -273,7 +299,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
         const uint4 w1 = *reinterpret_cast<const uint4*>(wrow + 16 * ((2 * h + 1) ^ ((row >> 1) & 3)));
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(empty_x(s));
+          mbar_arrive(empty_w(s));
           if (kb + 1 == kb1 || chunk_of(kb + 1) != o) mbar_arrive(empty_c(slot));  // chunk done
         }
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -343,6 +369,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, &g_status};
     for (int it = max(0, issued - C::kNSX); it < issued; ++it)
       mbar_wait(full_x(it % C::kNSX), (it / C::kNSX) & 1, drain);
+    for (int it = max(0, w_issued - C::kNSX); it < w_issued; ++it)
+      mbar_wait(full_w(it % C::kNSX), (it / C::kNSX) & 1, drain);
     for (int o = max(0, chunks_loaded - C::kChunkSlots); o < chunks_loaded; ++o)
       mbar_wait(full_c(o % C::kChunkSlots), (o / C::kChunkSlots) & 1, drain);
   }
@@ -454,13 +482,15 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;  // the K segments of a tile form a cluster
   attr[0].val.clusterDim.x = 1;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = p.splits;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_aug, tm_s, p);
 }
 

@@ -66,10 +66,8 @@ cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUten
 size_t gemm_smem_bytes(int bt);
 
 // Pre-pass kernels (wq_kernels.cu).
-cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
-                            int kaug, __nv_bfloat16* aug, cudaStream_t stream);
-cudaError_t launch_delta_aug(const float* delta, int G, int N, int kaug, __nv_bfloat16* delta_aug,
-                             cudaStream_t stream);
+cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int M, int K, int N, int group_size,
+                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, cudaStream_t stream);
 cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t stream);
 cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
                         uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,

@@ -181,69 +181,83 @@ __device__ __forceinline__ void write_aug(__nv_bfloat16* arow, int G, int g, flo
   arow[2 * G + g] = h;
 }
 
+// Correction pre-pass of the large-M GEMM, one launch: blocks [0, n_sum) form the
+// activation-side columns aug[m][0..kaug) = [a_hi | a_lo | a_hi | 0...] from the
+// group sums a_sum[m][g] (fp32, split into bf16 hi/lo); blocks [n_sum, ...) form
+// the weight-side columns delta_aug[n][0..kaug) = [d_hi | d_hi | d_lo | 0...]
+// (a tiled transpose: a 32 (g) x 32 (n) tile of delta is read with coalesced
+// rows, split in shared memory, and written as 32 consecutive j of each of the
+// 32 rows n, three times).  256 threads per block.  Programmatic dependent
+// launch: the grid lets the GEMM that follows be scheduled at once (it waits
+// for this grid's completion), and touches memory only after the preceding
+// grid completed (X may be written by it; the workspace may still be read by it).
+struct CorrPrep {
+  const void* X;
+  const float* delta;
+  __nv_bfloat16* aug;
+  __nv_bfloat16* delta_aug;
+  int M, K, N, group_size, G, kaug;
+  int n_sum_blocks;  // blocks of the group-sum part
+  int g_tiles;       // 32-wide group tiles of the delta part
+};
+
 template <int XK>
-__global__ void aug_prep_kernel(const void* __restrict__ X, int M, int K, int group_size, int G,
-                                int kaug, __nv_bfloat16* __restrict__ aug) {
-  const uint16_t* Xh = reinterpret_cast<const uint16_t*>(X);
-  if (group_size <= 1024) {
-    const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-    if (idx >= static_cast<long long>(M) * G) return;
+__device__ __forceinline__ void corr_group_sums(const CorrPrep& c, int bid) {
+  const uint16_t* Xh = reinterpret_cast<const uint16_t*>(c.X);
+  const int G = c.G;
+  const int pad = c.kaug - 3 * G;
+  if (c.group_size <= 1024) {
+    // one thread per (m, g); the thread of g == 0 also zeroes the row's padding
+    const long long idx = bid * 256LL + threadIdx.x;
+    if (idx >= static_cast<long long>(c.M) * G) return;
     const int m = static_cast<int>(idx / G);
     const int g = static_cast<int>(idx - static_cast<long long>(m) * G);
-    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * K +
-                                                     static_cast<size_t>(g) * group_size);
+    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * c.K +
+                                                     static_cast<size_t>(g) * c.group_size);
     float acc = 0.0f;
-    const int nv = group_size / 8;
+    const int nv = c.group_size / 8;
 #pragma unroll 16
     for (int i = 0; i < nv; ++i) acc += sum8<XK>(__ldg(gp + i));
-    write_aug(aug + static_cast<size_t>(m) * kaug, G, g, acc);
+    __nv_bfloat16* arow = c.aug + static_cast<size_t>(m) * c.kaug;
+    write_aug(arow, G, g, acc);
+    if (g == 0)
+      for (int j = 0; j < pad; ++j) arow[3 * G + j] = __float2bfloat16_rn(0.0f);
   } else {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    // one warp per (m, g) for long groups (per-channel)
+    const int warp = (bid * 256 + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (warp >= M * G) return;
+    if (warp >= c.M * G) return;
     const int m = warp / G;
     const int g = warp - m * G;
-    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * K +
-                                                     static_cast<size_t>(g) * group_size);
+    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * c.K +
+                                                     static_cast<size_t>(g) * c.group_size);
     float acc = 0.0f;
-    const int nv = group_size / 8;
+    const int nv = c.group_size / 8;
 #pragma unroll 8
     for (int i = lane; i < nv; i += 32) acc += sum8<XK>(__ldg(gp + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) write_aug(aug + static_cast<size_t>(m) * kaug, G, g, acc);
+    __nv_bfloat16* arow = c.aug + static_cast<size_t>(m) * c.kaug;
+    if (lane == 0) write_aug(arow, G, g, acc);
+    if (g == 0)
+      for (int j = lane; j < pad; j += 32) arow[3 * G + j] = __float2bfloat16_rn(0.0f);
   }
 }
 
-// Zero the padding columns [3G, kaug) of every aug row.
-__global__ void aug_pad_kernel(int M, int G, int kaug, __nv_bfloat16* __restrict__ aug) {
-  const int pad = kaug - 3 * G;
-  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
-  if (idx >= static_cast<long long>(M) * pad) return;
-  const int m = static_cast<int>(idx / pad);
-  const int j = 3 * G + static_cast<int>(idx - static_cast<long long>(m) * pad);
-  aug[static_cast<size_t>(m) * kaug + j] = __float2bfloat16_rn(0.0f);
-}
-
-// Weight-side correction columns: delta_aug[n][j] = [d_hi | d_hi | d_lo | 0...]
-// (j over 3G, padded to kaug) with d_hi = bf16_RN(delta), d_lo = bf16_RN(delta -
-// d_hi).  A tiled transpose: a 32 (g) x 32 (n) tile of delta is read with
-// coalesced rows, split in shared memory, and written as 32 consecutive j of
-// each of the 32 rows n, three times (one per term).
-__global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, int kaug,
-                                 __nv_bfloat16* __restrict__ out) {
+__device__ __forceinline__ void corr_delta_columns(const CorrPrep& c, int tile) {
   __shared__ uint16_t hi_t[32][33];
   __shared__ uint16_t lo_t[32][33];
-  const int g0 = blockIdx.x * 32;
-  const int n0 = blockIdx.y * 32;
-  const int tx = threadIdx.x;  // 0..31
-  const int ty = threadIdx.y;  // 0..7
+  const int G = c.G, N = c.N, kaug = c.kaug;
+  const int g0 = (tile % c.g_tiles) * 32;
+  const int n0 = (tile / c.g_tiles) * 32;
+  const int tx = threadIdx.x & 31;
+  const int ty = threadIdx.x >> 5;  // 0..7
   for (int r = ty; r < 32; r += 8) {
     const int g = g0 + r;
     uint16_t h = 0, l = 0;
     if (g < G) {
       __nv_bfloat16 bh, bl;
-      split_bf16(delta[static_cast<size_t>(g) * N + n0 + tx], bh, bl);
+      split_bf16(c.delta[static_cast<size_t>(g) * N + n0 + tx], bh, bl);
       h = __bfloat16_as_ushort(bh);
       l = __bfloat16_as_ushort(bl);
     }
@@ -251,7 +265,7 @@ __global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, 
     lo_t[r][tx] = l;
   }
   __syncthreads();
-  uint16_t* o = reinterpret_cast<uint16_t*>(out);
+  uint16_t* o = reinterpret_cast<uint16_t*>(c.delta_aug);
   for (int r = ty; r < 32; r += 8) {
     const int n = n0 + r;
     const int g = g0 + tx;
@@ -263,7 +277,7 @@ __global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, 
     }
   }
   // padding columns, written by the blocks of the first g tile
-  if (blockIdx.x == 0) {
+  if (g0 == 0) {
     for (int r = ty; r < 32; r += 8) {
       uint16_t* row = o + static_cast<size_t>(n0 + r) * kaug;
       for (int j = 3 * G + tx; j < kaug; j += 32) row[j] = 0;
@@ -271,8 +285,19 @@ __global__ void delta_aug_kernel(const float* __restrict__ delta, int G, int N, 
   }
 }
 
+template <int XK>
+__global__ void __launch_bounds__(256) corr_prep_kernel(const CorrPrep c) {
+  griddep_launch_dependents();
+  griddep_wait();
+  if (static_cast<int>(blockIdx.x) < c.n_sum_blocks) corr_group_sums<XK>(c, blockIdx.x);
+  else corr_delta_columns(c, blockIdx.x - c.n_sum_blocks);
+}
+
 __global__ void i8_to_f16_kernel(const int8_t* __restrict__ Xq, __half* __restrict__ X16,
                                  long long count) {
+  // programmatic dependent launch: as the correction pre-pass
+  griddep_launch_dependents();
+  griddep_wait();
   const long long i = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) * 4;
   if (i + 3 < count) {
     const char4 c = *reinterpret_cast<const char4*>(Xq + i);
@@ -321,37 +346,52 @@ cudaError_t launch_quantize_per_token(const __half* x, int8_t* Xq, float* x_scal
   return cudaGetLastError();
 }
 
-cudaError_t launch_aug_prep(const void* X, int x_kind, int M, int K, int group_size, int G,
-                            int kaug, __nv_bfloat16* aug, cudaStream_t st) {
-  const long long work = (group_size <= 1024) ? static_cast<long long>(M) * G
-                                              : static_cast<long long>(M) * G * 32;
-  const unsigned blocks = static_cast<unsigned>((work + 127) / 128);
-  if (x_kind == kXBF16) {
-    aug_prep_kernel<kXBF16><<<blocks, 128, 0, st>>>(X, M, K, group_size, G, kaug, aug);
-  } else {
-    aug_prep_kernel<kXF16><<<blocks, 128, 0, st>>>(X, M, K, group_size, G, kaug, aug);
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const long long pad = static_cast<long long>(M) * (kaug - 3 * G);
-  if (pad > 0) {
-    aug_pad_kernel<<<static_cast<unsigned>((pad + 255) / 256), 256, 0, st>>>(M, G, kaug, aug);
-    e = cudaGetLastError();
-  }
-  return e;
+static cudaLaunchAttribute pdl_attr_k() {
+  cudaLaunchAttribute a = {};
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
 }
 
-cudaError_t launch_delta_aug(const float* delta, int G, int N, int kaug, __nv_bfloat16* delta_aug,
-                             cudaStream_t st) {
-  dim3 grid((G + 31) / 32, N / 32);
-  delta_aug_kernel<<<grid, dim3(32, 8), 0, st>>>(delta, G, N, kaug, delta_aug);
-  return cudaGetLastError();
+cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int M, int K, int N, int group_size,
+                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, cudaStream_t st) {
+  CorrPrep c{};
+  c.X = X;
+  c.delta = delta;
+  c.aug = aug;
+  c.delta_aug = delta_aug;
+  c.M = M;
+  c.K = K;
+  c.N = N;
+  c.group_size = group_size;
+  c.G = G;
+  c.kaug = kaug;
+  const long long sum_threads = (group_size <= 1024) ? static_cast<long long>(M) * G
+                                                     : static_cast<long long>(M) * G * 32;
+  c.n_sum_blocks = static_cast<int>((sum_threads + 255) / 256);
+  c.g_tiles = (G + 31) / 32;
+  const long long blocks = c.n_sum_blocks + static_cast<long long>(c.g_tiles) * (N / 32);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attr_k()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return x_kind == kXBF16 ? cudaLaunchKernelEx(&cfg, corr_prep_kernel<kXBF16>, c)
+                          : cudaLaunchKernelEx(&cfg, corr_prep_kernel<kXF16>, c);
 }
 
 cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t st) {
   const long long threads = (count + 3) / 4;
-  i8_to_f16_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, st>>>(Xq, X16, count);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((threads + 255) / 256), 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1] = {pdl_attr_k()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, i8_to_f16_kernel, Xq, X16, count);
 }
 
 
