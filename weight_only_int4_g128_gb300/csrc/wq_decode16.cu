@@ -49,7 +49,7 @@ constexpr int kTmemCols = 256;
 constexpr int kThreads = 352;             // 11 warps
 constexpr int kMaxSplits = 8;             // portable cluster size
 constexpr int kRedBytes = 8704;           // >= splits * ceil(128 / splits) * 16 * 4 for splits <= 8
-constexpr int kNumBars = kNG + 3 * kNSX + kNSA + 2 * kChunkSlots + 2;
+constexpr int kNumBars = 2 * kNG + 3 * kNSX + kNSA + 2 * kChunkSlots + 2;
 constexpr int kSmemBytes = 1024 + kNSX * (kXStage + kWStage) + kChunkSlots * (kSChunk + kDChunk) +
                            kNSX * kMT * 4 + kRedBytes + kNumBars * 8 + 16;
 static_assert(kDCol0 + kNB * kMT <= kTmemCols, "TMEM budget");
@@ -91,7 +91,9 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
   const uint32_t sred = sas + kNSX * kMT * 4;                 // split-K partials (peers copy here)
   const uint32_t sbar = sred + kRedBytes;
   // Barriers.  Per load group g (k-blocks 2 gi, 2 gi + 1; g = gi % kNG, stages 2 g, 2 g + 1):
-  //   full_g    both weight tiles + both activation tiles landed
+  //   full_w    both weight tiles landed (the dequant warps need nothing else, so
+  //             with weight prefetch they may run before the preceding grid ends)
+  //   full_x    both activation tiles landed (block sums, MMAs)
   // Per stage s (k-block it, s = it % kNSX):
   //   mma_done  the k-block's MMAs completed (A-stage it % kNSA free, D buffer it % kNB full)
   //   asum_full the block sums of the stage's activation tile are in shared memory
@@ -99,13 +101,14 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
   //             the D buffer and (with the other stage of its group) the stage are free
   // full_a[a]  A-stage a holds the k-block's weights
   // full_c/empty_c  scale + delta rows of 8 groups landed / released
-  auto full_g = [&](int g) { return sbar + 8u * g; };
-  auto mma_done = [&](int s) { return sbar + 8u * (kNG + s); };
-  auto asum_full = [&](int s) { return sbar + 8u * (kNG + kNSX + s); };
-  auto pdone = [&](int s) { return sbar + 8u * (kNG + 2 * kNSX + s); };
-  auto full_a = [&](int a) { return sbar + 8u * (kNG + 3 * kNSX + a); };
-  auto full_c = [&](int c) { return sbar + 8u * (kNG + 3 * kNSX + kNSA + c); };
-  auto empty_c = [&](int c) { return sbar + 8u * (kNG + 3 * kNSX + kNSA + kChunkSlots + c); };
+  auto full_w = [&](int g) { return sbar + 8u * g; };
+  auto full_x = [&](int g) { return sbar + 8u * (kNG + g); };
+  auto mma_done = [&](int s) { return sbar + 8u * (2 * kNG + s); };
+  auto asum_full = [&](int s) { return sbar + 8u * (2 * kNG + kNSX + s); };
+  auto pdone = [&](int s) { return sbar + 8u * (2 * kNG + 2 * kNSX + s); };
+  auto full_a = [&](int a) { return sbar + 8u * (2 * kNG + 3 * kNSX + a); };
+  auto full_c = [&](int c) { return sbar + 8u * (2 * kNG + 3 * kNSX + kNSA + c); };
+  auto empty_c = [&](int c) { return sbar + 8u * (2 * kNG + 3 * kNSX + kNSA + kChunkSlots + c); };
   const uint32_t done_bar = sbar + 8u * (kNumBars - 2);
   const uint32_t red_full = sbar + 8u * (kNumBars - 1);
   uint8_t* const gmisc = gbase + (sbar + 8u * kNumBars - base);
@@ -128,26 +131,36 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
   auto chunk_of = [&](int it) { return per_channel ? 0 : ((kb0 + it) >> 3) - (g_first >> 3); };
   auto chunk_row = [&](int it) { return per_channel ? 0 : ((kb0 + it) & 7); };
   int chunks_loaded = 0;  // producer lane: chunk ordinals [0, chunks_loaded) are issued
-  auto group_tx = [&](int gi) { return static_cast<uint32_t>(min(kPair, nkb - kPair * gi) * kWStage + kPair * kXStage); };
+  auto w_bytes = [&](int gi) { return static_cast<uint32_t>(min(kPair, nkb - kPair * gi) * kWStage); };
+  // weights, scales and deltas are read once per call: keep them from evicting X and Y in L2
+  const uint64_t pol_stream = l2_evict_first();
+  const uint64_t pol_keep = l2_evict_last();
   auto issue_w = [&](int gi) {
     const int g = gi % kNG;
-    bulk_load(sw + g * kPair * kWStage, p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb0 + kPair * gi) * 2048,
-              static_cast<uint32_t>(min(kPair, nkb - kPair * gi) * kWStage), full_g(g));
+    mbar_arrive_expect_tx(full_w(g), w_bytes(gi));
+    bulk_load_hint(sw + g * kPair * kWStage,
+                   p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb0 + kPair * gi) * 2048, w_bytes(gi),
+                   full_w(g), pol_stream);
+  };
+  // activation tiles of both k-blocks of load group gi: one 3-D box {64 k, 16 rows, 4 atoms}
+  auto issue_x = [&](int gi) {
+    const int g = gi % kNG;
+    mbar_arrive_expect_tx(full_x(g), kPair * kXStage);
+    tma_load_3d_hint(sx + g * kPair * kXStage, &tm_x, full_x(g), 0, 0, 2 * (kb0 + kPair * gi), pol_keep);
   };
   auto issue_chunk = [&](int o) {
     const int slot = o % kChunkSlots;
     const int grow = ((g_first >> 3) + o) * kChunk;
     const uint32_t dst = sch + slot * (kSChunk + kDChunk);
     mbar_arrive_expect_tx(full_c(slot), chunk_tx);
-    tma_load_2d(dst, &tm_s, full_c(slot), n0, grow);
-    if (has_delta) tma_load_2d(dst + kSChunk, &tm_d, full_c(slot), n0, grow);
+    tma_load_2d_hint(dst, &tm_s, full_c(slot), n0, grow, pol_stream);
+    if (has_delta) tma_load_2d_hint(dst + kSChunk, &tm_d, full_c(slot), n0, grow, pol_stream);
   };
   // Weight-side copies of load group gi (producer lane only); every wait comes first.
   auto weight_copies = [&](int gi, const WaitCtx& wc) -> bool {
     const int last = chunk_of(min(nkb, kPair * gi + kPair) - 1);
     for (int o = chunks_loaded; o <= last; ++o)
       if (!mbar_wait(empty_c(o % kChunkSlots), ((o / kChunkSlots) & 1) ^ 1, wc)) return false;
-    mbar_arrive_expect_tx(full_g(gi % kNG), group_tx(gi));
     issue_w(gi);
     for (; chunks_loaded <= last; ++chunks_loaded) issue_chunk(chunks_loaded);
     return true;
@@ -161,7 +174,10 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
     prefetch_tensormap(&tm_x);
     prefetch_tensormap(&tm_s);
     if (has_delta) prefetch_tensormap(&tm_d);
-    for (int g = 0; g < kNG; ++g) mbar_init(full_g(g), 1);
+    for (int g = 0; g < kNG; ++g) {
+      mbar_init(full_w(g), 1);
+      mbar_init(full_x(g), 1);
+    }
     for (int s = 0; s < kNSX; ++s) {
       mbar_init(mma_done(s), 1);
       mbar_init(asum_full(s), 1);
@@ -182,10 +198,7 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
     // Weight-side copies of the first load groups go out before anything else
     // (fresh stages and chunk slots: nothing to wait for), one group per lane.
     __syncwarp();
-    if (lane < pre) {
-      mbar_arrive_expect_tx(full_g(lane), group_tx(lane));
-      issue_w(lane);
-    }
+    if (lane < pre) issue_w(lane);
     if (lane == 0 && pre > 0) {
       const int last = chunk_of(min(nkb, kPair * pre) - 1);  // at most kChunkSlots chunks
       for (; chunks_loaded <= last; ++chunks_loaded) issue_chunk(chunks_loaded);
@@ -203,13 +216,15 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
 
   // Programmatic dependent launch: the next grid in the stream may be scheduled
   // now (it waits for this one to complete before it touches memory this one
-  // uses); nothing before griddep_wait() touches memory the preceding grid may
-  // write (X, Y).  Only the weight-side copies of the first stages were issued
-  // earlier, and only when the caller enabled it.
+  // uses).  Only two places touch global memory the preceding grid may write:
+  // the producer lane's copies (X always; the weight side too unless the caller
+  // enabled weight prefetch) and the stores of Y.  Both come after
+  // griddep_wait(); until then the dequant warps may already turn prefetched
+  // weight tiles into TMEM A-stages (shared memory and TMEM only).
   griddep_launch_dependents();
-  griddep_wait();
 
-  int issued = 0;  // load groups whose activation box the producer lane has issued
+  int w_issued = pre;  // load groups whose weight tiles have been issued (producer lane)
+  int x_issued = 0;    // load groups whose activation box has been issued (producer lane)
   const int q = warp & 3;         // TMEM lane quarter this warp may access
   const int row = q * 32 + lane;  // weight row of the tile = TMEM lane
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -221,6 +236,7 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, status};
+      griddep_wait();
       for (int gi = 0; gi < ngi; ++gi) {
         const int g = gi % kNG;
         if (gi >= pre) {
@@ -228,10 +244,10 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
           bool ok = true;
           for (int j = 0; j < kPair && ok; ++j) ok = mbar_wait(pdone(kPair * g + j), prev, wc);
           if (!ok || !weight_copies(gi, wc)) break;
+          w_issued = gi + 1;
         }
-        // activation tiles of both k-blocks: one 3-D box {64 k, 16 rows, 4 atoms}
-        tma_load_3d(sx + g * kPair * kXStage, &tm_x, full_g(g), 0, 0, 2 * (kb0 + kPair * gi));
-        issued = gi + 1;
+        issue_x(gi);
+        x_issued = gi + 1;
       }
     }
   } else if (warp == 1) {
@@ -244,9 +260,10 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
         const int s = it % kNSX;
         const int a = it % kNSA;
         const int b = it % kNB;
-        // full_a implies the stage's bytes landed; D buffer b was last read by the
-        // promotion of k-block it - kNB
+        // weights in A-stage a, activation tiles landed; D buffer b was last read
+        // by the promotion of k-block it - kNB
         if (!mbar_wait(full_a(a), (it / kNSA) & 1, wc)) break;
+        if (!mbar_wait(full_x(s / kPair), (it / kNSX) & 1, wc)) break;
         if (it >= kNB) {
           const int pk = it - kNB;
           if (!mbar_wait(pdone(pk % kNSX), (pk / kNSX) & 1, wc)) break;
@@ -271,7 +288,7 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
     const int h = lane & 1;   // 64-k atom of the block
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kNSX;
-      if (!warp_wait16(full_g(s / kPair), (it / kNSX) & 1, wc)) break;
+      if (!warp_wait16(full_x(s / kPair), (it / kNSX) & 1, wc)) break;
       if (has_delta) {
         const uint8_t* rowp = xring + s * kXStage + h * kXAtom + r * 128;
         float sum = 0.0f;
@@ -292,7 +309,7 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
     const uint8_t* wring = gbase + (sw - base);
     auto load_words = [&](int it, uint4 (&wv)[4]) -> bool {
       const int s = it % kNSX;
-      if (!warp_wait16(full_g(s / kPair), (it / kNSX) & 1, wc)) return false;
+      if (!warp_wait16(full_w(s / kPair), (it / kNSX) & 1, wc)) return false;
       const uint8_t* wrow = wring + s * kWStage + row * 64;
 #pragma unroll
       for (int c = 0; c < 4; ++c) wv[c] = *reinterpret_cast<const uint4*>(wrow + 16 * (c ^ ((row >> 1) & 3)));
@@ -377,17 +394,15 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
 
   // ---------------------------------------------------------------- split-K reduction + store
   __syncthreads();  // every role is past its loop
+  griddep_wait();   // Y may be read or written by the preceding grid (returns at once by now)
   const bool aborted = *abort_flag != 0;
   if (aborted && warp == 0 && lane == 0) {
     // Let every copy the producer issued land before the shared memory is reused
-    // or the CTA exits.  Groups whose weight tiles were prefetched but whose
-    // activation box was not issued get it now, so that their barrier completes.
-    for (int gi = issued; gi < pre; ++gi)
-      tma_load_3d(sx + (gi % kNG) * kPair * kXStage, &tm_x, full_g(gi % kNG), 0, 0, 2 * (kb0 + kPair * gi));
-    issued = max(issued, pre);
+    // or the CTA exits.
     volatile int never = 0;
     const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, status};
-    for (int gi = max(0, issued - kNG); gi < issued; ++gi) mbar_wait(full_g(gi % kNG), (gi / kNG) & 1, drain);
+    for (int gi = max(0, w_issued - kNG); gi < w_issued; ++gi) mbar_wait(full_w(gi % kNG), (gi / kNG) & 1, drain);
+    for (int gi = max(0, x_issued - kNG); gi < x_issued; ++gi) mbar_wait(full_x(gi % kNG), (gi / kNG) & 1, drain);
     for (int o = max(0, chunks_loaded - kChunkSlots); o < chunks_loaded; ++o)
       mbar_wait(full_c(o % kChunkSlots), (o / kChunkSlots) & 1, drain);
   }
