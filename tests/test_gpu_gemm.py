@@ -71,6 +71,13 @@ SMALL = [
     (9, 640, 256, 128, "bf16"),
     (200, 1280, 256, 128, "bf16"),
     (64, 2048, 256, -1, "bf16"),
+    # decode kernel: more k-blocks per CTA than ring stages, bf16, one group per
+    # column, 8 tokens
+    (2, 5120, 128, 128, "f16"),
+    (7, 8192, 256, 128, "bf16"),
+    (6, 1024, 256, -1, "f16"),
+    (8, 2048, 384, 128, "f16"),
+    (4, 640, 256, -1, "bf16"),
 ]
 
 
@@ -119,15 +126,18 @@ def test_one_hot_rows_give_dequantized_weights_bit_exact(wq, adt, K):
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("M", [4, 8, 16])
 @pytest.mark.parametrize("adt", ["f16", "bf16"])
 @pytest.mark.parametrize("gs", [128, -1])
-def test_one_hot_decode_path_bit_exact(wq, adt, gs):
-    """M = 16 one-hot rows (the decode kernel): Y[m, :] = RN((q - 8) * scale) of row k_m."""
+def test_one_hot_decode_path_bit_exact(wq, adt, gs, M):
+    """M one-hot rows (the decode kernel): Y[m, :] = RN((q - 8) * scale) of row k_m."""
     K, N = 2048, 384
-    d = synth.make_inputs(550, 16, K, N, group_size=gs, a_dtype=adt)
+    d = synth.make_inputs(550, M, K, N, group_size=gs, a_dtype=adt)
     ks = np.array([0, 1, 7, 8, 127, 128, 129, 511, 640, 1000, 1023, 1024, 1500, 2000, 2046, 2047])
-    eye = np.zeros((16, K), np.float32)
-    eye[np.arange(16), ks] = 1.0
+    if M < 16:
+        ks = ks[np.linspace(0, 15, M).astype(int)]
+    eye = np.zeros((M, K), np.float32)
+    eye[np.arange(M), ks] = 1.0
     if adt == "bf16":
         d["A"] = (eye.view(np.uint32) >> 16).astype(np.uint16)
         out, fn = torch.bfloat16, oracle.dequant_sym_bf16
@@ -140,7 +150,7 @@ def test_one_hot_decode_path_bit_exact(wq, adt, gs):
     assert np.array_equal(got, want)
 
 
-@pytest.mark.parametrize("M,K", [(8, 512), (70, 1024), (257, 256), (16, 4096)])
+@pytest.mark.parametrize("M,K", [(8, 512), (3, 4096), (70, 1024), (257, 256), (16, 4096)])
 def test_integer_weights_exact(wq, M, K):
     """scale = 1, zero = -8 (so delta = 0): C = X @ (q - 8) is an exact integer matmul."""
     N = 256
