@@ -99,18 +99,33 @@ def _check(rc: int, where: str):
         raise WQError(rc, where, load_library().wq_last_error().decode())
 
 
+def _raw_stream(device_index: int) -> int:
+    """Handle of the current CUDA stream of a device, as an integer.  torch's own
+    accessor for it is used when present (a cheap call), else the public API."""
+    torch = _torch()
+    get = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if get is not None:
+        return get(device_index)
+    return torch.cuda.current_stream(device_index).cuda_stream
+
+
 def _stream(t=None):
     torch = _torch()
-    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(_raw_stream(t.device.index if t is not None else torch.cuda.current_device()))
 
 
 def _ptr(t):
     return ctypes.c_void_p(t.data_ptr()) if t is not None else None
 
 
+_DTYPE_CODES = {}
+
+
 def _dtype_code(dt) -> int:
-    torch = _torch()
-    return {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32}[dt]
+    if not _DTYPE_CODES:
+        torch = _torch()
+        _DTYPE_CODES.update({torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16, torch.float32: DTYPE_F32})
+    return _DTYPE_CODES[dt]
 
 
 def _gs(K: int, group_size: int) -> int:
@@ -206,13 +221,35 @@ class Workspace:
 _ws = {}
 
 
-def _workspace(device, nbytes):
-    torch = _torch()
-    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+def _stream_workspace(device, stream: int) -> Workspace:
+    key = (device.index, stream)
     ws = _ws.get(key)
     if ws is None:
         ws = _ws[key] = Workspace(device)
-    return ws.get(nbytes)
+    return ws
+
+
+def _workspace(device, nbytes):
+    return _stream_workspace(device, _raw_stream(device.index)).get(nbytes)
+
+
+def _call_gemm(fn, where, args_head, args_tail, workspace, variant, M, N, K, group_size, device, stream):
+    """Run a GEMM entry point.  Without a caller workspace the stream's cached
+    scratch is passed as it is; only if the library reports it too small is its
+    size queried, the scratch grown and the call repeated (the library checks the
+    workspace before it launches anything)."""
+    lib = _lib or load_library()
+    if workspace is not None:
+        ws = workspace
+    else:
+        ws = _stream_workspace(device, stream).buf
+    rc = fn(*args_head, ws.data_ptr() if ws is not None else None, ws.numel() if ws is not None else 0,
+            stream, *args_tail)
+    if rc == 3 and workspace is None:  # WQ_ERR_WORKSPACE: grow the stream's scratch and retry
+        ws = _stream_workspace(device, stream).get(workspace_size(variant, M, N, K, group_size))
+        rc = fn(*args_head, ws.data_ptr(), ws.numel(), stream, *args_tail)
+    if rc != 0:
+        raise WQError(rc, where, lib.wq_last_error().decode())
 
 
 # -- GEMMs -----------------------------------------------------------------------------
@@ -221,18 +258,17 @@ def gemm_w4a16(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=
                workspace=None):
     """Y = X @ W_sym + A_group_sum @ delta  (delta None: symmetric).  X [M,K] fp16/bf16."""
     torch = _torch()
-    out_dtype = out_dtype or torch.float16
     _require_cuda(X, Bpacked, S, delta, out)
     M, K = X.shape
     N = Bpacked.numel() * 8 // K
-    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=X.device)
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=X.device)
     variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
-    need = workspace_size(variant, M, N, K, group_size) if M > 0 else 0
-    ws = workspace if workspace is not None else (_workspace(X.device, need) if need else None)
-    _check(load_library().wq_gemm_w4a16(
-        _ptr(X), _dtype_code(X.dtype), _ptr(Bpacked), _ptr(S), _ptr(delta), _ptr(Y),
-        _dtype_code(Y.dtype), M, N, K, group_size, _ptr(ws),
-        ws.numel() if ws is not None else 0, _stream()), "wq_gemm_w4a16")
+    lib = _lib or load_library()
+    _call_gemm(lib.wq_gemm_w4a16, "wq_gemm_w4a16",
+               (X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
+                delta.data_ptr() if delta is not None else None, Y.data_ptr(), _dtype_code(Y.dtype),
+                M, N, K, group_size), (), workspace, variant, M, N, K, group_size, X.device,
+               _raw_stream(X.device.index))
     return Y
 
 
@@ -240,17 +276,15 @@ def gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size: int = 128, out_dtype=None
               workspace=None):
     """Y = x_scale[m] * Xq @ W_sym  (folded weights).  Xq [M,K] int8."""
     torch = _torch()
-    out_dtype = out_dtype or torch.float16
     _require_cuda(Xq, x_scale, Bpacked, S_abs, out)
     M, K = Xq.shape
     N = Bpacked.numel() * 8 // K
-    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=Xq.device)
-    need = workspace_size(VARIANT_W4A8, M, N, K, group_size) if M > 0 else 0
-    ws = workspace if workspace is not None else (_workspace(Xq.device, need) if need else None)
-    _check(load_library().wq_gemm_w4a8(
-        _ptr(Xq), _ptr(x_scale), _ptr(Bpacked), _ptr(S_abs), _ptr(Y), _dtype_code(Y.dtype),
-        M, N, K, group_size, _ptr(ws), ws.numel() if ws is not None else 0, _stream()),
-        "wq_gemm_w4a8")
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=Xq.device)
+    lib = _lib or load_library()
+    _call_gemm(lib.wq_gemm_w4a8, "wq_gemm_w4a8",
+               (Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S_abs.data_ptr(), Y.data_ptr(),
+                _dtype_code(Y.dtype), M, N, K, group_size), (), workspace, VARIANT_W4A8, M, N, K,
+               group_size, Xq.device, _raw_stream(Xq.device.index))
     return Y
 
 
