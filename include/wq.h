@@ -191,6 +191,30 @@ int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t* Bpacked, c
                           const float* delta, void* Y, int y_dtype, int M, int N, int K,
                           int group_size, void* stream);
 
+/*
+ * W4A16 GEMM between host buffers: X is copied host -> device, the GEMM runs
+ * as wq_gemm_w4a16 ("Marlin INT4 on Ada -- how it works", section "The
+ * pipeline, end to end": Y = X @ W_sym + A_group_sum @ delta), and Y is
+ * copied device -> host, all enqueued on `stream` with cudaMemcpyAsync.
+ * Pinned (page-locked) host buffers let the copies run asynchronously; the
+ * call returns before the work completes, so read Y_host after synchronizing
+ * the stream.  The copies to and from the host are this library's addition.
+ *   X_host   [M][K] host memory, fp16 or bf16 (x_dtype), row-major.
+ *   Y_host   [M][N] host memory, output (y_dtype F16, BF16 or F32).
+ *   Bpacked, S, delta: device, as wq_gemm_w4a16.
+ *   workspace / workspace_bytes: device scratch of at least
+ *            wq_host_workspace_size(...) bytes, 256-byte aligned: the device
+ *            copies of X and Y, then the GEMM's own workspace.
+ * All arguments are checked before anything is enqueued.
+ */
+int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked, const void* S,
+                       const float* delta, void* Y_host, int y_dtype, int M, int N, int K,
+                       int group_size, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace wq_gemm_w4a16_host needs (0 for an unsupported problem);
+ * variant WQ_VARIANT_W4A16 or WQ_VARIANT_W4A16_SYM. */
+size_t wq_host_workspace_size(int variant, int M, int N, int K, int group_size, int y_dtype);
+
 /* Bytes of workspace the GEMM needs for this problem (0 if none). */
 size_t wq_workspace_size(int variant, int M, int N, int K, int group_size);
 

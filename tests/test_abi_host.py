@@ -107,6 +107,38 @@ def test_shape_and_argument_errors_before_device_work(lib):
     assert lib.wq_set_option(wq.OPTION_WEIGHT_PREFETCH, 0) == 0
 
 
+def test_host_buffer_entry_checks_and_workspace(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    # staging for X [M,K] fp16 and Y [M,N] (256-byte aligned each) ahead of the GEMM's scratch
+    for M, N, K, y in ((16, 4096, 4096, 0), (1, 11008, 4096, 1), (512, 4096, 4096, 0), (3, 256, 384, 1)):
+        gemm = lib.wq_workspace_size(wq.VARIANT_W4A16, M, N, K, 128)
+        al = lambda b: (b + 255) // 256 * 256
+        assert lib.wq_host_workspace_size(wq.VARIANT_W4A16, M, N, K, 128, y) == al(M * K * 2) + al(M * N * 2) + gemm
+    f32 = lib.wq_host_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 128, 2)
+    assert f32 == 16 * 4096 * 2 + 16 * 4096 * 4
+    assert lib.wq_host_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128, 0) == 0  # not a host-entry variant
+    assert lib.wq_host_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4000, 128, 0) == 0
+    assert lib.wq_host_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 128, 9) == 0
+    need = lib.wq_host_workspace_size(wq.VARIANT_W4A16, 16, 256, 256, 128, 0)
+    ws = P(0x100000)  # 256-byte aligned, never dereferenced
+    h = lib.wq_gemm_w4a16_host
+    assert h(fake, 0, fake, fake, fake, fake, 0, 16, 256, 200, 128, ws, need, None) == 2      # K % 128
+    assert h(fake, 0, fake, fake, fake, fake, 0, 16, 256, 256, 64, ws, need, None) == 2       # group size
+    assert h(fake, 0, fake, fake, fake, fake, 0, -1, 256, 256, 128, ws, need, None) == 2      # M < 0
+    assert h(fake, 7, fake, fake, fake, fake, 0, 16, 256, 256, 128, ws, need, None) == 1      # x dtype
+    assert h(fake, 0, fake, fake, fake, fake, 9, 16, 256, 256, 128, ws, need, None) == 1      # y dtype
+    assert h(None, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, ws, need, None) == 1      # null X
+    assert h(fake, 0, fake, fake, fake, None, 0, 16, 256, 256, 128, ws, need, None) == 1      # null Y
+    assert h(fake, 0, P(0x10008), fake, fake, fake, 0, 16, 256, 256, 128, ws, need, None) == 1  # misaligned
+    rc = h(fake, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, ws, need - 1, None)
+    assert rc == 3 and b"needed" in lib.wq_last_error()                                          # too small
+    assert h(fake, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, None, need, None) == 3
+    assert h(fake, 0, fake, fake, fake, fake, 0, 16, 256, 256, 128, P(0x100010), need, None) == 1  # alignment
+    # host X and Y may sit at any address: only the device pointers are checked for alignment
+    assert h(None, 0, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0        # empty
+
+
 def test_no_device_means_an_error_not_a_fallback(lib):
     import torch
     if torch.cuda.is_available():

@@ -327,3 +327,32 @@ def test_back_to_back_launches_see_their_inputs(wq, prefetch):
             assert torch.equal(Y, R)
     finally:
         wq.set_weight_prefetch(False)
+
+
+@pytest.mark.parametrize("M,K,N,adt,sym,ydt", [
+    (4, 2048, 512, "f16", False, torch.float16),      # decode kernel
+    (16, 1024, 384, "bf16", True, torch.bfloat16),    # decode kernel, symmetric
+    (300, 512, 384, "f16", False, torch.float32),     # large-M kernel with the correction pre-pass
+    (130, 1280, 256, "bf16", False, torch.float16),
+])
+def test_host_buffer_entry_matches_device_entry(wq, M, K, N, adt, sym, ydt):
+    """gemm_w4a16_host (host X and Y, copies on the stream) gives the device entry's
+    result bit for bit, and the oracle's within the W4A16 tolerance; two calls in a row
+    reuse the same staging."""
+    d = synth.make_inputs(4100 + M, M, K, N, a_dtype=adt)
+    Yd, (Bp, S, dl) = _w4a16(wq, d, out_dtype=ydt, sym=sym)
+    delta = None if sym else dl
+    hX = _x(d).cpu().pin_memory()
+    hY = torch.empty((M, N), dtype=ydt).pin_memory()
+    for scale in (2.0, 1.0):
+        got = wq.gemm_w4a16_host((hX.float() * scale).to(hX.dtype).pin_memory() if scale != 1.0 else hX,
+                                 Bp, S, delta, 128, out=hY)
+        torch.cuda.synchronize()
+    assert got.data_ptr() == hY.data_ptr() and not hY.is_cuda
+    assert torch.equal(hY, Yd.cpu())
+    err = oracle.rel_fro(hY.double().numpy(), _ref_w4a16(d, sym=sym))
+    assert err <= TOL_W4A16, err
+    # a new pinned output when none is given
+    Y2 = wq.gemm_w4a16_host(hX, Bp, S, delta, 128, out_dtype=ydt)
+    torch.cuda.synchronize()
+    assert Y2.is_pinned() and torch.equal(Y2, Yd.cpu())

@@ -21,7 +21,7 @@ from . import build as _build
 
 __all__ = [
     "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
-    "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a8", "workspace_size",
+    "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
     "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "set_weight_prefetch",
@@ -52,6 +52,8 @@ EXPORTS = {
     "wq_set_option": (_I, [_I, ctypes.c_longlong]),
     "wq_gemm_w4a16_noalloc": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P]),
     "wq_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
+    "wq_gemm_w4a16_host": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
 }
 OPTION_WEIGHT_PREFETCH = 1
 
@@ -269,6 +271,39 @@ def gemm_w4a16(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=
                 delta.data_ptr() if delta is not None else None, Y.data_ptr(), _dtype_code(Y.dtype),
                 M, N, K, group_size), (), workspace, variant, M, N, K, group_size, X.device,
                _raw_stream(X.device.index))
+    return Y
+
+
+def gemm_w4a16_host(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=None,
+                    workspace=None):
+    """gemm_w4a16 between host tensors: X [M,K] fp16/bf16 on the host (pinned for
+    asynchronous copies) is copied to the weights' device, multiplied, and Y comes
+    back into a host tensor (`out`, or a new pinned one).  The copies and the GEMM
+    are enqueued on the device's current stream; Y is valid after that stream is
+    synchronized."""
+    torch = _torch()
+    if X.is_cuda or not X.is_contiguous() or (out is not None and (out.is_cuda or not out.is_contiguous())):
+        raise ValueError("X and out must be contiguous host tensors")
+    _require_cuda(Bpacked, S, delta)
+    M, K = X.shape
+    N = Bpacked.numel() * 8 // K
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, pin_memory=True)
+    variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
+    lib = _lib or load_library()
+    device = Bpacked.device
+    stream = _raw_stream(device.index)
+    ydt = _dtype_code(Y.dtype)
+    ws = workspace if workspace is not None else _stream_workspace(device, stream).buf
+    head = (X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
+            delta.data_ptr() if delta is not None else None, Y.data_ptr(), ydt, M, N, K, group_size)
+    rc = lib.wq_gemm_w4a16_host(*head, ws.data_ptr() if ws is not None else None,
+                                ws.numel() if ws is not None else 0, stream)
+    if rc == 3 and workspace is None:  # WQ_ERR_WORKSPACE: grow the stream's scratch and retry
+        need = int(lib.wq_host_workspace_size(variant, M, N, K, group_size, ydt))
+        ws = _stream_workspace(device, stream).get(need)
+        rc = lib.wq_gemm_w4a16_host(*head, ws.data_ptr(), ws.numel(), stream)
+    if rc != 0:
+        raise WQError(rc, "wq_gemm_w4a16_host", lib.wq_last_error().decode())
     return Y
 
 

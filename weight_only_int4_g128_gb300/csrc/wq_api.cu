@@ -514,6 +514,57 @@ int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const voi
                    "wq_gemm_w4a16");
 }
 
+static size_t y_elem_bytes(int y_dtype) { return y_dtype == WQ_DTYPE_F32 ? 4 : 2; }
+
+size_t wq_host_workspace_size(int variant, int M, int N, int K, int group_size, int y_dtype) {
+  if (variant != WQ_VARIANT_W4A16 && variant != WQ_VARIANT_W4A16_SYM) return 0;
+  if (y_kind_of(y_dtype) < 0 || M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
+  const int gs = (group_size == -1) ? K : group_size;
+  if (gs != 128 && gs != K) return 0;
+  return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * N * y_elem_bytes(y_dtype)) +
+         make_plan(variant, M, N, K, gs).bytes;
+}
+
+int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                       void* Y_host, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a16_host: M=%d", M);
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (x_dtype != WQ_DTYPE_F16 && x_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_host: x_dtype must be F16 or BF16");
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_host: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!X_host || !Bpacked || !S || !Y_host) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_host: null pointer");
+  if (!aligned16(Bpacked) || !aligned16(S) || (delta && !aligned16(delta)))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_host: Bpacked, S and delta must be 16-byte aligned");
+  const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
+  const size_t x_bytes = static_cast<size_t>(M) * K * 2;
+  const size_t y_bytes = static_cast<size_t>(M) * N * y_elem_bytes(y_dtype);
+  const size_t need = wq_host_workspace_size(variant, M, N, K, gs, y_dtype);
+  if (!workspace || workspace_bytes < need)
+    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a16_host: workspace of %zu bytes given, %zu needed", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_host: workspace must be 256-byte aligned");
+  if ((rc = check_device())) return rc;
+  uint8_t* const ws = static_cast<uint8_t*>(workspace);
+  void* const Xd = ws;
+  void* const Yd = ws + align256(x_bytes);
+  uint8_t* const gws = ws + align256(x_bytes) + align256(y_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(Xd, X_host, x_bytes, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of X to the device");
+  rc = gemm_core(Xd, x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16, Bpacked, S, delta, nullptr, Yd, yk, M, N, K,
+                 gs, variant, gws, workspace_bytes - (gws - ws), st, "wq_gemm_w4a16_host");
+  if (rc) return rc;
+  e = cudaMemcpyAsync(Y_host, Yd, y_bytes, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of Y to the host");
+  return WQ_OK;
+}
+
 int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S_abs, void* Y,
                  int y_dtype, int M, int N, int K, int group_size, void* workspace, size_t workspace_bytes,
                  void* stream) {
