@@ -230,7 +230,32 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   cudaError_t e;
 
   if (plan.gemv && variant != WQ_VARIANT_W4A8) {
-    // decode W4A16: one launch, activations read directly
+    // decode W4A16: one launch, activations read directly.  Up to 8 tokens the
+    // weight-streaming kernel (warp-level MMAs on register-dequantized weights)
+    // takes every problem whose segment fits its shared memory; 9..16 tokens,
+    // where the MMA work doubles, and the rest go to the tcgen05 decode kernel.
+    int gv_splits = 0, gv_kbps = 0;
+    if (wq::gemv_plan(M, N, K, gs, delta != nullptr, &gv_splits, &gv_kbps)) {
+      wq::GemmParams p{};
+      p.M = M;
+      p.N = N;
+      p.K = K;
+      p.group_size = gs;
+      p.G = G;
+      p.kb_total = K / 128;
+      p.kb_per_split = gv_kbps;
+      p.splits = gv_splits;
+      p.X = X;
+      p.B = Bpacked;
+      p.S = static_cast<const __half*>(S);
+      p.delta = delta;
+      p.Y = Y;
+      p.y_kind = y_kind;
+      p.timeout_ns = timeout_ns();
+      p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+      e = wq::launch_gemv(x_kind, p, st);
+      return after_launch(e, name, st);
+    }
     CUtensorMap tm_x, tm_s, tm_d;
     const CUtensorMapDataType xdt =
         x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

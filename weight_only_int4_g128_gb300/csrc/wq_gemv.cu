@@ -1,0 +1,508 @@
+// wq_gemv.cu -- the weight-streaming decode path (M <= 8 tokens) of the W4A16
+// GEMM: the weight codes go from HBM straight into registers, are dequantized
+// there and contracted by warp-level MMAs, so no dequantized weight is ever
+// written to shared or tensor memory.
+//
+// Why not the tcgen05 pipeline here: with at most 8 tokens the MMA's N is tiny
+// and the work is the weight stream (the opening of "Marlin INT4 on Ada -- how
+// it works": with no reuse across outputs, the weight reads bound the kernel).
+// A tcgen05 MMA takes its weight operand
+// from TMEM or shared memory, so every dequantized 128 x 128 block (32 KB of
+// fp16) must first be stored there; on this part that staging, not HBM, paces a
+// per-SM pipeline at ~275 ns per 8 KB block.  A warp-level MMA takes the weight
+// fragment from registers, where the dequant leaves it.
+//
+// Arithmetic (section "The core mismatch": W_sym = (q - 8) * scale, C = C_sym +
+// A_group_sum @ delta): each 128-k block is contracted with the exact integers
+// (q - 8) in fp16 / bf16 into fresh fp32 accumulators, then
+//     acc[n][m] += scale[g][n] * D_kb[n][m] + delta[g][n] * a_sum[kb][m]
+// in fp32, with a_sum the block sums of the token rows (fp32, computed while
+// the activation tile is staged).  The 8 token slots are the MMA's N = 8; slots
+// past M hold zeros.
+//
+// Work split: one CTA per (128-row column tile, K segment); warp w owns rows
+// 16 w .. 16 w + 15 of the tile (one m16 strip) for the whole segment.  The K
+// segments of a tile form a thread-block cluster and are reduced through
+// distributed shared memory (each rank owns a contiguous block of rows).
+//
+// Order of k inside an MMA.  The sum over k does not depend on the order in
+// which k enters an MMA, as long as the weight and activation fragments use the
+// same order.  The packed layout gives lane (g, t) of the warp the 16-byte chunk
+// t of its rows: words 4t .. 4t+3, i.e. k = 32t .. 32t+31 of the block, each
+// word holding four (even k, odd k) code pairs.  MMA step s = 4h + p (h = 0, 1;
+// p = 0..3) takes pair p of words 4t + 2h (fragment k 2t, 2t+1) and 4t + 2h + 1
+// (fragment k 2t+8, 2t+9); the activation fragment takes x at the same physical
+// k: 32t + 16h + 2p (+ 8).  One chunk of codes per row and one 64-byte run of
+// the activation row per lane cover a whole k-block with no shuffles.
+#include "wq_device.cuh"
+
+namespace wq {
+
+namespace gv {
+constexpr int kWarps = 8;                 // one 16-row strip of the 128-row tile each
+constexpr int kThreads = kWarps * 32;
+constexpr int kMT = 8;                    // token slots = MMA N
+constexpr int kMaxM = kMT;
+constexpr int kMaxSplits = 8;             // portable cluster size
+constexpr int kMaxSmem = 113 * 1024;      // two CTAs per SM
+constexpr int kUint4PerBlock = kTileN * kWordsPerKBlock / 4;  // 512
+constexpr int kRingSlot = 2 * 32 * 16;    // one k-block of one warp: 2 row halves x 32 lanes x 16 B
+constexpr int kRingDepth = 8;             // k-blocks of codes in flight per warp
+// k-blocks requested before the preceding grid has finished (weight prefetch):
+// enough to cover the hand-off, few enough that the activation loads issued
+// right after it do not queue behind a whole ring of weight traffic.
+constexpr int kPreWait = 3;
+
+// Shared memory of one CTA.  Offsets in bytes from the 128-aligned base.
+struct Layout {
+  int ring;    // per-warp code rings [8][depth][2][32][16 B]; reused for the partials
+  int xs;      // activations [8][kbps * 128] 16-bit, 16-byte chunks swizzled, rows >= M zero
+  int asum;    // block sums [kbps][8] fp32
+  int ssc;     // scales [gseg][128] fp16
+  int sdl;     // delta [gseg][128] fp32
+  int red;     // split-K partials from every rank [splits][rpr][8] fp32
+  int bars;    // sd_full, red_full mbarriers, abort flag
+  int bytes;   // total (with 128 bytes of alignment slack)
+};
+
+__host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
+
+__host__ __device__ inline Layout layout(int kbps, int splits, int gseg, bool has_delta, int depth) {
+  Layout L;
+  const int rpr = (kTileN + splits - 1) / splits;
+  int off = 0;
+  L.ring = off;
+  off = align128(off + kWarps * depth * kRingSlot);  // >= the partials [128][8] fp32
+  L.xs = off;
+  off = align128(off + kMT * kbps * kKBlock * 2);
+  L.asum = off;
+  off = align128(off + kbps * kMT * 4);
+  L.ssc = off;
+  off = align128(off + gseg * kTileN * 2);
+  L.sdl = off;
+  if (has_delta) off = align128(off + gseg * kTileN * 4);
+  L.red = off;
+  if (splits > 1) off = align128(off + splits * rpr * kMT * 4);
+  L.bars = off;
+  off = align128(off + 32);
+  L.bytes = off + 128;
+  return L;
+}
+}  // namespace gv
+
+// 16-byte asynchronous copy global -> shared (L1 bypassed), with an L2 policy.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's most recent copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// D = A * B + C, m16n8k16, fp32 accumulate; A 16 x 16 (row), B 16 x 8 (col).
+template <int XK>
+__device__ __forceinline__ void mma16816(float (&d)[4], const float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if (XK == kXBF16) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%10, %11, %12, %13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+  }
+}
+
+template <int XK>
+__device__ __forceinline__ void dq_word(uint32_t w, uint32_t (&o)[4]) {
+  if (XK == kXBF16) dq8_bf16_exact(w, o);
+  else dq8_f16_exact(w, o);
+}
+
+template <int XK>
+__device__ __forceinline__ float sum_chunk(const uint4& v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (XK == kXF16) {
+      s += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu)));
+      s += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
+    } else {
+      s += __uint_as_float(u[i] << 16);
+      s += __uint_as_float(u[i] & 0xFFFF0000u);
+    }
+  }
+  return s;
+}
+
+// Swizzle of the activation tile: logical 16-byte chunk c of token row m is
+// stored at chunk c ^ (bit 3 of c | (m & 1) << 1).  The eight lanes of a
+// quarter warp (two token rows x four lanes t, chunks 4t + q) then hit eight
+// distinct bank groups.
+__device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) | ((m & 1) << 1)); }
+
+template <int XK, int D>
+__global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams p, unsigned* status) {
+  using namespace gv;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 127u) & ~127u;
+  uint8_t* const sm = smem_raw + (base - raw);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2;
+  const int t = lane & 3;
+  const int tile = blockIdx.x;
+  const int n0 = tile * kTileN;
+  const int seg = blockIdx.y;  // == rank in the cluster (cluster dims 1 x splits x 1)
+  const int splits = p.splits;
+  const int kbps = p.kb_per_split;
+  const int kb0 = seg * kbps;
+  const int nkb = min(p.kb_total, kb0 + kbps) - kb0;
+  const bool has_delta = p.delta != nullptr;
+  const int M = p.M;
+  const int N = p.N;
+  const bool per_channel = p.G == 1;  // one group spans the whole K
+  const int g0 = per_channel ? 0 : kb0;
+  const int gseg = per_channel ? 1 : nkb;
+  const Layout L = layout(kbps, splits, per_channel ? 1 : kbps, has_delta, D);
+  const int rpr = (kTileN + splits - 1) / splits;
+  const int own_rows = max(0, min(kTileN - seg * rpr, rpr));
+
+  uint8_t* const xs = sm + L.xs;
+  float* const asum = reinterpret_cast<float*>(sm + L.asum);
+  const __half* const ssc = reinterpret_cast<const __half*>(sm + L.ssc);
+  const float* const sdl = reinterpret_cast<const float*>(sm + L.sdl);
+  const uint32_t sd_full = base + L.bars;
+  const uint32_t red_full = base + L.bars + 8;
+  volatile int* const abort_flag = reinterpret_cast<volatile int*>(sm + L.bars + 16);
+  const int xstride = kbps * kKBlock * 2;  // bytes per token row of the tile
+
+  const uint32_t sd_bytes = static_cast<uint32_t>(gseg * kTileN * (has_delta ? 6 : 2));
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    mbar_init(sd_full, 1);
+    mbar_init(red_full, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && splits > 1)
+    mbar_arrive_expect_tx(red_full, static_cast<uint32_t>(own_rows * splits * kMT * 4));
+  if (splits > 1) cluster_arrive_relaxed();  // barriers initialized and armed (waited before any copy)
+
+  // Scale and delta rows of the segment's groups: one bulk copy per row.  Like
+  // the codes, they are only ever written by the pack, so with weight prefetch
+  // they are requested before the preceding grid has finished.
+  const uint64_t pol_stream = l2_evict_first();
+  auto issue_sd = [&]() {
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(sd_full, sd_bytes);
+      for (int r = 0; r < gseg; ++r) {
+        const size_t src = static_cast<size_t>(g0 + r) * N + n0;
+        bulk_load_hint(base + L.ssc + r * kTileN * 2, p.S + src, kTileN * 2, sd_full, pol_stream);
+        if (has_delta) bulk_load_hint(base + L.sdl + r * kTileN * 4, p.delta + src, kTileN * 4, sd_full, pol_stream);
+      }
+    }
+  };
+
+  // Codes: rows rA = 16 warp + g and rB = rA + 8 of the tile, logical chunk t
+  // (stored at slot t ^ ((r / 2) % 4); both rows share the slot).
+  const int rA = 16 * warp + g;
+  const int rB = rA + 8;
+  const uint4* const blk0 =
+      reinterpret_cast<const uint4*>(p.B) + (static_cast<size_t>(tile) * p.kb_total + kb0) * kUint4PerBlock;
+  const int offA = rA * 4 + (t ^ ((g >> 1) & 3));
+  const int offB = offA + 32;
+  // Ring of this warp: slot d holds k-block (d mod D) as [row half][lane][16 B];
+  // each lane copies and later reads only its own two chunks, so the copies
+  // need no barrier: the lane's own wait_group orders them.
+  const uint32_t ring = base + L.ring + static_cast<uint32_t>(warp * D * kRingSlot + lane * 16);
+  auto issue_kb = [&](int kb, int slot) {
+    const uint4* src = blk0 + static_cast<size_t>(kb) * kUint4PerBlock;
+    cp_async16(ring + slot * kRingSlot, src + offA, pol_stream);
+    cp_async16(ring + slot * kRingSlot + 512, src + offB, pol_stream);
+  };
+  // One copy group per ring slot d in [d0, d1) (empty past the segment).
+  auto issue_codes = [&](int d0, int d1) {
+#pragma unroll
+    for (int d = 0; d < D; ++d) {
+      if (d >= d0 && d < d1) {
+        if (d < nkb) issue_kb(d, d);
+        cp_async_commit();
+      }
+    }
+  };
+  constexpr int kPre = kPreWait < D ? kPreWait : D;
+  if (p.weight_prefetch) {
+    issue_sd();
+    issue_codes(0, kPre);
+  }
+  griddep_launch_dependents();
+  griddep_wait();  // X written by the preceding grid is visible from here on
+  if (!p.weight_prefetch) {
+    issue_sd();
+    issue_codes(0, kPre);
+  }
+
+  // ---- stage the activation rows of the segment (slots >= M zero) and their
+  // 128-k block sums.  The activation loads go out first, the rest of the code
+  // ring right behind them.
+  {
+    const int per_tok = nkb * 16;  // 16-byte chunks per token row of the segment
+    const int total = kMT * per_tok;
+    const uint8_t* const xg = static_cast<const uint8_t*>(p.X);
+    constexpr int kU = 8;  // one round trip for up to 16 k-blocks x 8 tokens x 16 chunks
+    for (int b = 0; b < total; b += kThreads * kU) {
+      uint4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx = b + u * kThreads + threadIdx.x;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (idx < total) {
+          const int m = idx / per_tok;
+          const int rem = idx - m * per_tok;
+          if (m < M)
+            v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
+        }
+      }
+      if (b == 0) issue_codes(kPre, D);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int idx0 = b + u * kThreads;
+        if (idx0 >= total) break;  // uniform
+        const int idx = idx0 + threadIdx.x;
+        float s = 0.0f;
+        int m = 0, rem = 0;
+        if (idx < total) {
+          m = idx / per_tok;
+          rem = idx - m * per_tok;
+          *reinterpret_cast<uint4*>(xs + m * xstride + 16 * xswz(rem, m)) = v[u];
+          if (has_delta) s = sum_chunk<XK>(v[u]);
+        }
+        if (has_delta) {
+          // the 16 chunks of one (token, k-block) are 16 consecutive lanes
+          s += __shfl_xor_sync(0xffffffffu, s, 1);
+          s += __shfl_xor_sync(0xffffffffu, s, 2);
+          s += __shfl_xor_sync(0xffffffffu, s, 4);
+          s += __shfl_xor_sync(0xffffffffu, s, 8);
+          if (idx < total && (rem & 15) == 0) asum[(rem >> 4) * kMT + m] = s;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  {
+    const WaitCtx wsd{abort_flag, p.timeout_ns, kDevTimeoutProducer, status};
+    mbar_wait(sd_full, 0, wsd);
+  }
+
+  // ---- main loop: per k-block 8 MMA steps in two chains, then the promotion
+  float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const int sw = (t >> 1) | ((g & 1) << 1);  // xswz for this lane's chunks 4t + q: flips the low bits of q
+  const uint8_t* const xrow = xs + g * xstride + 64 * t;
+  int slot = 0;
+  for (int i = 0; i < nkb; ++i) {
+    cp_async_wait<D - 1>();  // k-block i (group i) has landed
+    const uint4 a = lds128(ring + slot * kRingSlot);
+    const uint4 c = lds128(ring + slot * kRingSlot + 512);
+    uint32_t xr[16];
+    const uint8_t* const row = xrow + i * (kKBlock * 2);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * (q ^ sw));
+      xr[4 * q] = v.x;
+      xr[4 * q + 1] = v.y;
+      xr[4 * q + 2] = v.z;
+      xr[4 * q + 3] = v.w;
+    }
+    // Steps 0..3 (words 4t, 4t+1) and 4..7 (words 4t+2, 4t+3) accumulate into
+    // two independent chains, interleaved, and are added once per k-block.
+    uint32_t r0[2][4], r1[2][4], r2[2][4], r3[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      dq_word<XK>(h ? a.z : a.x, r0[h]);  // row g, fragment k 2t..2t+1
+      dq_word<XK>(h ? c.z : c.x, r1[h]);  // row g + 8
+      dq_word<XK>(h ? a.w : a.y, r2[h]);  // row g, fragment k 2t+8..2t+9
+      dq_word<XK>(h ? c.w : c.y, r3[h]);  // row g + 8
+    }
+    // The ring slot has been read (the dequantized words exist, so both loads
+    // returned): refill it with k-block i + D.
+    asm volatile("" ::"r"(r0[0][0]), "r"(r1[0][0]), "r"(r2[1][3]), "r"(r3[1][3]) : "memory");
+    if (i + D < nkb) issue_kb(i + D, slot);
+    cp_async_commit();
+    slot = (slot + 1 == D) ? 0 : slot + 1;
+    float acc[2][4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      mma16816<XK>(acc[h], zero4, r0[h][0], r1[h][0], r2[h][0], r3[h][0], xr[8 * h], xr[8 * h + 4]);
+#pragma unroll
+    for (int pp = 1; pp < 4; ++pp)
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        mma16816<XK>(acc[h], acc[h], r0[h][pp], r1[h][pp], r2[h][pp], r3[h][pp], xr[8 * h + pp], xr[8 * h + 4 + pp]);
+    const int gl = per_channel ? 0 : i;
+    const float sA = __half2float(ssc[gl * kTileN + rA]);
+    const float sB = __half2float(ssc[gl * kTileN + rB]);
+    float d[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) d[e] = acc[0][e] + acc[1][e];
+    if (has_delta) {
+      const float dA = sdl[gl * kTileN + rA];
+      const float dB = sdl[gl * kTileN + rB];
+      const float2 as = *reinterpret_cast<const float2*>(asum + i * kMT + 2 * t);
+      tot[0] = fmaf(dA, as.x, fmaf(sA, d[0], tot[0]));
+      tot[1] = fmaf(dA, as.y, fmaf(sA, d[1], tot[1]));
+      tot[2] = fmaf(dB, as.x, fmaf(sB, d[2], tot[2]));
+      tot[3] = fmaf(dB, as.y, fmaf(sB, d[3], tot[3]));
+    } else {
+      tot[0] = fmaf(sA, d[0], tot[0]);
+      tot[1] = fmaf(sA, d[1], tot[1]);
+      tot[2] = fmaf(sB, d[2], tot[2]);
+      tot[3] = fmaf(sB, d[3], tot[3]);
+    }
+  }
+  cp_async_wait<0>();  // nothing of this thread is in flight (the trailing groups are empty)
+
+  // ---- split-K reduction + store
+  __syncthreads();  // every warp is done with its ring and the activation tile
+  const bool aborted = *abort_flag != 0;
+  if (aborted) {
+    if (threadIdx.x == 0) {
+      // let the scale / delta copies land before the shared memory is reused or the CTA exits
+      volatile int never = 0;
+      const WaitCtx drain{&never, 50000000ull, kDevTimeoutProducer, status};
+      mbar_wait(sd_full, 0, drain);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) tot[e] = __int_as_float(0x7fc00000);
+    __syncthreads();
+  }
+  if (splits == 1) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int tok = 2 * t + (e & 1);
+      const int row = (e < 2) ? rA : rB;
+      if (tok < M) store_y_any(p.Y, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
+    }
+    return;
+  }
+  // Partials, row-major [128 rows][8 tokens], in the ring area: the rows rank o
+  // owns are one contiguous block.
+  float* const part = reinterpret_cast<float*>(sm + L.ring);
+  *reinterpret_cast<float2*>(part + rA * kMT + 2 * t) = make_float2(tot[0], tot[1]);
+  *reinterpret_cast<float2*>(part + rB * kMT + 2 * t) = make_float2(tot[2], tot[3]);
+  fence_proxy_async_smem();  // the generic writes become visible to the bulk copies
+  __syncthreads();
+  cluster_wait();  // every rank's barriers are initialized and armed
+  if (warp == 0) {
+    if (lane < splits) {
+      const int o = lane;
+      const int rows_o = min(kTileN - o * rpr, rpr);
+      if (rows_o > 0) {
+        bulk_copy_to_peer(mapa_shared(base + L.red + static_cast<uint32_t>(seg * rpr * kMT * 4), o),
+                          base + L.ring + static_cast<uint32_t>(o * rpr * kMT * 4),
+                          static_cast<uint32_t>(rows_o * kMT * 4), mapa_shared(red_full, o));
+      }
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the partials stay valid until the copies have read them
+    }
+  }
+  const float* const red = reinterpret_cast<const float*>(sm + L.red);
+  const int total = own_rows * M;
+  if (static_cast<int>(threadIdx.x) < total) {
+    volatile int never = 0;
+    const WaitCtx wred{&never, p.timeout_ns, kDevTimeoutFixup, status};
+    mbar_wait(red_full, 0, wred);
+  }
+  for (int i = threadIdx.x; i < total; i += kThreads) {
+    const int m = i / own_rows;
+    const int lr = i - m * own_rows;
+    float sum = 0.0f;
+    for (int src = 0; src < splits; ++src) sum += red[(src * rpr + lr) * kMT + m];
+    store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
+  }
+}
+
+// Split of K over a thread-block cluster for the weight-streaming path: the
+// most K segments (at most 8, the portable cluster size) that still give one
+// wave of two CTAs per SM, so that every SM streams with 16 warps.  Returns 0
+// when the problem is not for this path (M > 8) or no split fits the shared
+// memory limit.
+int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_out, int* kbps_out) {
+  if (M < 1 || M > gv::kMaxM) return 0;
+  const int kb = K / kKBlock;
+  const int tiles = N / kTileN;
+  int best = -1;
+  for (int s = 1; s <= gv::kMaxSplits && s <= kb; ++s) {
+    const int kbps = (kb + s - 1) / s;
+    const int sp = (kb + kbps - 1) / kbps;
+    const int gseg = (group_size == K) ? 1 : kbps;
+    if (gv::layout(kbps, sp, gseg, has_delta, gv::kRingDepth).bytes > gv::kMaxSmem) continue;
+    if (best < 0 || tiles * sp <= 2 * kNumSMs) best = sp;
+  }
+  if (best < 0) return 0;
+  *splits_out = best;
+  *kbps_out = (kb + best - 1) / best;
+  return 1;
+}
+
+template <int XK, int D>
+static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
+  static unsigned long long attr_mask = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(attr_mask & bit)) {
+    e = cudaFuncSetAttribute(gemv_kernel<XK, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
+    if (e != cudaSuccess) return e;
+    attr_mask |= bit;
+  }
+  const int gseg = (p.G == 1) ? 1 : p.kb_per_split;
+  const gv::Layout L = gv::layout(p.kb_per_split, p.splits, gseg, p.delta != nullptr, D);
+  if (L.bytes > gv::kMaxSmem) return cudaErrorInvalidValue;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.N / kTileN, p.splits, 1);
+  cfg.blockDim = dim3(gv::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = L.bytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = p.splits;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D>, p, status);
+}
+
+cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
+  unsigned* status = status_word();
+  if (!status) return cudaErrorInvalidSymbol;
+  if (p.splits < 1 || p.splits > gv::kMaxSplits || p.M < 1 || p.M > gv::kMaxM || p.x_scale || !p.X ||
+      p.kb_per_split < 1 || (p.splits - 1) * p.kb_per_split >= p.kb_total)
+    return cudaErrorInvalidValue;
+  if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth>(p, status, stream);
+  return launch_gemv_t<kXF16, gv::kRingDepth>(p, status, stream);
+}
+
+}  // namespace wq

@@ -36,6 +36,7 @@ struct GemmParams {
   int splits;            // number of K segments (one thread-block cluster per tile)
   int aug_stages;        // correction stages (Kaug / 128), 0 when there is no correction
   int kaug;              // padded correction length (multiple of 128)
+  const void* X;         // [M][K] activations (weight-streaming decode kernel)
   const uint32_t* B;     // packed weights, blocked layout (one 8 KB block per tile, k-block)
   const __half* S;       // [G][N] group scales
   const float* delta;    // [G][N] zero-point residual, or null
@@ -59,6 +60,8 @@ int decode_max_splits();
 cudaError_t launch_decode16(int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
                             const GemmParams& p, cudaStream_t stream);
 int decode16_max_splits();
+cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream);
+int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits, int* kb_per_split);
 int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
