@@ -56,7 +56,7 @@ constexpr int kPreWait = 3;
 // Shared memory of one CTA.  Offsets in bytes from the 128-aligned base.
 struct Layout {
   int ring;    // per-warp code rings [8][depth][2][32][16 B]; reused for the partials
-  int xs;      // activations [8][kbps * 128] 16-bit, 16-byte chunks swizzled, rows >= M zero
+  int xs;      // activations [M][kbps * 128] 16-bit, 16-byte chunks swizzled, then one zero k-block
   int asum;    // block sums [kbps][8] fp32
   int ssc;     // scales [gseg][128] fp16
   int sdl;     // delta [gseg][128] fp32
@@ -67,14 +67,14 @@ struct Layout {
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline Layout layout(int kbps, int splits, int gseg, bool has_delta, int depth) {
+__host__ __device__ inline Layout layout(int M, int kbps, int splits, int gseg, bool has_delta, int depth) {
   Layout L;
   const int rpr = (kTileN + splits - 1) / splits;
   int off = 0;
   L.ring = off;
   off = align128(off + kWarps * depth * kRingSlot);  // >= the partials [128][8] fp32
   L.xs = off;
-  off = align128(off + kMT * kbps * kKBlock * 2);
+  off = align128(off + (M * kbps + 1) * kKBlock * 2);
   L.asum = off;
   off = align128(off + kbps * kMT * 4);
   L.ssc = off;
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   const bool per_channel = p.G == 1;  // one group spans the whole K
   const int g0 = per_channel ? 0 : kb0;
   const int gseg = per_channel ? 1 : nkb;
-  const Layout L = layout(kbps, splits, per_channel ? 1 : kbps, has_delta, D);
+  const Layout L = layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, D);
   const int rpr = (kTileN + splits - 1) / splits;
   const int own_rows = max(0, min(kTileN - seg * rpr, rpr));
 
@@ -210,10 +210,13 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   // the codes, they are only ever written by the pack, so with weight prefetch
   // they are requested before the preceding grid has finished.
   const uint64_t pol_stream = l2_evict_first();
+  // The lanes of warp 0 issue the copies side by side (one group row each), so
+  // no thread is held up issuing them one after the other.
   auto issue_sd = [&]() {
-    if (threadIdx.x == 0) {
-      mbar_arrive_expect_tx(sd_full, sd_bytes);
-      for (int r = 0; r < gseg; ++r) {
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(sd_full, sd_bytes);
+      __syncwarp();
+      for (int r = lane; r < gseg; r += 32) {
         const size_t src = static_cast<size_t>(g0 + r) * N + n0;
         bulk_load_hint(base + L.ssc + r * kTileN * 2, p.S + src, kTileN * 2, sd_full, pol_stream);
         if (has_delta) bulk_load_hint(base + L.sdl + r * kTileN * 4, p.delta + src, kTileN * 4, sd_full, pol_stream);
@@ -260,12 +263,16 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
     issue_codes(0, kPre);
   }
 
-  // ---- stage the activation rows of the segment (slots >= M zero) and their
-  // 128-k block sums.  The activation loads go out first, the rest of the code
-  // ring right behind them.
+  // ---- stage the activation rows of the segment and their 128-k block sums;
+  // token slots past M read a zero k-block instead.  The activation loads go
+  // out first, the rest of the code ring right behind them.
   {
     const int per_tok = nkb * 16;  // 16-byte chunks per token row of the segment
-    const int total = kMT * per_tok;
+    const int total = M * per_tok;
+    if (threadIdx.x < 16)
+      *reinterpret_cast<uint4*>(xs + M * xstride + 16 * threadIdx.x) = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < kbps * kMT; i += kThreads)
+      if (i % kMT >= M) asum[i] = 0.0f;
     const uint8_t* const xg = static_cast<const uint8_t*>(p.X);
     constexpr int kU = 8;  // one round trip for up to 16 k-blocks x 8 tokens x 16 chunks
     for (int b = 0; b < total; b += kThreads * kU) {
@@ -277,8 +284,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
         if (idx < total) {
           const int m = idx / per_tok;
           const int rem = idx - m * per_tok;
-          if (m < M)
-            v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
+          v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
         }
       }
       if (b == 0) issue_codes(kPre, D);
@@ -316,14 +322,16 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const int sw = (t >> 1) | ((g & 1) << 1);  // xswz for this lane's chunks 4t + q: flips the low bits of q
-  const uint8_t* const xrow = xs + g * xstride + 64 * t;
+  // token slot g: its row of the tile, or the zero k-block (not advanced) past M
+  const uint8_t* const xrow = xs + (g < M ? g * xstride : M * xstride) + 64 * t;
+  const int xstep = g < M ? kKBlock * 2 : 0;
   int slot = 0;
   for (int i = 0; i < nkb; ++i) {
     cp_async_wait<D - 1>();  // k-block i (group i) has landed
     const uint4 a = lds128(ring + slot * kRingSlot);
     const uint4 c = lds128(ring + slot * kRingSlot + 512);
     uint32_t xr[16];
-    const uint8_t* const row = xrow + i * (kKBlock * 2);
+    const uint8_t* const row = xrow + i * xstep;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * (q ^ sw));
@@ -454,7 +462,7 @@ int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_o
     const int kbps = (kb + s - 1) / s;
     const int sp = (kb + kbps - 1) / kbps;
     const int gseg = (group_size == K) ? 1 : kbps;
-    if (gv::layout(kbps, sp, gseg, has_delta, gv::kRingDepth).bytes > gv::kMaxSmem) continue;
+    if (gv::layout(M, kbps, sp, gseg, has_delta, gv::kRingDepth).bytes > gv::kMaxSmem) continue;
     if (best < 0 || tiles * sp <= 2 * kNumSMs) best = sp;
   }
   if (best < 0) return 0;
@@ -476,7 +484,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
     attr_mask |= bit;
   }
   const int gseg = (p.G == 1) ? 1 : p.kb_per_split;
-  const gv::Layout L = gv::layout(p.kb_per_split, p.splits, gseg, p.delta != nullptr, D);
+  const gv::Layout L = gv::layout(p.M, p.kb_per_split, p.splits, gseg, p.delta != nullptr, D);
   if (L.bytes > gv::kMaxSmem) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, p.splits, 1);
