@@ -412,7 +412,7 @@ def run_gpu(args, shapes, ws, rank, local):
                     if peaks_src == "measured" else "fallback 1.7 PFLOP/s sustained"}
     roofline.update({
         "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-        "kernel": "wq::decode16_kernel (W4A16, M <= 16) / wq::gemm_kernel; time per GEMM call",
+        "kernel": "wq::gemv_kernel (W4A16, M <= 8) / wq::decode16_kernel (M 9..16) / wq::gemm_kernel; time per GEMM call",
         "traffic_launch": ({"shape": traffic["shape"], "algorithmic_bytes": traffic["algorithmic_bytes_per_launch"],
                             "source": traffic["capture"]} if traffic else None),
         "per_shape": shape_rows})
