@@ -90,9 +90,10 @@ def test_w4a16_small_parity(wq, M, K, N, gs, adt):
     assert err <= TOL_W4A16, err
 
 
+@pytest.mark.parametrize("M", [33, 5])
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
-def test_w4a16_output_dtypes(wq, out_dtype):
-    d = synth.make_inputs(77, 33, 512, 256)
+def test_w4a16_output_dtypes(wq, out_dtype, M):
+    d = synth.make_inputs(77, M, 512, 256)
     Y, _ = _w4a16(wq, d, out_dtype)
     assert Y.dtype == out_dtype
     err = oracle.rel_fro(Y.double().cpu().numpy(), _ref_w4a16(d))
@@ -356,3 +357,23 @@ def test_host_buffer_entry_matches_device_entry(wq, M, K, N, adt, sym, ydt):
     Y2 = wq.gemm_w4a16_host(hX, Bp, S, delta, 128, out_dtype=ydt)
     torch.cuda.synchronize()
     assert Y2.is_pinned() and torch.equal(Y2, Yd.cpu())
+
+
+@pytest.mark.parametrize("M,K,N,gs,adt", [
+    (3, 1408, 256, 128, "f16"),     # 11 k-blocks over 6 segments of 2: the last segment has one
+    (2, 256, 20480, 128, "f16"),    # 160 column tiles: one segment, partials stored from registers
+    (1, 2560, 19200, 128, "f16"),   # 150 tiles x 2 segments of 10 k-blocks: the 8-deep ring wraps
+    (8, 2560, 19200, -1, "bf16"),   # the same with 8 tokens, one group per column, bf16
+    (5, 3968, 384, 128, "bf16"),    # 31 k-blocks over 8 segments of 4 (the last 3)
+])
+def test_weight_streaming_decode_segments(wq, M, K, N, gs, adt):
+    """Decode shapes (M <= 8) whose K segmentation exercises a ragged last segment,
+    a single segment (no cluster reduction) and a code ring that wraps several
+    times; compared with the oracle element by element."""
+    d = synth.make_inputs(5300 + M * 13 + K, M, K, N, group_size=gs, a_dtype=adt)
+    Y, _ = _w4a16(wq, d)
+    ref = _ref_w4a16(d)
+    got = Y.double().cpu().numpy()
+    err = oracle.rel_fro(got, ref)
+    assert err <= TOL_W4A16, err
+    assert np.isfinite(got).all()
