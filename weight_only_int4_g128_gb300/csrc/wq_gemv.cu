@@ -258,10 +258,6 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   }
   griddep_launch_dependents();
   griddep_wait();  // X written by the preceding grid is visible from here on
-  if (!p.weight_prefetch) {
-    issue_sd();
-    issue_codes(0, kPre);
-  }
 
   // ---- stage the activation rows of the segment and their 128-k block sums;
   // token slots past M read a zero k-block instead.  The activation loads go
@@ -287,7 +283,13 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
           v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
         }
       }
-      if (b == 0) issue_codes(kPre, D);
+      if (b == 0) {
+        if (!p.weight_prefetch) {
+          issue_sd();
+          issue_codes(0, kPre);
+        }
+        issue_codes(kPre, D);
+      }
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int idx0 = b + u * kThreads;
