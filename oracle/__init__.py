@@ -75,6 +75,7 @@ def _load():
             lib.wq_o_gemm_asym_identity.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
             lib.wq_o_group_sum.argtypes = [P, I, I, I, P]
             lib.wq_o_gemm_w4a8.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+            lib.wq_o_gemm_w4a8_asym.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P]
             lib.wq_o_quantize_per_token.argtypes = [P, I, I, P, P]
             lib.wq_o_rel_fro.restype = ctypes.c_double
             lib.wq_o_rel_fro.argtypes = [P, P, ctypes.c_int64]
@@ -276,6 +277,25 @@ def gemm_w4a8(Xq, x_scale, q, scale_bits, group_size, cols=None) -> np.ndarray:
     C = np.empty((M, n1 - n0), np.float64)
     lib.wq_o_gemm_w4a8(_p(X), _p(xs), _p(q), _p(s), M, K, N, _gs(K, group_size), n0, n1,
                        _p(C))
+    return C
+
+
+def gemm_w4a8_asym(Xq, x_scale, q, scale_bits, zero_bits, group_size, cols=None) -> np.ndarray:
+    """C = x_scale[m] * sum_k Xq[m,k] (q*scale + zero), fp64 (unsigned codes with a
+    zero point, no fold; HyperQwen W4A8 article, "int8 tensor cores: how the numbers
+    were verified", item 2)."""
+    lib = _load()
+    X = _c(Xq, np.int8)
+    xs = _c(x_scale, np.float32)
+    q = _c(q, np.uint8)
+    s = _c(scale_bits, np.uint16)
+    z = _c(zero_bits, np.uint16)
+    M, K = X.shape
+    N = q.shape[1]
+    n0, n1 = _cols(N, cols)
+    C = np.empty((M, n1 - n0), np.float64)
+    lib.wq_o_gemm_w4a8_asym(_p(X), _p(xs), _p(q), _p(s), _p(z), M, K, N, _gs(K, group_size), n0, n1,
+                            _p(C))
     return C
 
 

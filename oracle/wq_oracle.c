@@ -402,6 +402,42 @@ WQ_O_API void wq_o_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint8
   free(Ws);
 }
 
+/* W4A8 with zero-point (asymmetric) uint4 weights ([HQ] "int8 tensor cores:
+ * how the numbers were verified", item 2: int8 activations against uint4
+ * codes that carry a zero point; the weight is the one [ADA] "The core
+ * mismatch" defines, q * scale + zero):
+ *   C[m][n] = x_scale[m] * sum_k Xq[m][k] * (q[k][n] * scale[g][n] + zero[g][n])
+ * in binary64 (the plain definition), columns n0 <= n < n1.  No fold: the
+ * codes are the unsigned uint4 values and the scales keep their signs. */
+WQ_O_API void wq_o_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint8_t* q,
+                                  const uint16_t* scale, const uint16_t* zero, int M, int K,
+                                  int N, int gs, int n0, int n1, double* C) {
+  int NC = n1 - n0;
+  double* W = (double*)malloc(sizeof(double) * (size_t)K * NC);
+  for (int k = 0; k < K; ++k) {
+    int g = k / gs;
+    for (int c = 0; c < NC; ++c) {
+      int n = n0 + c;
+      double s = wq_o_half_to_double(scale[(int64_t)g * N + n]);
+      double z = (g_mutation == 6) ? 0.0 : wq_o_half_to_double(zero[(int64_t)g * N + n]);
+      W[(int64_t)k * NC + c] = (double)q[(int64_t)k * N + n] * s + z;
+    }
+  }
+#pragma omp parallel for schedule(static)
+  for (int m = 0; m < M; ++m) {
+    double* crow = C + (int64_t)m * NC;
+    for (int c = 0; c < NC; ++c) crow[c] = 0.0;
+    for (int k = 0; k < K; ++k) {
+      double a = (double)Xq[(int64_t)m * K + k];
+      const double* wrow = W + (int64_t)k * NC;
+      for (int c = 0; c < NC; ++c) crow[c] += a * wrow[c];
+    }
+    double xs = (double)x_scale[m];
+    for (int c = 0; c < NC; ++c) crow[c] *= xs;
+  }
+  free(W);
+}
+
 /* ---------------------------------------------------------------------- */
 /* Per-token int8 activation quantization ([HQ] "why W4A8": activations    */
 /* are quantized per token to int8)                                        */

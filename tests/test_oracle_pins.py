@@ -373,6 +373,50 @@ def test_error_magnitudes_match_printed_numbers():
     assert e8 < float(vals["w4a8_acceptance"])
 
 
+# --------------------------------------------------------------------------- W4A8, zero-point weights
+
+def test_w4a8_asym_integer_closed_form():
+    """Unit scales and integer zero points make every weight the integer q + z, so C is
+    x_scale[m] times an exact int64 matmul (a textbook integer product)."""
+    rng = _rng(40)
+    M, K, N = 3, 384, 24
+    Xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    xs = rng.uniform(0.01, 0.05, size=M).astype(np.float32)
+    q = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    G = K // 128
+    zi = rng.integers(-12, 5, size=(G, N))
+    sb = oracle.half_bits(np.ones((G, N), np.float16))
+    zb = oracle.half_bits(zi.astype(np.float16))
+    W = q.astype(np.int64) + np.repeat(zi, 128, axis=0)
+    want = (Xq.astype(np.int64) @ W).astype(np.float64) * xs.astype(np.float64)[:, None]
+    got = oracle.gemm_w4a8_asym(Xq, xs, q, sb, zb, 128)
+    assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("gs", [128, -1])
+def test_w4a8_asym_equals_identity_form_on_int8_rows(gs):
+    """x_scale * (Xq @ W_sym + group_sum(Xq) @ delta): the W4A16 identity form (pinned above)
+    applied to the int8 rows as exact fp64 values, then scaled per token."""
+    d = synth.make_inputs(41, 4, 512, 32, group_size=gs)
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    got = oracle.gemm_w4a8_asym(Xq, xs, d["q"], sb, zb, gs)
+    ident = oracle.gemm_asym_identity(Xq.astype(np.float64), d["q"], sb, zb, gs) * xs.astype(np.float64)[:, None]
+    assert oracle.rel_fro(got, ident) <= 1e-12
+
+
+def test_w4a8_asym_reduces_to_symmetric_when_zero_is_minus_8_scale():
+    """zero = -8 scale (delta = 0) turns q*s + z into (q - 8)*s: the symmetric W4A8
+    reference with the same (positive, so unfolded) scales, exactly."""
+    d = synth.make_inputs(42, 2, 256, 16)
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    sb = oracle.half_bits(d["scale"])
+    z = (-8.0 * d["scale"].astype(np.float64)).astype(np.float16)  # exact: times a power of two
+    got = oracle.gemm_w4a8_asym(Xq, xs, d["q"], sb, oracle.half_bits(z), 128)
+    want = oracle.gemm_w4a8(Xq, xs, d["q"], sb, 128)
+    assert np.array_equal(got, want)
+
+
 # --------------------------------------------------------------------------- pin sensitivity
 
 def _pins_pass():
@@ -383,15 +427,17 @@ def _pins_pass():
         test_fold_equivalence_except_minus8()
         test_w4a8_matches_integer_closed_form()
         test_zero_weights_give_zero()
+        test_w4a8_asym_integer_closed_form()
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5, 6])
 def test_planted_mistakes_are_caught(mid):
     """A plausible mistake planted in the oracle (wrong delta sign, wrong clamp, wrong
-    offset, dropped correction, dropped activation scale) fails at least one pin."""
+    offset, dropped correction, dropped activation scale, dropped W4A8 zero point) fails
+    at least one pin."""
     assert _pins_pass()
     with oracle.mutation(mid):
         assert not _pins_pass()
