@@ -67,6 +67,7 @@ extern "C" {
 #define WQ_VARIANT_W4A16 0      /* wq_gemm_w4a16 with delta (asymmetric) */
 #define WQ_VARIANT_W4A16_SYM 1  /* wq_gemm_w4a16 with delta == NULL */
 #define WQ_VARIANT_W4A8 2       /* wq_gemm_w4a8 */
+#define WQ_VARIANT_W4A8_ASYM 3  /* wq_gemm_w4a8_asym with delta (zero-point weights) */
 
 /*
  * Load-time pack of asymmetric W4A16 weights ("Marlin INT4 on Ada", section
@@ -148,6 +149,27 @@ int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const voi
 int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked,
                  const void* S_abs, void* Y, int y_dtype, int M, int N, int K, int group_size,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * W4A8 GEMM with zero-point (asymmetric) uint4 weights (HyperQwen W4A8
+ * article, section "int8 tensor cores: how the numbers were verified", item
+ * 2: int8 activations against uint4 codes with a zero point; the weight is
+ * q * scale + zero as "Marlin INT4 on Ada", section "The core mismatch",
+ * defines it):
+ *   Y[m][n] = x_scale[m] * sum_k Xq[m][k] * (q[k][n] * scale[g][n] + zero[g][n])
+ *           = x_scale[m] * (sum_k Xq[m][k] (q - 8) scale + sum_g a_sum[m][g] delta[g][n])
+ * with a_sum the group sums of the int8 rows (exact in fp32).
+ *   Xq, x_scale as wq_gemm_w4a8.
+ *   Bpacked, S, delta from wq_pack_w4a16 (codes unfolded, scales with their
+ *            signs, delta = zero + 8 scale); delta NULL gives the symmetric
+ *            product with those scales (the same as wq_gemm_w4a8).
+ *   workspace: wq_workspace_size(WQ_VARIANT_W4A8_ASYM, ...) bytes (or
+ *            WQ_VARIANT_W4A8 with delta == NULL).  Other arguments as
+ *            wq_gemm_w4a16.
+ */
+int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
+                      const float* delta, void* Y, int y_dtype, int M, int N, int K, int group_size,
+                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Per-token int8 quantization of fp16 activations (HyperQwen article, "why

@@ -139,6 +139,26 @@ def test_host_buffer_entry_checks_and_workspace(lib):
     assert h(None, 0, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0        # empty
 
 
+def test_w4a8_zero_point_entry_checks_and_workspace(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    # decode: the same activation-component scratch as W4A8; large M: W4A8's fp16 copy of the
+    # int8 rows plus the W4A16 correction columns
+    assert lib.wq_workspace_size(wq.VARIANT_W4A8_ASYM, 16, 4096, 4096, 128) == \
+        lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
+    big = lib.wq_workspace_size(wq.VARIANT_W4A8_ASYM, 512, 4096, 4096, 128)
+    assert big >= lib.wq_workspace_size(wq.VARIANT_W4A8, 512, 4096, 4096, 128) + (512 + 4096) * 128 * 2
+    assert lib.wq_workspace_size(4, 16, 4096, 4096, 128) == 0
+    f = lib.wq_gemm_w4a8_asym
+    assert f(fake, fake, fake, fake, fake, fake, 0, 16, 256, 200, 128, fake, 1 << 20, None) == 2  # K % 128
+    assert f(fake, fake, fake, fake, fake, fake, 0, 16, 256, 256, 64, fake, 1 << 20, None) == 2   # group
+    assert f(fake, fake, fake, fake, fake, fake, 9, 16, 256, 256, 128, fake, 1 << 20, None) == 1  # y dtype
+    assert f(None, fake, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1  # null Xq
+    assert f(fake, None, fake, fake, fake, fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1  # x_scale
+    assert f(fake, fake, fake, fake, P(0x10008), fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1
+    assert f(None, None, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0        # empty
+
+
 def test_no_device_means_an_error_not_a_fallback(lib):
     import torch
     if torch.cuda.is_available():

@@ -377,3 +377,40 @@ def test_weight_streaming_decode_segments(wq, M, K, N, gs, adt):
     err = oracle.rel_fro(got, ref)
     assert err <= TOL_W4A16, err
     assert np.isfinite(got).all()
+
+
+@pytest.mark.parametrize("M,K,N,gs,odt", [
+    (1, 1024, 384, 128, torch.float16),    # decode path (e4m3 components)
+    (5, 2048, 256, -1, torch.float16),
+    (16, 1280, 256, 128, torch.bfloat16),
+    (33, 768, 256, 128, torch.float16),    # large-M path (int8 -> fp16, correction columns)
+    (200, 1024, 384, 128, torch.float32),
+])
+def test_w4a8_zero_point_parity(wq, M, K, N, gs, odt):
+    """W4A8 with zero-point uint4 weights (packed by pack_w4a16, no fold): against the
+    oracle over the int8 rows (2e-3) and against the fp16-activation reference (5 %)."""
+    d = synth.make_inputs(6100 + M + K, M, K, N, group_size=gs)
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), gs)
+    Y = wq.gemm_w4a8_asym(_cuda(Xq), _cuda(xs), Bp, S, dl, gs, out_dtype=odt)
+    torch.cuda.synchronize()
+    got = Y.double().cpu().numpy()
+    sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    ref8 = oracle.gemm_w4a8_asym(Xq, xs, d["q"], sb, zb, gs)
+    err = oracle.rel_fro(got, ref8)
+    assert err <= TOL_W4A8, err
+    ref16 = oracle.gemm_asym_plain(oracle.activations_to_double(d["A"], "f16"), d["q"], sb, zb, gs)
+    assert oracle.rel_fro(got, ref16) <= TOL_W4A8_VS_F16
+
+
+@pytest.mark.parametrize("M", [4, 40])
+def test_w4a8_zero_point_without_delta_is_symmetric(wq, M):
+    """delta None: the symmetric product with the scales as given, the same as the W4A8
+    reference with those (positive, unfolded) scales."""
+    d = synth.make_inputs(6200 + M, M, 512, 256)
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    Bp, S, _ = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
+    Y = wq.gemm_w4a8_asym(_cuda(Xq), _cuda(xs), Bp, S, None, 128)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_w4a8(Xq, xs, d["q"], oracle.half_bits(d["scale"]), 128)
+    assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= TOL_W4A8

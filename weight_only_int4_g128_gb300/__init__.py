@@ -10,6 +10,7 @@ library is not built, or the device is not sm_103, calls raise.
     Bpacked, S_abs = pack_w4a8(q, scale_signed, group_size)
     Xq, x_scale = quantize_per_token(x)
     Y = gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size)
+    Y = gemm_w4a8_asym(Xq, x_scale, *pack_w4a16(q, scale, zero, group_size), group_size)
 """
 from __future__ import annotations
 
@@ -21,15 +22,16 @@ from . import build as _build
 
 __all__ = [
     "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
-    "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "workspace_size",
+    "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "gemm_w4a8_asym",
+    "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
-    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "set_weight_prefetch",
+    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "set_weight_prefetch",
     "OPTION_WEIGHT_PREFETCH",
 ]
 
 DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
-VARIANT_W4A16, VARIANT_W4A16_SYM, VARIANT_W4A8 = 0, 1, 2
+VARIANT_W4A16, VARIANT_W4A16_SYM, VARIANT_W4A8, VARIANT_W4A8_ASYM = 0, 1, 2, 3
 ERRORS = {1: "WQ_ERR_INVALID_ARG", 2: "WQ_ERR_UNSUPPORTED_SHAPE", 3: "WQ_ERR_WORKSPACE",
           4: "WQ_ERR_ARCH", 5: "WQ_ERR_CUDA", 6: "WQ_ERR_TIMEOUT"}
 
@@ -42,6 +44,7 @@ EXPORTS = {
     "wq_dequant_w4": (_I, [_P, _P, _P, _I, _I, _I, _I, _P]),
     "wq_gemm_w4a16": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_gemm_w4a8_asym": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_quantize_per_token": (_I, [_P, _P, _P, _I, _I, _P]),
     "wq_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "wq_device_supported": (_I, [_I]),
@@ -319,6 +322,24 @@ def gemm_w4a8(Xq, x_scale, Bpacked, S_abs, group_size: int = 128, out_dtype=None
     _call_gemm(lib.wq_gemm_w4a8, "wq_gemm_w4a8",
                (Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S_abs.data_ptr(), Y.data_ptr(),
                 _dtype_code(Y.dtype), M, N, K, group_size), (), workspace, VARIANT_W4A8, M, N, K,
+               group_size, Xq.device, _raw_stream(Xq.device.index))
+    return Y
+
+
+def gemm_w4a8_asym(Xq, x_scale, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=None,
+                   workspace=None):
+    """Y = x_scale[m] * (Xq @ W_sym + A_group_sum(Xq) @ delta): zero-point uint4 weights
+    packed by pack_w4a16 (delta None: symmetric with the scales as given).  Xq [M,K] int8."""
+    torch = _torch()
+    _require_cuda(Xq, x_scale, Bpacked, S, delta, out)
+    M, K = Xq.shape
+    N = Bpacked.numel() * 8 // K
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=Xq.device)
+    lib = _lib or load_library()
+    _call_gemm(lib.wq_gemm_w4a8_asym, "wq_gemm_w4a8_asym",
+               (Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S.data_ptr(),
+                delta.data_ptr() if delta is not None else None, Y.data_ptr(), _dtype_code(Y.dtype), M, N, K,
+                group_size), (), workspace, VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8, M, N, K,
                group_size, Xq.device, _raw_stream(Xq.device.index))
     return Y
 

@@ -201,18 +201,20 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   if (splits > kb) splits = kb;
   p.kb_per_split = (kb + splits - 1) / splits;
   p.splits = (kb + p.kb_per_split - 1) / p.kb_per_split;
-  p.kaug = (!p.gemv && variant == WQ_VARIANT_W4A16) ? ((3 * G + 127) / 128) * 128 : 0;
+  const bool corr = variant == WQ_VARIANT_W4A16 || variant == WQ_VARIANT_W4A8_ASYM;
+  const bool int8x = variant == WQ_VARIANT_W4A8 || variant == WQ_VARIANT_W4A8_ASYM;
+  p.kaug = (!p.gemv && corr) ? ((3 * G + 127) / 128) * 128 : 0;
   size_t off = 0;
   p.off_aug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(M) * p.kaug * 2);
   p.off_daug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
   p.off_x16 = off;
-  if (variant == WQ_VARIANT_W4A8 && !p.gemv) off = align256(off + static_cast<size_t>(M) * K * 2);
+  if (int8x && !p.gemv) off = align256(off + static_cast<size_t>(M) * K * 2);
   // decode W4A8: e4m3 activation components + per-block sums/factors row, padded: [56][K]
   // bytes (the W4A16 decode kernel reads the activations directly)
   p.off_x8 = off;
-  if (p.gemv && variant == WQ_VARIANT_W4A8) off = align256(off + static_cast<size_t>(wq::decode_b_rows()) * K);
+  if (p.gemv && int8x) off = align256(off + static_cast<size_t>(wq::decode_b_rows()) * K);
   p.bytes = off;
   return p;
 }
@@ -229,7 +231,9 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   const int G = K / gs;
   cudaError_t e;
 
-  if (plan.gemv && variant != WQ_VARIANT_W4A8) {
+  const bool int8x = variant == WQ_VARIANT_W4A8 || variant == WQ_VARIANT_W4A8_ASYM;
+  const bool corr = delta && (variant == WQ_VARIANT_W4A16 || variant == WQ_VARIANT_W4A8_ASYM);
+  if (plan.gemv && !int8x) {
     // decode W4A16: one launch, activations read directly.  Up to 8 tokens the
     // weight-streaming kernel (warp-level MMAs on register-dequantized weights)
     // takes every problem whose segment fits its shared memory; 9..16 tokens,
@@ -291,7 +295,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   if (plan.gemv) {
     // decode W4A8: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
     uint8_t* x8 = wsb + plan.off_x8;
-    const int pk = (variant == WQ_VARIANT_W4A8) ? wq::kXI8 : x_kind;
+    const int pk = int8x ? wq::kXI8 : x_kind;
     e = wq::launch_decode_prep(X, pk, M, K, x_scale, x8, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode activation pre-pass");
     CUtensorMap tm_b, tm_s, tm_d;
@@ -299,7 +303,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     if (rc) return rc;
     rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
-    if (delta && variant == WQ_VARIANT_W4A16) {
+    if (corr) {
       rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
       if (rc) return rc;
     } else {
@@ -316,7 +320,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     p.splits = plan.splits;
     p.B = Bpacked;
     p.S = static_cast<const __half*>(S);
-    p.delta = (variant == WQ_VARIANT_W4A16) ? delta : nullptr;
+    p.delta = corr ? delta : nullptr;
     p.Y = Y;
     p.y_kind = y_kind;
     p.timeout_ns = timeout_ns();
@@ -327,7 +331,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   }
 
   const void* xg = X;
-  if (variant == WQ_VARIANT_W4A8) {
+  if (int8x) {
     __half* x16 = reinterpret_cast<__half*>(wsb + plan.off_x16);
     e = wq::launch_i8_to_f16(static_cast<const int8_t*>(X), x16, static_cast<long long>(M) * K, st);
     if (e != cudaSuccess) return cuda_fail(e, "int8 -> fp16 pre-pass");
@@ -336,7 +340,8 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   __nv_bfloat16* aug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_aug);
   __nv_bfloat16* daug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_daug);
   if (plan.kaug) {
-    e = wq::launch_corr_prep(X, x_kind, delta, M, K, N, gs, G, plan.kaug, aug, daug, st);
+    // group sums of the activations the GEMM reads (for W4A8 the int8 rows as fp16, exact)
+    e = wq::launch_corr_prep(xg, x_kind, delta, M, K, N, gs, G, plan.kaug, aug, daug, st);
     if (e != cudaSuccess) return cuda_fail(e, "correction pre-pass");
   }
 
@@ -354,7 +359,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   // scale and delta rows: 8 group rows of 128 columns per copy (rows past G read as zero)
   rc = make_map(&tm_s, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, S, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
-  if (delta && variant == WQ_VARIANT_W4A16) {
+  if (corr) {
     rc = make_map(&tm_d, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, delta, G, N, 8, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (rc) return rc;
   } else {
@@ -374,7 +379,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.kaug = plan.kaug;
   p.B = Bpacked;
   p.S = static_cast<const __half*>(S);
-  p.delta = (variant == WQ_VARIANT_W4A16) ? delta : nullptr;
+  p.delta = corr ? delta : nullptr;
   p.delta_aug = plan.kaug ? daug : nullptr;
   p.x_scale = x_scale;
   p.Y = Y;
@@ -447,7 +452,7 @@ size_t wq_workspace_size(int variant, int M, int N, int K, int group_size) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
   int gs = (group_size == -1) ? K : group_size;
   if (gs != 128 && gs != K) return 0;
-  if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8) return 0;
+  if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8_ASYM) return 0;
   return make_plan(variant, M, N, K, gs).bytes;
 }
 
@@ -607,6 +612,26 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
   if ((rc = check_device())) return rc;
   return gemm_core(Xq, wq::kXF16, Bpacked, S_abs, nullptr, x_scale, Y, yk, M, N, K, gs, WQ_VARIANT_W4A8,
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "wq_gemm_w4a8");
+}
+
+int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
+                      const float* delta, void* Y, int y_dtype, int M, int N, int K, int group_size,
+                      void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a8_asym: M=%d", M);
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_asym: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!Xq || !x_scale || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_asym: null pointer");
+  if (!aligned16(Xq) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S) || (delta && !aligned16(delta)))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_asym: Xq, Bpacked, S, delta and Y must be 16-byte aligned");
+  if ((rc = check_device())) return rc;
+  return gemm_core(Xq, wq::kXF16, Bpacked, S, delta, x_scale, Y, yk, M, N, K, gs,
+                   delta ? WQ_VARIANT_W4A8_ASYM : WQ_VARIANT_W4A8, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), "wq_gemm_w4a8_asym");
 }
 
 int wq_device_status(unsigned int* status, int reset, void* stream) {
