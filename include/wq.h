@@ -172,6 +172,26 @@ int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bp
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * W4A8 GEMM on fp16 activations quantized per token inside the call
+ * (HyperQwen W4A8 article, section "why W4A8": activations quantized per token
+ * to int8).  x_scale[m] = RN32(max_k |X[m][k]| / 127) and the codes
+ * clamp(round_half_even(RN32(X / x_scale)), -127, 127) are exactly those of
+ * wq_quantize_per_token; Y is then that of wq_gemm_w4a8_asym (delta given) or
+ * wq_gemm_w4a8 (delta NULL), bit for bit.  The codes are never written out:
+ * the activation pre-pass of the GEMM quantizes them on the way (one launch
+ * instead of two).
+ *   X        [M][K] fp16 device.
+ *   x_scale  [M] fp32 device, output: the per-token scales.
+ *   Bpacked, S, delta: from wq_pack_w4a16 (zero-point weights; delta may be
+ *            NULL) or wq_pack_w4a8 (folded symmetric weights, delta NULL).
+ *   workspace: wq_workspace_size(WQ_VARIANT_W4A8_ASYM, ...) bytes with delta,
+ *            wq_workspace_size(WQ_VARIANT_W4A8, ...) without.
+ */
+int wq_gemm_w4a8_fp16(const void* X, const uint32_t* Bpacked, const void* S, const float* delta, float* x_scale,
+                      void* Y, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                      size_t workspace_bytes, void* stream);
+
+/*
  * Per-token int8 quantization of fp16 activations (HyperQwen article, "why
  * W4A8": activations quantized per token):
  *   x_scale[m] = fp32_RN(max_k |x[m][k]| / 127)

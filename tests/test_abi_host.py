@@ -159,6 +159,18 @@ def test_w4a8_zero_point_entry_checks_and_workspace(lib):
     assert f(None, None, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0        # empty
 
 
+def test_w4a8_quantize_inside_entry_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    f = lib.wq_gemm_w4a8_fp16
+    assert f(fake, fake, fake, None, fake, fake, 0, 16, 256, 200, 128, fake, 1 << 20, None) == 2   # K % 128
+    assert f(fake, fake, fake, None, fake, fake, 5, 16, 256, 256, 128, fake, 1 << 20, None) == 1   # y dtype
+    assert f(None, fake, fake, None, fake, fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1   # null X
+    assert f(fake, fake, fake, None, None, fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1   # x_scale
+    assert f(fake, fake, fake, None, P(0x10002), fake, 0, 16, 256, 256, 128, fake, 1 << 20, None) == 1
+    assert f(None, None, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0         # empty
+
+
 def test_no_device_means_an_error_not_a_fallback(lib):
     import torch
     if torch.cuda.is_available():

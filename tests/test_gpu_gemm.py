@@ -414,3 +414,32 @@ def test_w4a8_zero_point_without_delta_is_symmetric(wq, M):
     torch.cuda.synchronize()
     ref = oracle.gemm_w4a8(Xq, xs, d["q"], oracle.half_bits(d["scale"]), 128)
     assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= TOL_W4A8
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1024, 256), (7, 2048, 384), (16, 1280, 256), (40, 768, 256), (300, 1024, 384)])
+@pytest.mark.parametrize("zero_point", [False, True])
+def test_w4a8_quantize_inside_equals_two_steps(wq, M, K, N, zero_point):
+    """gemm_w4a8_fp16 (per-token quantization inside the activation pre-pass) gives the
+    x_scale of quantize_per_token and the Y of quantize_per_token + the int8 GEMM, bit for
+    bit, on both kernel paths; and the oracle's value within 2e-3."""
+    if zero_point:
+        d = synth.make_inputs(6300 + M, M, K, N)
+        Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
+    else:
+        d = synth.make_inputs(6400 + M, M, K, N, mode="w4a8")
+        Bp, S = wq.pack_w4a8(_cuda(d["q"]), _cuda(d["scale"]), 128)
+        dl = None
+    X = _cuda(d["A"])
+    Xq, xs = wq.quantize_per_token(X)
+    Y2 = wq.gemm_w4a8_asym(Xq, xs, Bp, S, dl, 128) if zero_point else wq.gemm_w4a8(Xq, xs, Bp, S, 128)
+    Y1, xs1 = wq.gemm_w4a8_fp16(X, Bp, S, dl, 128)
+    torch.cuda.synchronize()
+    assert torch.equal(xs1, xs)
+    assert torch.equal(Y1, Y2)
+    Xq_o, xs_o = oracle.quantize_per_token(d["A"])
+    if zero_point:
+        ref = oracle.gemm_w4a8_asym(Xq_o, xs_o, d["q"], oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"]), 128)
+    else:
+        qf, sfb = oracle.fold(d["q"], oracle.half_bits(d["scale"]), 128)
+        ref = oracle.gemm_w4a8(Xq_o, xs_o, qf, sfb, 128)
+    assert oracle.rel_fro(Y1.double().cpu().numpy(), ref) <= TOL_W4A8

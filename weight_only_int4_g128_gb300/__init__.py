@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
     "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "gemm_w4a8_asym",
-    "workspace_size",
+    "gemm_w4a8_fp16", "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
     "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "set_weight_prefetch",
@@ -45,6 +45,7 @@ EXPORTS = {
     "wq_gemm_w4a16": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8_asym": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_gemm_w4a8_fp16": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_quantize_per_token": (_I, [_P, _P, _P, _I, _I, _P]),
     "wq_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "wq_device_supported": (_I, [_I]),
@@ -342,6 +343,26 @@ def gemm_w4a8_asym(Xq, x_scale, Bpacked, S, delta, group_size: int = 128, out_dt
                 group_size), (), workspace, VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8, M, N, K,
                group_size, Xq.device, _raw_stream(Xq.device.index))
     return Y
+
+
+def gemm_w4a8_fp16(X, Bpacked, S, delta=None, group_size: int = 128, out_dtype=None, out=None,
+                   x_scale=None, workspace=None):
+    """W4A8 on fp16 activations X [M,K], quantized per token inside the call.  Returns
+    (Y, x_scale); Y equals gemm_w4a8_asym (delta given) / gemm_w4a8 (delta None) on the
+    codes of quantize_per_token(X), bit for bit."""
+    torch = _torch()
+    _require_cuda(X, Bpacked, S, delta, out, x_scale)
+    M, K = X.shape
+    N = Bpacked.numel() * 8 // K
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=X.device)
+    xs = x_scale if x_scale is not None else torch.empty((M,), dtype=torch.float32, device=X.device)
+    lib = _lib or load_library()
+    _call_gemm(lib.wq_gemm_w4a8_fp16, "wq_gemm_w4a8_fp16",
+               (X.data_ptr(), Bpacked.data_ptr(), S.data_ptr(), delta.data_ptr() if delta is not None else None,
+                xs.data_ptr(), Y.data_ptr(), _dtype_code(Y.dtype), M, N, K, group_size), (), workspace,
+               VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8, M, N, K, group_size, X.device,
+               _raw_stream(X.device.index))
+    return Y, xs
 
 
 # -- device queries ------------------------------------------------------------------------

@@ -220,9 +220,11 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
 }
 
 // ---------------------------------------------------------------- GEMM core
+// quant_in (W4A8 variants only): X is fp16 [M][K], quantized per token by the
+// activation pre-pass, which also writes x_scale (then an output).
 int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S, const float* delta,
               const float* x_scale, void* Y, int y_kind, int M, int N, int K, int gs, int variant,
-              void* ws, size_t ws_bytes, cudaStream_t st, const char* name) {
+              void* ws, size_t ws_bytes, cudaStream_t st, const char* name, bool quant_in = false) {
   const Plan plan = make_plan(variant, M, N, K, gs);
   if (plan.bytes > 0 && (!ws || ws_bytes < plan.bytes))
     return fail(WQ_ERR_WORKSPACE, "%s: workspace of %zu bytes given, %zu needed", name, ws_bytes, plan.bytes);
@@ -296,7 +298,8 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     // decode W4A8: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
     uint8_t* x8 = wsb + plan.off_x8;
     const int pk = int8x ? wq::kXI8 : x_kind;
-    e = wq::launch_decode_prep(X, pk, M, K, x_scale, x8, st);
+    e = quant_in ? wq::launch_decode_prep_quant(static_cast<const __half*>(X), M, K, const_cast<float*>(x_scale), x8, st)
+                 : wq::launch_decode_prep(X, pk, M, K, x_scale, x8, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode activation pre-pass");
     CUtensorMap tm_b, tm_s, tm_d;
     int rc = make_map_b3d(&tm_b, x8, wq::decode_b_rows(), K);
@@ -333,7 +336,8 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   const void* xg = X;
   if (int8x) {
     __half* x16 = reinterpret_cast<__half*>(wsb + plan.off_x16);
-    e = wq::launch_i8_to_f16(static_cast<const int8_t*>(X), x16, static_cast<long long>(M) * K, st);
+    e = quant_in ? wq::launch_quant_f16(static_cast<const __half*>(X), M, K, x16, const_cast<float*>(x_scale), st)
+                 : wq::launch_i8_to_f16(static_cast<const int8_t*>(X), x16, static_cast<long long>(M) * K, st);
     if (e != cudaSuccess) return cuda_fail(e, "int8 -> fp16 pre-pass");
     xg = x16;
   }
@@ -632,6 +636,28 @@ int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bp
   return gemm_core(Xq, wq::kXF16, Bpacked, S, delta, x_scale, Y, yk, M, N, K, gs,
                    delta ? WQ_VARIANT_W4A8_ASYM : WQ_VARIANT_W4A8, workspace, workspace_bytes,
                    static_cast<cudaStream_t>(stream), "wq_gemm_w4a8_asym");
+}
+
+int wq_gemm_w4a8_fp16(const void* X, const uint32_t* Bpacked, const void* S, const float* delta, float* x_scale,
+                      void* Y, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                      size_t workspace_bytes, void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a8_fp16: M=%d", M);
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_fp16: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!X || !x_scale || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_fp16: null pointer");
+  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S) || (delta && !aligned16(delta)) ||
+      (reinterpret_cast<uintptr_t>(x_scale) & 3u))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_fp16: X, Bpacked, S, delta and Y must be 16-byte aligned, "
+                                    "x_scale 4-byte aligned");
+  if ((rc = check_device())) return rc;
+  return gemm_core(X, wq::kXF16, Bpacked, S, delta, x_scale, Y, yk, M, N, K, gs,
+                   delta ? WQ_VARIANT_W4A8_ASYM : WQ_VARIANT_W4A8, workspace, workspace_bytes,
+                   static_cast<cudaStream_t>(stream), "wq_gemm_w4a8_fp16", true);
 }
 
 int wq_device_status(unsigned int* status, int reset, void* stream) {

@@ -148,37 +148,17 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t b) {
   return __half2float(__half(h));
 }
 
-template <int XK>
-__global__ void __launch_bounds__(256) decode_prep_kernel(const void* X, int M, int K, const float* x_scale,
-                                                          uint8_t* X8) {
-  const int nkb = K / kKBlock;
-  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (kb, m) pair, m fastest
+// One (128-k block, token) of the activation operand: this lane's 4 values v
+// (k = 128 kb + 4 lane .. + 3) become three exact e4m3 components under a
+// power-of-two block factor; lane 0 stores the block's sum and factor, both
+// times the token's scale xs.
+__device__ __forceinline__ void prep_block(const float (&v)[4], int m, int kb, int K, float xs, uint8_t* X8) {
   const int lane = threadIdx.x & 31;
-  const int m = wid & (dec::kMT - 1);
-  const int kb = wid >> 4;
-  // The decode kernel that follows may be scheduled at once: it waits for this
-  // grid to complete before it reads X8.  X may be written by the preceding
-  // grid, and X8 may still be read by it, so nothing is touched before the wait.
-  griddep_launch_dependents();
-  griddep_wait();
-  if (kb >= nkb) return;
   const size_t o = static_cast<size_t>(kb) * kKBlock + lane * 4;
   uint32_t* const r1 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m) * K + o);
   uint32_t* const r2 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m + 1) * K + o);
   uint32_t* const r3 = reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m + 2) * K + o);
   float* const srow = reinterpret_cast<float*>(X8 + static_cast<size_t>(dec::kBN) * K + static_cast<size_t>(kb) * kKBlock);
-  if (m >= M) {
-    *r1 = 0u;
-    *r2 = 0u;
-    *r3 = 0u;
-    if (lane == 0) {
-      srow[m] = 0.0f;
-      srow[dec::kMT + m] = 0.0f;
-    }
-    return;
-  }
-  float v[4];
-  load4<XK>(X, static_cast<size_t>(m) * K + o, v);
   float amax = 0.0f;
   int bad = 0;
 #pragma unroll
@@ -219,9 +199,126 @@ __global__ void __launch_bounds__(256) decode_prep_kernel(const void* X, int M, 
   *r2 = b2;
   *r3 = b3;
   if (lane == 0) {
-    const float xs = x_scale ? x_scale[m] : 1.0f;
     srow[m] = sum * xs;
     srow[dec::kMT + m] = bad ? __int_as_float(0x7fc00000) : f * xs;
+  }
+}
+
+// Token slots past M: zero components, sum and factor.
+__device__ __forceinline__ void prep_block_zero(int m, int kb, int K, uint8_t* X8) {
+  const int lane = threadIdx.x & 31;
+  const size_t o = static_cast<size_t>(kb) * kKBlock + lane * 4;
+#pragma unroll
+  for (int c = 0; c < 3; ++c) *reinterpret_cast<uint32_t*>(X8 + static_cast<size_t>(3 * m + c) * K + o) = 0u;
+  if (lane == 0) {
+    float* const srow = reinterpret_cast<float*>(X8 + static_cast<size_t>(dec::kBN) * K + static_cast<size_t>(kb) * kKBlock);
+    srow[m] = 0.0f;
+    srow[dec::kMT + m] = 0.0f;
+  }
+}
+
+template <int XK>
+__global__ void __launch_bounds__(256) decode_prep_kernel(const void* X, int M, int K, const float* x_scale,
+                                                          uint8_t* X8) {
+  const int nkb = K / kKBlock;
+  const int wid = blockIdx.x * 8 + (threadIdx.x >> 5);  // (kb, m) pair, m fastest
+  const int lane = threadIdx.x & 31;
+  const int m = wid & (dec::kMT - 1);
+  const int kb = wid >> 4;
+  // The decode kernel that follows may be scheduled at once: it waits for this
+  // grid to complete before it reads X8.  X may be written by the preceding
+  // grid, and X8 may still be read by it, so nothing is touched before the wait.
+  griddep_launch_dependents();
+  griddep_wait();
+  if (kb >= nkb) return;
+  if (m >= M) {
+    prep_block_zero(m, kb, K, X8);
+    return;
+  }
+  float v[4];
+  load4<XK>(X, static_cast<size_t>(m) * K + static_cast<size_t>(kb) * kKBlock + lane * 4, v);
+  prep_block(v, m, kb, K, x_scale ? x_scale[m] : 1.0f, X8);
+}
+
+// Per-token int8 quantization of fp16 rows (HyperQwen W4A8 article, "why
+// W4A8": activations quantized per token; absmax / 127, round half to even,
+// clamp to [-127, 127]) fused with the activation operand above: one CTA per
+// token slot computes the row's absmax, writes x_scale[m], and turns the codes
+// of every k-block into e4m3 components.  The codes and scale are the ones
+// quantize_per_token_kernel produces; they are never written out.
+__device__ __forceinline__ float quant_code(float x, float xs) {
+  if (!(xs > 0.0f)) return 0.0f;
+  return fminf(fmaxf(rintf(__fdiv_rn(x, xs)), -127.0f), 127.0f);
+}
+
+__device__ __forceinline__ float row_absmax_f16(const __half* row, int K, float* red) {
+  float amax = 0.0f;
+  for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + k);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      amax = fmaxf(amax, fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xFFFFu)))));
+      amax = fmaxf(amax, fabsf(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16)))));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  float v = 0.0f;
+  for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) v = fmaxf(v, red[i]);
+  return v;
+}
+
+__global__ void __launch_bounds__(256) decode_prep_quant_kernel(const __half* X, int M, int K, float* x_scale,
+                                                                uint8_t* X8) {
+  __shared__ float red[8];
+  const int m = blockIdx.x;  // token slot of the tile
+  const int nkb = K / kKBlock;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  griddep_launch_dependents();
+  griddep_wait();  // as decode_prep_kernel
+  if (m >= M) {
+    for (int kb = warp; kb < nkb; kb += 8) prep_block_zero(m, kb, K, X8);
+    return;
+  }
+  const __half* const row = X + static_cast<size_t>(m) * K;
+  const float xs = __fdiv_rn(row_absmax_f16(row, K, red), 127.0f);
+  if (threadIdx.x == 0) x_scale[m] = xs;
+  for (int kb = warp; kb < nkb; kb += 8) {
+    float v[4];
+    load4<kXF16>(row, static_cast<size_t>(kb) * kKBlock + lane * 4, v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = quant_code(v[i], xs);
+    prep_block(v, m, kb, K, xs, X8);
+  }
+}
+
+// The same quantization for the large-M path: one CTA per row writes the codes
+// as fp16 (exact) for the fp16 tensor-core GEMM, and x_scale[m].
+__global__ void __launch_bounds__(256) quant_f16_kernel(const __half* X, int K, __half* X16, float* x_scale) {
+  __shared__ float red[8];
+  const int m = blockIdx.x;
+  griddep_launch_dependents();
+  griddep_wait();  // X may be written by the preceding grid, X16 read by it
+  const __half* const row = X + static_cast<size_t>(m) * K;
+  const float xs = __fdiv_rn(row_absmax_f16(row, K, red), 127.0f);
+  if (threadIdx.x == 0) x_scale[m] = xs;
+  __half* const out = X16 + static_cast<size_t>(m) * K;
+  for (int k = threadIdx.x * 8; k < K; k += blockDim.x * 8) {
+    const uint4 u = *reinterpret_cast<const uint4*>(row + k);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float lo = quant_code(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] & 0xFFFFu))), xs);
+      const float hi = quant_code(__half2float(__ushort_as_half(static_cast<uint16_t>(w[i] >> 16))), xs);
+      const __half2 h2 = __floats2half2_rn(lo, hi);  // integers |c| <= 127: exact
+      o[i] = *reinterpret_cast<const uint32_t*>(&h2);
+    }
+    *reinterpret_cast<uint4*>(out + k) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -340,7 +437,6 @@ __global__ void __launch_bounds__(dec::kThreads, 2)
   const bool per_channel = p.group_size != kKBlock;  // group size 128, or one group per column
   const int g_first = per_channel ? 0 : kb0;
   auto chunk_of = [&](int it) { return per_channel ? 0 : ((kb0 + it) >> 3) - (g_first >> 3); };
-  auto chunk_row = [&](int it) { return per_channel ? 0 : ((kb0 + it) & 7); };
   int chunks_loaded = 0;  // producer lane: chunk ordinals [0, chunks_loaded) are issued
   auto group_tx = [&](int gi) { return static_cast<uint32_t>(min(kPair, nkb - kPair * gi) * kWStage + kPair * kBStage); };
   auto issue_w = [&](int gi) {  // the pair's weight tiles: one bulk copy
@@ -624,6 +720,29 @@ static cudaLaunchAttribute pdl_attr() {
   a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
   a.val.programmaticStreamSerializationAllowed = 1;
   return a;
+}
+
+cudaError_t launch_decode_prep_quant(const __half* X, int M, int K, float* x_scale, uint8_t* X8,
+                                     cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(dec::kMT, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_prep_quant_kernel, X, M, K, x_scale, X8);
+}
+
+cudaError_t launch_quant_f16(const __half* X, int M, int K, __half* X16, float* x_scale, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(M, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1] = {pdl_attr()};
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quant_f16_kernel, X, K, X16, x_scale);
 }
 
 cudaError_t launch_decode_prep(const void* X, int x_kind, int M, int K, const float* x_scale, uint8_t* X8,

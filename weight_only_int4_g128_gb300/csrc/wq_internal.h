@@ -54,6 +54,9 @@ int set_last_error(int code, const char* fmt, ...);
 // Host-side launchers (wq_gemm.cu, wq_decode.cu).
 cudaError_t launch_decode_prep(const void* X, int x_kind, int M, int K, const float* x_scale, uint8_t* X8,
                                cudaStream_t stream);
+cudaError_t launch_decode_prep_quant(const __half* X, int M, int K, float* x_scale, uint8_t* X8,
+                                     cudaStream_t stream);
+cudaError_t launch_quant_f16(const __half* X, int M, int K, __half* X16, float* x_scale, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap& tm_b, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
                           const GemmParams& p, cudaStream_t stream);
 int decode_max_splits();
