@@ -419,8 +419,8 @@ def run_gpu(args, shapes, ws, rank, local):
 
     # --- end to end through the public API: pinned host X -> device, GEMM, Y -> pinned host.
     # W4A16: one call with host buffers (wq.gemm_w4a16_host copies X in and Y out on the
-    # stream).  W4A8: the fp16 activations are copied in, quantized per token on the
-    # device, multiplied, and Y is copied back.
+    # stream).  W4A8: the fp16 activations are copied in, quantized per token inside
+    # the GEMM call (gemm_w4a8_fp16), and Y is copied back.
     e2e_steps = max(20, min(200, args.steps // 50))
     hx, hy, dx = [], [], []
     for p in probs:
@@ -432,6 +432,7 @@ def run_gpu(args, shapes, ws, rank, local):
         hx.append(t.pin_memory())
         hy.append(torch.empty((s["M"], s["N"]), dtype=torch.float16).pin_memory())
         dx.append(torch.empty(hx[-1].shape, dtype=hx[-1].dtype, device=dev) if s["mode"] == "w4a8" else None)
+        p["xs"] = torch.empty((s["M"],), dtype=torch.float32, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in hx)
     d2h = sum(t.numel() * t.element_size() for t in hy)
 
@@ -440,8 +441,7 @@ def run_gpu(args, shapes, ws, rank, local):
         Bp, S, dl = p["w"][r]
         if s["mode"] == "w4a8":
             dx[j].copy_(hx[j], non_blocking=True)
-            Xq, xs = wq.quantize_per_token(dx[j])
-            wq.gemm_w4a8(Xq, xs, Bp, S, s["group_size"], out=p["Y"], workspace=p["ws"])
+            wq.gemm_w4a8_fp16(dx[j], Bp, S, None, s["group_size"], out=p["Y"], x_scale=p["xs"], workspace=p["ws"])
             hy[j].copy_(p["Y"], non_blocking=True)
         else:
             wq.gemm_w4a16_host(hx[j], Bp, S, dl, s["group_size"], out=hy[j])
@@ -476,7 +476,7 @@ def run_gpu(args, shapes, ws, rank, local):
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "note": "pinned host X -> device, GEMM, Y -> pinned host through the public API "
-                        "(gemm_w4a16_host; W4A8: copy, quantize_per_token, gemm_w4a8, copy), "
+                        "(gemm_w4a16_host; W4A8: copy, gemm_w4a8_fp16 quantizing inside, copy), "
                         "synchronised every step"},
     }
     if rank == 0 and not args.no_cpu_baseline:
