@@ -299,6 +299,27 @@ def gemm_w4a8_asym(Xq, x_scale, q, scale_bits, zero_bits, group_size, cols=None)
     return C
 
 
+def gemm_grouped_asym(A64, expert_offsets, q, scale_bits, zero_bits, group_size) -> np.ndarray:
+    """Mixture-of-experts GEMM: rows expert_offsets[e] .. expert_offsets[e+1] of A times expert
+    e's weight q[e]*scale[e] + zero[e] (zero_bits None: (q - 8)*scale), fp64 (SGLang W4A8
+    article, section "task split": one GEMM per group).  q [E, K, N], scale/zero [E, G, N]."""
+    A = np.asarray(A64, np.float64)
+    E = len(expert_offsets) - 1
+    N = q.shape[2]
+    C = np.zeros((A.shape[0], N), np.float64)
+    wrong = _load().wq_o_get_mutation() == 7  # planted mistake: each segment takes the next expert
+    for e in range(E):
+        r0, r1 = int(expert_offsets[e]), int(expert_offsets[e + 1])
+        if r1 == r0:
+            continue
+        w = (e + 1) % E if wrong else e
+        if zero_bits is None:
+            C[r0:r1] = gemm_asym_identity(A[r0:r1], q[w], scale_bits[w], None, group_size)
+        else:
+            C[r0:r1] = gemm_asym_plain(A[r0:r1], q[w], scale_bits[w], zero_bits[w], group_size)
+    return C
+
+
 def quantize_per_token(x_f16: np.ndarray):
     """Per-token absmax int8 quantization: returns (Xq int8 [M,K], x_scale fp32 [M])."""
     lib = _load()

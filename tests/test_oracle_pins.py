@@ -417,6 +417,41 @@ def test_w4a8_asym_reduces_to_symmetric_when_zero_is_minus_8_scale():
     assert np.array_equal(got, want)
 
 
+# --------------------------------------------------------------------------- grouped (mixture of experts)
+
+def _grouped_case(seed, E=4, K=256, N=32, counts=(3, 0, 5, 2)):
+    rng = _rng(seed)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    M = int(offs[-1])
+    A = rng.standard_normal((M, K)).astype(np.float16).astype(np.float64)
+    q = rng.integers(0, 16, size=(E, K, N)).astype(np.uint8)
+    s = rng.uniform(0.005, 0.02, size=(E, K // 128, N)).astype(np.float16)
+    z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+    return A, offs, q, oracle.half_bits(s), oracle.half_bits(z)
+
+
+def test_grouped_equals_block_diagonal_gemm():
+    """The grouped product equals one plain GEMM of block-expanded rows (expert e's rows
+    occupy columns e*K .. (e+1)*K, zeros elsewhere) against the experts' weights stacked
+    along K: the zero blocks add exactly nothing, so the two agree bit for bit."""
+    A, offs, q, sb, zb = _grouped_case(50)
+    E, K, N = q.shape
+    M = A.shape[0]
+    Ablk = np.zeros((M, E * K))
+    for e in range(E):
+        Ablk[offs[e]:offs[e + 1], e * K:(e + 1) * K] = A[offs[e]:offs[e + 1]]
+    qcat = q.reshape(E * K, N)
+    want = oracle.gemm_asym_plain(Ablk, qcat, sb.reshape(-1, N), zb.reshape(-1, N), 128)
+    got = oracle.gemm_grouped_asym(A, offs, q, sb, zb, 128)
+    assert np.array_equal(got, want)
+
+
+def test_grouped_with_one_expert_is_the_plain_gemm():
+    A, _, q, sb, zb = _grouped_case(51, E=1, counts=(6,))
+    got = oracle.gemm_grouped_asym(A, [0, 6], q, sb, zb, 128)
+    assert np.array_equal(got, oracle.gemm_asym_plain(A, q[0], sb[0], zb[0], 128))
+
+
 # --------------------------------------------------------------------------- pin sensitivity
 
 def _pins_pass():
@@ -428,16 +463,17 @@ def _pins_pass():
         test_w4a8_matches_integer_closed_form()
         test_zero_weights_give_zero()
         test_w4a8_asym_integer_closed_form()
+        test_grouped_equals_block_diagonal_gemm()
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5, 6, 7])
 def test_planted_mistakes_are_caught(mid):
     """A plausible mistake planted in the oracle (wrong delta sign, wrong clamp, wrong
-    offset, dropped correction, dropped activation scale, dropped W4A8 zero point) fails
-    at least one pin."""
+    offset, dropped correction, dropped activation scale, dropped W4A8 zero point, rows
+    multiplied by the wrong expert) fails at least one pin."""
     assert _pins_pass()
     with oracle.mutation(mid):
         assert not _pins_pass()
