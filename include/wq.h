@@ -151,6 +151,29 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Grouped (mixture-of-experts) W4A16 GEMM: the token rows of X are sorted by
+ * expert, and expert e multiplies rows expert_offsets[e] .. expert_offsets[e+1]
+ * by its own weights (the grouped GEMM of the SGLang W4A8 MoE article, section
+ * "task split": one GEMM per group, tiled along K):
+ *   Y[r][n] = sum_k X[r][k] W_e[k][n]   for r in expert e's rows,
+ * each W_e the asymmetric (delta given) or symmetric weight of wq_gemm_w4a16.
+ *   X, Y          [M][K] / [M][N] device, M = expert_offsets[experts].
+ *   Bpacked       experts x (K*N/8 words) device: wq_pack_w4a16 outputs
+ *                 stacked, expert-major.
+ *   S, delta      experts x [G][N] device (delta NULL: symmetric).
+ *   expert_offsets HOST int array of experts + 1 entries, offsets[0] == 0,
+ *                 non-decreasing; experts in 1..64.
+ *   workspace     wq_workspace_size(variant, max tokens of one expert, N, K,
+ *                 group_size) bytes (0 when every expert has <= 8 tokens).
+ * With at most 8 tokens per expert this is one launch over all experts (an
+ * expert without tokens costs nothing); otherwise one GEMM per expert.
+ * Other arguments as wq_gemm_w4a16.
+ */
+int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                          void* Y, int y_dtype, const int* expert_offsets, int experts, int N, int K,
+                          int group_size, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * W4A8 GEMM with zero-point (asymmetric) uint4 weights (HyperQwen W4A8
  * article, section "int8 tensor cores: how the numbers were verified", item
  * 2: int8 activations against uint4 codes with a zero point; the weight is

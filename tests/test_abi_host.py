@@ -171,6 +171,24 @@ def test_w4a8_quantize_inside_entry_checks(lib):
     assert f(None, None, None, None, None, None, 0, 0, 256, 256, 128, None, 0, None) == 0         # empty
 
 
+def test_grouped_entry_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    f = lib.wq_gemm_w4a16_grouped
+    offs = (ctypes.c_int * 4)(0, 2, 2, 5)
+    assert f(fake, 0, fake, fake, fake, fake, 0, offs, 3, 256, 200, 128, None, 0, None) == 2      # K % 128
+    assert f(fake, 0, fake, fake, fake, fake, 0, offs, 0, 256, 256, 128, None, 0, None) == 1      # experts
+    assert f(fake, 0, fake, fake, fake, fake, 0, offs, 65, 256, 256, 128, None, 0, None) == 1
+    assert f(fake, 0, fake, fake, fake, fake, 0, None, 3, 256, 256, 128, None, 0, None) == 1      # offsets
+    bad = (ctypes.c_int * 4)(0, 3, 2, 5)
+    assert f(fake, 0, fake, fake, fake, fake, 0, bad, 3, 256, 256, 128, None, 0, None) == 1       # decreasing
+    nz = (ctypes.c_int * 4)(1, 2, 3, 5)
+    assert f(fake, 0, fake, fake, fake, fake, 0, nz, 3, 256, 256, 128, None, 0, None) == 1        # offsets[0]
+    empty = (ctypes.c_int * 4)(0, 0, 0, 0)
+    assert f(None, 0, None, None, None, None, 0, empty, 3, 256, 256, 128, None, 0, None) == 0     # no tokens
+    assert f(fake, 0, P(0x10008), fake, fake, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 1
+
+
 def test_no_device_means_an_error_not_a_fallback(lib):
     import torch
     if torch.cuda.is_available():

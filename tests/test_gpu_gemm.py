@@ -443,3 +443,52 @@ def test_w4a8_quantize_inside_equals_two_steps(wq, M, K, N, zero_point):
         qf, sfb = oracle.fold(d["q"], oracle.half_bits(d["scale"]), 128)
         ref = oracle.gemm_w4a8(Xq_o, xs_o, qf, sfb, 128)
     assert oracle.rel_fro(Y1.double().cpu().numpy(), ref) <= TOL_W4A8
+
+
+def _moe_inputs(seed, E, K, N, counts, gs=128, adt="f16", sym=False):
+    rng = np.random.default_rng(seed)
+    offs = [0] + list(np.cumsum(counts))
+    M = int(offs[-1])
+    a = rng.standard_normal((M, K))
+    if adt == "bf16":
+        A = oracle.double_to_bf16(a)  # bits
+        X = _cuda(A.view(np.int16)).view(torch.bfloat16)
+        A64 = oracle.bf16_to_double(A)
+    else:
+        A = a.astype(np.float16)
+        X = _cuda(A)
+        A64 = A.astype(np.float64)
+    G = K // (K if gs == -1 else gs)
+    q = rng.integers(0, 16, size=(E, K, N)).astype(np.uint8)
+    s = rng.uniform(0.005, 0.02, size=(E, G, N)).astype(np.float16)
+    z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+    return offs, X, A64, q, s, z
+
+
+@pytest.mark.parametrize("E,K,N,counts,gs,adt,sym", [
+    (8, 256, 7168, (3, 1, 0, 4, 2, 2, 3, 1), 128, "f16", False),   # 16 tokens over 8 experts
+    (8, 256, 7168, (2, 2, 2, 2, 2, 2, 2, 2), 128, "bf16", True),
+    (4, 1024, 512, (1, 8, 0, 5), -1, "f16", False),                  # per-channel groups
+    (3, 512, 384, (12, 0, 40), 128, "f16", False),                   # > 8 tokens: one GEMM per expert
+])
+def test_grouped_moe_parity(wq, E, K, N, counts, gs, adt, sym):
+    """Mixture-of-experts W4A16 against the oracle (each expert's rows times its own
+    weights), element by element within 2e-3."""
+    offs, X, A64, q, s, z = _moe_inputs(7000 + E + K, E, K, N, counts, gs, adt, sym)
+    packs = [wq.pack_w4a16(_cuda(q[e]), _cuda(s[e]), _cuda(z[e]), gs) for e in range(E)]
+    Bp = torch.stack([p_[0] for p_ in packs])
+    S = torch.stack([p_[1] for p_ in packs])
+    dl = None if sym else torch.stack([p_[2] for p_ in packs])
+    Y = wq.gemm_w4a16_grouped(X, Bp, S, dl, offs, gs)
+    torch.cuda.synchronize()
+    sb, zb = oracle.half_bits(s), oracle.half_bits(z)
+    ref = oracle.gemm_grouped_asym(A64, offs, q, sb, None if sym else zb, gs)
+    err = oracle.rel_fro(Y.double().cpu().numpy(), ref)
+    assert err <= TOL_W4A16, err
+    # each expert's rows equal that expert's plain GEMM through the single-problem entry
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        if r1 > r0:
+            Ye = wq.gemm_w4a16(X[r0:r1].contiguous(), Bp[e], S[e], None if sym else dl[e], gs)
+            torch.cuda.synchronize()
+            assert oracle.rel_fro(Y[r0:r1].double().cpu().numpy(), Ye.double().cpu().numpy()) <= 1e-3

@@ -23,7 +23,7 @@ from . import build as _build
 __all__ = [
     "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
     "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "gemm_w4a8_asym",
-    "gemm_w4a8_fp16", "workspace_size",
+    "gemm_w4a8_fp16", "gemm_w4a16_grouped", "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
     "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "set_weight_prefetch",
@@ -46,6 +46,7 @@ EXPORTS = {
     "wq_gemm_w4a8": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8_asym": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8_fp16": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_gemm_w4a16_grouped": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_quantize_per_token": (_I, [_P, _P, _P, _I, _I, _P]),
     "wq_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "wq_device_supported": (_I, [_I]),
@@ -363,6 +364,37 @@ def gemm_w4a8_fp16(X, Bpacked, S, delta=None, group_size: int = 128, out_dtype=N
                VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8, M, N, K, group_size, X.device,
                _raw_stream(X.device.index))
     return Y, xs
+
+
+def gemm_w4a16_grouped(X, Bpacked, S, delta, expert_offsets, group_size: int = 128, out_dtype=None,
+                       out=None, workspace=None):
+    """Mixture-of-experts W4A16: rows expert_offsets[e] .. expert_offsets[e+1] of X (sorted by
+    expert) times expert e's weights.  Bpacked [E, ...], S / delta [E, G, N] are the stacked
+    pack_w4a16 outputs; expert_offsets is a host sequence of E + 1 ints."""
+    torch = _torch()
+    _require_cuda(X, Bpacked, S, delta, out)
+    M, K = X.shape
+    E = int(S.shape[0])
+    N = int(S.shape[-1])
+    offs = (ctypes.c_int * (E + 1))(*[int(v) for v in expert_offsets])
+    if len(expert_offsets) != E + 1 or offs[E] != M:
+        raise ValueError("expert_offsets must have experts + 1 entries ending at X.shape[0]")
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=X.device)
+    lib = _lib or load_library()
+    stream = _raw_stream(X.device.index)
+    if workspace is None:
+        max_m = max((offs[e + 1] - offs[e] for e in range(E)), default=0)
+        variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
+        need = workspace_size(variant, max_m, N, K, group_size) if max_m > 0 else 0
+        workspace = _stream_workspace(X.device, stream).get(need) if need > 0 else None
+    rc = lib.wq_gemm_w4a16_grouped(X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
+                                   delta.data_ptr() if delta is not None else None, Y.data_ptr(),
+                                   _dtype_code(Y.dtype), offs, E, N, K, group_size,
+                                   workspace.data_ptr() if workspace is not None else None,
+                                   workspace.numel() if workspace is not None else 0, stream)
+    if rc != 0:
+        raise WQError(rc, "wq_gemm_w4a16_grouped", lib.wq_last_error().decode())
+    return Y
 
 
 # -- device queries ------------------------------------------------------------------------

@@ -618,6 +618,94 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
                    workspace, workspace_bytes, static_cast<cudaStream_t>(stream), "wq_gemm_w4a8");
 }
 
+int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                          void* Y, int y_dtype, const int* expert_offsets, int experts, int N, int K,
+                          int group_size, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (x_dtype != WQ_DTYPE_F16 && x_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: x_dtype must be F16 or BF16");
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: bad y_dtype %d", y_dtype);
+  if (experts < 1 || experts > wq::kMaxExperts)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: experts=%d (1..%d)", experts, wq::kMaxExperts);
+  if (!expert_offsets) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: null expert_offsets");
+  if (expert_offsets[0] != 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: expert_offsets[0] != 0");
+  int max_m = 0;
+  for (int e = 0; e < experts; ++e) {
+    const int me = expert_offsets[e + 1] - expert_offsets[e];
+    if (me < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: expert_offsets decrease at %d", e);
+    max_m = me > max_m ? me : max_m;
+  }
+  const int M = expert_offsets[experts];
+  if (M == 0) return WQ_OK;
+  if (!X || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: null pointer");
+  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(S) || !aligned16(Y) || (delta && !aligned16(delta)))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_grouped: X, Bpacked, S, delta and Y must be 16-byte aligned");
+  const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
+  const int G = K / gs;
+  const long long b_stride = static_cast<long long>(K) * N / 8;
+  const long long sd_stride = static_cast<long long>(G) * N;
+  const int xk = x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16;
+  const size_t ysz = (yk == wq::kYF32) ? 4 : 2;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // One launch over all experts when each has at most 8 tokens (the
+  // weight-streaming kernel, one K segment per tile); else one GEMM per expert.
+  int g_splits = 0, g_kbps = 0;
+  if (wq::gemv_plan(max_m, N, K, gs, delta != nullptr, &g_splits, &g_kbps) &&
+      wq::gemv_plan_fits(max_m, K / 128, 1, gs == K, delta != nullptr)) {
+    if ((rc = check_device())) return rc;
+    wq::GemmParams p{};
+    p.M = max_m;
+    p.N = N;
+    p.K = K;
+    p.group_size = gs;
+    p.G = G;
+    p.kb_total = K / 128;
+    p.kb_per_split = K / 128;
+    p.splits = 1;
+    p.X = X;
+    p.B = Bpacked;
+    p.S = static_cast<const __half*>(S);
+    p.delta = delta;
+    p.Y = Y;
+    p.y_kind = yk;
+    p.timeout_ns = timeout_ns();
+    p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+    p.experts = experts;
+    p.b_stride = b_stride;
+    p.sd_stride = sd_stride;
+    for (int e = 0; e <= experts; ++e) p.goff[e] = expert_offsets[e];
+    return after_launch(wq::launch_gemv(xk, p, st), "wq_gemm_w4a16_grouped", st);
+  }
+  // every expert's workspace need is checked before anything is enqueued
+  size_t need = 0;
+  for (int e = 0; e < experts; ++e) {
+    const int me = expert_offsets[e + 1] - expert_offsets[e];
+    if (me > 0) {
+      const size_t b = make_plan(variant, me, N, K, gs).bytes;
+      need = b > need ? b : need;
+    }
+  }
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a16_grouped: workspace of %zu bytes given, %zu needed", workspace_bytes,
+                need);
+  if ((rc = check_device())) return rc;
+  for (int e = 0; e < experts; ++e) {
+    const int r0 = expert_offsets[e];
+    const int me = expert_offsets[e + 1] - r0;
+    if (me == 0) continue;
+    rc = gemm_core(static_cast<const uint8_t*>(X) + static_cast<size_t>(r0) * K * 2, xk, Bpacked + e * b_stride,
+                   static_cast<const __half*>(S) + e * sd_stride, delta ? delta + e * sd_stride : nullptr, nullptr,
+                   static_cast<uint8_t*>(Y) + static_cast<size_t>(r0) * N * ysz, yk, me, N, K, gs, variant, workspace,
+                   workspace_bytes, st, "wq_gemm_w4a16_grouped");
+    if (rc) return rc;
+  }
+  return WQ_OK;
+}
+
 int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
                       const float* delta, void* Y, int y_dtype, int M, int N, int K, int group_size,
                       void* workspace, size_t workspace_bytes, void* stream) {

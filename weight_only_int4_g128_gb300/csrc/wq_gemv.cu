@@ -176,8 +176,26 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   const int kb0 = seg * kbps;
   const int nkb = min(p.kb_total, kb0 + kbps) - kb0;
   const bool has_delta = p.delta != nullptr;
-  const int M = p.M;
   const int N = p.N;
+  // This CTA's problem: the whole GEMM, or (grouped launch) expert blockIdx.z's
+  // token rows and weights.  An expert without tokens has nothing to do.
+  int M = p.M;
+  const uint8_t* Xp = static_cast<const uint8_t*>(p.X);
+  uint8_t* Yp = static_cast<uint8_t*>(p.Y);
+  const uint32_t* Bp = p.B;
+  const __half* Sp = p.S;
+  const float* Dp = p.delta;
+  if (p.experts > 0) {
+    const int e = blockIdx.z;
+    const int r0 = p.goff[e];
+    M = p.goff[e + 1] - r0;
+    if (M <= 0) return;
+    Xp += static_cast<size_t>(r0) * p.K * 2;
+    Yp += static_cast<size_t>(r0) * N * (p.y_kind == kYF32 ? 4 : 2);
+    Bp += e * p.b_stride;
+    Sp += e * p.sd_stride;
+    if (has_delta) Dp += e * p.sd_stride;
+  }
   const bool per_channel = p.G == 1;  // one group spans the whole K
   const int g0 = per_channel ? 0 : kb0;
   const int gseg = per_channel ? 1 : nkb;
@@ -218,8 +236,8 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
       __syncwarp();
       for (int r = lane; r < gseg; r += 32) {
         const size_t src = static_cast<size_t>(g0 + r) * N + n0;
-        bulk_load_hint(base + L.ssc + r * kTileN * 2, p.S + src, kTileN * 2, sd_full, pol_stream);
-        if (has_delta) bulk_load_hint(base + L.sdl + r * kTileN * 4, p.delta + src, kTileN * 4, sd_full, pol_stream);
+        bulk_load_hint(base + L.ssc + r * kTileN * 2, Sp + src, kTileN * 2, sd_full, pol_stream);
+        if (has_delta) bulk_load_hint(base + L.sdl + r * kTileN * 4, Dp + src, kTileN * 4, sd_full, pol_stream);
       }
     }
   };
@@ -229,7 +247,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
   const int rA = 16 * warp + g;
   const int rB = rA + 8;
   const uint4* const blk0 =
-      reinterpret_cast<const uint4*>(p.B) + (static_cast<size_t>(tile) * p.kb_total + kb0) * kUint4PerBlock;
+      reinterpret_cast<const uint4*>(Bp) + (static_cast<size_t>(tile) * p.kb_total + kb0) * kUint4PerBlock;
   const int offA = rA * 4 + (t ^ ((g >> 1) & 3));
   const int offB = offA + 32;
   // Ring of this warp: slot d holds k-block (d mod D) as [row half][lane][16 B];
@@ -269,7 +287,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
       *reinterpret_cast<uint4*>(xs + M * xstride + 16 * threadIdx.x) = make_uint4(0u, 0u, 0u, 0u);
     for (int i = threadIdx.x; i < kbps * kMT; i += kThreads)
       if (i % kMT >= M) asum[i] = 0.0f;
-    const uint8_t* const xg = static_cast<const uint8_t*>(p.X);
+    const uint8_t* const xg = Xp;
     constexpr int kU = 8;  // one round trip for up to 16 k-blocks x 8 tokens x 16 chunks
     for (int b = 0; b < total; b += kThreads * kU) {
       uint4 v[kU];
@@ -409,7 +427,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
     for (int e = 0; e < 4; ++e) {
       const int tok = 2 * t + (e & 1);
       const int row = (e < 2) ? rA : rB;
-      if (tok < M) store_y_any(p.Y, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
+      if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
     }
     return;
   }
@@ -446,7 +464,7 @@ __global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams 
     const int lr = i - m * own_rows;
     float sum = 0.0f;
     for (int src = 0; src < splits; ++src) sum += red[(src * rpr + lr) * kMT + m];
-    store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
+    store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
   }
 }
 
@@ -473,6 +491,12 @@ int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_o
   return 1;
 }
 
+// Whether a launch with these segments fits the shared memory limit.
+bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta) {
+  return M >= 1 && M <= gv::kMaxM &&
+         gv::layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, gv::kRingDepth).bytes <= gv::kMaxSmem;
+}
+
 template <int XK, int D>
 static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
@@ -489,7 +513,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   const gv::Layout L = gv::layout(p.M, p.kb_per_split, p.splits, gseg, p.delta != nullptr, D);
   if (L.bytes > gv::kMaxSmem) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.N / kTileN, p.splits, 1);
+  cfg.gridDim = dim3(p.N / kTileN, p.splits, p.experts > 0 ? p.experts : 1);
   cfg.blockDim = dim3(gv::kThreads, 1, 1);
   cfg.dynamicSmemBytes = L.bytes;
   cfg.stream = st;
@@ -509,6 +533,7 @@ cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
   unsigned* status = status_word();
   if (!status) return cudaErrorInvalidSymbol;
   if (p.splits < 1 || p.splits > gv::kMaxSplits || p.M < 1 || p.M > gv::kMaxM || p.x_scale || !p.X ||
+      p.experts < 0 || p.experts > kMaxExperts ||
       p.kb_per_split < 1 || (p.splits - 1) * p.kb_per_split >= p.kb_total)
     return cudaErrorInvalidValue;
   if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth>(p, status, stream);

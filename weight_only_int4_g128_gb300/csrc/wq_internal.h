@@ -15,6 +15,7 @@ constexpr int kTileN = 128;        // weight rows (output columns) per CTA = MMA
 constexpr int kKBlock = 128;       // K elements per pipeline stage
 constexpr int kWordsPerKBlock = kKBlock / 8;
 constexpr int kNumSMs = 152;
+constexpr int kMaxExperts = 64;    // experts of one grouped GEMM call
 
 // Status bits written by kernels into the device status word.
 constexpr unsigned kDevTimeoutProducer = 1u << 0;
@@ -46,6 +47,13 @@ struct GemmParams {
   int y_kind;
   unsigned long long timeout_ns;
   int weight_prefetch;   // issue weight copies before waiting on the preceding grid
+  // Grouped (mixture-of-experts) launch of the weight-streaming decode kernel:
+  // blockIdx.z = expert e, whose token rows are goff[e] .. goff[e+1] of X and Y
+  // and whose weights sit b_stride words / sd_stride elements after expert 0's.
+  // experts == 0: a plain GEMM.
+  int experts;
+  long long b_stride, sd_stride;
+  int goff[kMaxExperts + 1];
 };
 
 // Record the message for wq_last_error() on this thread and return `code`.
@@ -65,6 +73,7 @@ cudaError_t launch_decode16(int x_kind, const CUtensorMap& tm_x, const CUtensorM
 int decode16_max_splits();
 cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream);
 int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits, int* kb_per_split);
+bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta);
 int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
