@@ -44,6 +44,7 @@ WORKLOAD_NAMES = {
     "c2": "W4A16 asym batched M{64,128,256} K8192 N8192 g128 and per-channel fp16",
     "c3": "W4A16 asym prefill M4096 K5120 N17408 + M4096 K17408 N5120 g128 bf16",
     "c4": "W4A8 sym M{16,256,2048} K5120 N17408 g128 int8 per-token",
+    "moe": "W4A16 asym grouped (mixture of experts): 16 tokens top-1 over 8 experts, K256 N7168 g128 fp16",
 }
 
 
@@ -490,6 +491,142 @@ def run_gpu(args, shapes, ws, rank, local):
     return 0
 
 
+# ----------------------------------------------------------------------------- MoE workload
+def moe_weight_bytes(d) -> int:
+    """Weight bytes the grouped call must read: codes, scales and delta of every expert that
+    received at least one token."""
+    E, K, N = d["q"].shape
+    G = d["scale"].shape[1]
+    live = int(np.count_nonzero(np.diff(d["offsets"])))
+    return live * (K * N // 2 + G * N * 6)
+
+
+def moe_oracle(d, budget_s):
+    import oracle
+    A = d["A"].astype(np.float64)
+    sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.gemm_grouped_asym(A, d["offsets"], d["q"], sb, zb, synth.MOE["group_size"])
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return n * moe_weight_bytes(d) / el / 1e9, el, threads, f"{n} full grouped call(s), fp64 naive loops"
+
+
+def run_moe(args, ws, rank, local):
+    d = synth.moe_inputs()
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        gbs, el, threads, sample = moe_oracle(d, max(2.0, min(20.0, 4.0 * args.steps)))
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+            "config": {"workload": WORKLOAD_NAMES["moe"], "sampled": False},
+            "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return 0
+    import torch
+    import weight_only_int4_g128_gb300 as wq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wq.load_library(build_if_missing=True)
+    if not wq.device_supported(local):
+        raise RuntimeError("not an sm_103 device")
+    wq.set_weight_prefetch(True)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    E = d["q"].shape[0]
+    gs = synth.MOE["group_size"]
+    packs = [wq.pack_w4a16(cu(d["q"][e]), cu(d["scale"][e]), cu(d["zero"][e]), gs) for e in range(E)]
+    w0 = (torch.stack([p_[0] for p_ in packs]), torch.stack([p_[1] for p_ in packs]),
+          torch.stack([p_[2] for p_ in packs]))
+    wb = moe_weight_bytes(d)
+    set_bytes = sum(t.numel() * t.element_size() for t in w0)
+    reps = max(1, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    W = [w0] + [tuple(t.clone() for t in w0) for _ in range(reps - 1)]
+    offs = [int(v) for v in d["offsets"]]
+    X = cu(d["A"])
+    Y = torch.empty((X.shape[0], w0[1].shape[-1]), dtype=torch.float16, device=dev)
+    for r in range(reps):
+        wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for r in range(reps):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % reps].replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            graphs[i % reps].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    value = ws * (wb + X.numel() * 2 + Y.numel() * 2) / (ms * 1e-3) / 1e9
+    peaks, src = load_peaks()
+    achieved = wb / (ms * 1e-3) / 1e9
+    # end to end: pinned host X in, grouped call, Y to pinned host, synchronised each step
+    hx = torch.from_numpy(np.ascontiguousarray(d["A"])).pin_memory()
+    hy = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
+    dx = torch.empty_like(X)
+    n_e2e = max(20, min(500, args.steps // 20))
+    with torch.cuda.stream(stream):
+        for i in range(3 + n_e2e):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            dx.copy_(hx, non_blocking=True)
+            wq.gemm_w4a16_grouped(dx, *W[i % reps], offs, gs, out=Y)
+            hy.copy_(Y, non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "config": {"workload": WORKLOAD_NAMES["moe"], "tokens_per_expert": [offs[e + 1] - offs[e] for e in range(E)],
+                   "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
+                   "graph": "one CUDA graph per weight copy holds one grouped call",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "wq::gemv_kernel, grouped launch (grid.z = expert); weight bytes of experts with tokens",
+                     "peak_source": src},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "e2e": {"value": round(ws * wb / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": hx.numel() * 2,
+                "d2h_bytes_per_step": hy.numel() * 2},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, el, threads, sample = moe_oracle(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": sample, "seconds": round(el, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -507,6 +644,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_init()
+    if args.workload == "moe":
+        return run_moe(args, ws, rank, local)
     shapes = synth.shapes(args.workload)
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]

@@ -101,3 +101,23 @@ def make_activations(seed: int, M: int, K: int, a_dtype: str = "f16", a_std: flo
     rng = np.random.Generator(np.random.PCG64(seed))
     a = rng.standard_normal((M, K), dtype=np.float32) * np.float32(a_std)
     return _bf16_bits(a) if a_dtype == "bf16" else a.astype(np.float16)
+
+
+# Mixture-of-experts workload: 16 tokens routed (top-1) over 8 experts, each expert
+# a K=256 x N=7168 asymmetric g128 weight (the grouped W4A8 test shape of the SGLang
+# MoE article, batch 16, k 256, n 7168, 8 experts), fp16 activations.
+MOE = dict(experts=8, tokens=16, K=256, N=7168, group_size=GROUP, seed=5000)
+
+
+def moe_inputs(seed: int = MOE["seed"], experts: int = MOE["experts"], tokens: int = MOE["tokens"],
+               K: int = MOE["K"], N: int = MOE["N"], group_size: int = MOE["group_size"]):
+    """Routing counts (uniform top-1 choice per token, tokens sorted by expert), the
+    activations [tokens, K] fp16, and per-expert weights (make_inputs recipe)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    choice = rng.integers(0, experts, size=tokens)
+    counts = np.bincount(choice, minlength=experts)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    A = make_activations(seed + 1, tokens, K)
+    ws = [make_inputs(seed + 2 + e, 1, K, N, group_size=group_size, weights_only=True) for e in range(experts)]
+    return {"offsets": offsets, "A": A, "q": np.stack([w["q"] for w in ws]),
+            "scale": np.stack([w["scale"] for w in ws]), "zero": np.stack([w["zero"] for w in ws])}
