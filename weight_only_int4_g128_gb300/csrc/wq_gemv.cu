@@ -156,8 +156,11 @@ __device__ __forceinline__ float sum_chunk(const uint4& v) {
 // distinct bank groups.
 __device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) | ((m & 1) << 1)); }
 
-template <int XK, int D>
-__global__ void __launch_bounds__(gv::kThreads, 2) gemv_kernel(const GemmParams p, unsigned* status) {
+// MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
+// wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
+// per column tile and expert) then fit in one wave.
+template <int XK, int D, int MINB>
+__global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmParams p, unsigned* status) {
   using namespace gv;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -497,7 +500,7 @@ bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delt
          gv::layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, gv::kRingDepth).bytes <= gv::kMaxSmem;
 }
 
-template <int XK, int D>
+template <int XK, int D, int MINB>
 static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   int dev = 0;
@@ -505,7 +508,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_mask & bit)) {
-    e = cudaFuncSetAttribute(gemv_kernel<XK, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
+    e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
     if (e != cudaSuccess) return e;
     attr_mask |= bit;
   }
@@ -526,7 +529,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D>, p, status);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D, MINB>, p, status);
 }
 
 cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
@@ -536,8 +539,12 @@ cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
       p.experts < 0 || p.experts > kMaxExperts ||
       p.kb_per_split < 1 || (p.splits - 1) * p.kb_per_split >= p.kb_total)
     return cudaErrorInvalidValue;
-  if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth>(p, status, stream);
-  return launch_gemv_t<kXF16, gv::kRingDepth>(p, status, stream);
+  if (p.experts > 0) {
+    if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 3>(p, status, stream);
+    return launch_gemv_t<kXF16, gv::kRingDepth, 3>(p, status, stream);
+  }
+  if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 2>(p, status, stream);
+  return launch_gemv_t<kXF16, gv::kRingDepth, 2>(p, status, stream);
 }
 
 }  // namespace wq
