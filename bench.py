@@ -222,7 +222,7 @@ def run_reference(args, shapes, ws, rank):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
         "tflops": round(tfl, 9), "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "dtype": "f64", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
         "config": {"workload": WORKLOAD_NAMES[args.workload], "sampled": True},
         "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
@@ -463,7 +463,7 @@ def run_gpu(args, shapes, ws, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "tflops": round(tflops, 3),
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
         "config": {"workload": WORKLOAD_NAMES[args.workload],
                    "shapes": [f"M{p['s']['M']} K{p['s']['K']} N{p['s']['N']}" for p in probs],
                    "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB "
@@ -527,7 +527,7 @@ def run_moe(args, ws, rank, local):
             "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+            "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
             "config": {"workload": WORKLOAD_NAMES["moe"], "sampled": False},
             "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
@@ -604,7 +604,7 @@ def run_moe(args, ws, rank, local):
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in DESIGN.md)",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
         "config": {"workload": WORKLOAD_NAMES["moe"], "tokens_per_expert": [offs[e + 1] - offs[e] for e in range(E)],
                    "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
                    "graph": "one CUDA graph per weight copy holds one grouped call",
