@@ -173,6 +173,21 @@ def dist_init():
     return ws, rank, local
 
 
+def max_over_ranks(ms: float, ws: int, device) -> float:
+    """The job's time: the slowest rank's (all-reduce MAX over the process group)."""
+    if ws <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], device=device, dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(ws: int, units_per_rank_step: float, ms_per_step: float, scale: float = 1e9) -> float:
+    """Whole-job throughput: every rank processes units_per_rank_step per step (weak scaling)."""
+    return ws * units_per_rank_step / (ms_per_step * 1e-3) / scale
+
+
 # ----------------------------------------------------------------------------- oracle arm
 def oracle_sample(shapes, budget_s: float, cols: int = 2048):
     """Time the CPU oracle on column windows of every shape until budget_s has passed."""
@@ -340,16 +355,12 @@ def run_gpu(args, shapes, ws, rank, local):
     if ws > 1:
         torch.distributed.barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if ws > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
     ms_per_step = ms / args.steps
     step_wbytes = sum(weight_bytes(p["s"]) for p in probs)
     step_flops = sum(flops(p["s"]) for p in probs)
-    value = ws * step_wbytes / (ms_per_step * 1e-3) / 1e9
-    tflops = ws * step_flops / (ms_per_step * 1e-3) / 1e12
+    value = job_rate(ws, step_wbytes, ms_per_step)
+    tflops = job_rate(ws, step_flops, ms_per_step, 1e12)
 
     peaks, peaks_src = load_peaks()
     if args.quick:
@@ -538,6 +549,8 @@ def run_moe(args, ws, rank, local):
     import weight_only_int4_g128_gb300 as wq
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
     wq.load_library(build_if_missing=True)
     if not wq.device_supported(local):
         raise RuntimeError("not an sm_103 device")
@@ -570,6 +583,8 @@ def run_moe(args, ws, rank, local):
             graphs[i % reps].replay()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
     clocks.start()
     time.sleep(0.3)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -581,9 +596,11 @@ def run_moe(args, ws, rank, local):
             graphs[i % reps].replay()
         e1.record(stream)
     torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
     clk = clocks.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    value = ws * (wb + X.numel() * 2 + Y.numel() * 2) / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
+    value = job_rate(ws, wb + X.numel() * 2 + Y.numel() * 2, ms)
     peaks, src = load_peaks()
     achieved = wb / (ms * 1e-3) / 1e9
     # end to end: pinned host X in, grouped call, Y to pinned host, synchronised each step
@@ -622,6 +639,8 @@ def run_moe(args, ws, rank, local):
         gbs, el, threads, sample = moe_oracle(d, args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": sample, "seconds": round(el, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

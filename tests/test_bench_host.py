@@ -1,0 +1,58 @@
+"""Host-side logic of bench.py's multi-rank path, on CPU: two gloo ranks agree on the
+slowest rank's time, the job rate counts every rank's work, and the reference arm runs
+and prints on rank 0 only.  No GPU needed."""
+import io
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, ws: int, port: int, out):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=ws)
+    try:
+        ms = bench.max_over_ranks(10.0 + 5.0 * rank, ws, torch.device("cpu"))
+        out[rank] = ms
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    ws = 2
+    out = mp.get_context("spawn").Manager().dict()
+    mp.start_processes(_rank_main, args=(ws, _free_port(), out), nprocs=ws, start_method="spawn", join=True)
+    assert dict(out) == {0: 15.0, 1: 15.0}
+
+
+def test_job_rate_counts_every_rank():
+    one = bench.job_rate(1, 1e9, 2.0)
+    assert one == pytest.approx(500.0)
+    assert bench.job_rate(4, 1e9, 2.0) == pytest.approx(4 * one)
+    assert bench.max_over_ranks(3.5, 1, None) == 3.5
+
+
+def test_reference_arm_prints_on_rank_0_only():
+    class A:
+        steps, warmup, workload = 1, 3, "c0"
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.run_reference(A, synth.shapes("c0"), 2, 1) == 0
+    assert buf.getvalue() == ""
