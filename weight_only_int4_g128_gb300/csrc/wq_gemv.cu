@@ -57,7 +57,7 @@ constexpr int kPreWait = 3;
 struct Layout {
   int ring;    // per-warp code rings [8][depth][2][32][16 B]; reused for the partials
   int xs;      // activations [M][kbps * 128] 16-bit, 16-byte chunks swizzled, then one zero k-block
-  int asum;    // block sums [kbps][8] fp32
+  int asum;    // per (k-block, token slot): block sum and code-offset term, [kbps][2][8] fp32
   int ssc;     // scales [gseg][128] fp16
   int sdl;     // delta [gseg][128] fp32
   int red;     // split-K partials from every rank [splits][rpr][8] fp32
@@ -76,7 +76,7 @@ __host__ __device__ inline Layout layout(int M, int kbps, int splits, int gseg, 
   L.xs = off;
   off = align128(off + (M * kbps + 1) * kKBlock * 2);
   L.asum = off;
-  off = align128(off + kbps * kMT * 4);
+  off = align128(off + kbps * 2 * kMT * 4);
   L.ssc = off;
   off = align128(off + gseg * kTileN * 2);
   L.sdl = off;
@@ -127,28 +127,34 @@ __device__ __forceinline__ void mma16816(float (&d)[4], const float (&c)[4], uin
   }
 }
 
-template <int XK>
-__device__ __forceinline__ void dq_word(uint32_t w, uint32_t (&o)[4]) {
-  if (XK == kXBF16) dq8_bf16_exact(w, o);
-  else dq8_f16_exact(w, o);
-}
 
+// Sums of one 16-byte chunk (k = 8c .. 8c+7) of an activation row, split by
+// the position of k in its code word: k % 8 in {0, 1, 4, 5} (the low nibble of
+// each code byte) into lo, {2, 3, 6, 7} (the high nibble) into hi.
 template <int XK>
-__device__ __forceinline__ float sum_chunk(const uint4& v) {
+__device__ __forceinline__ void sum_chunk(const uint4& v, float& lo, float& hi) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-  float s = 0.0f;
+  float s[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (XK == kXF16) {
-      s += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu)));
-      s += __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
+      s[i] = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu))) +
+             __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
     } else {
-      s += __uint_as_float(u[i] << 16);
-      s += __uint_as_float(u[i] & 0xFFFF0000u);
+      s[i] = __uint_as_float(u[i] << 16) + __uint_as_float(u[i] & 0xFFFF0000u);
     }
   }
-  return s;
+  lo = s[0] + s[2];
+  hi = s[1] + s[3];
 }
+
+// Code pairs as MMA operands with an offset instead of (v - 8), one LOP3 each:
+// fp16 gives 1024 + v (nibble at bits 0..3 of each half) or 1024 + 16 v (bits
+// 4..7); bf16 gives 128 + v (its 7-bit mantissa cannot hold a nibble at bits
+// 4..7, so those pairs are shifted first).  All are exact.
+__device__ __forceinline__ uint32_t off_lo_f16(uint32_t w) { return lop_and_or(w, 0x000F000Fu, 0x64006400u); }
+__device__ __forceinline__ uint32_t off_hi_f16(uint32_t w) { return lop_and_or(w, 0x00F000F0u, 0x64006400u); }
+__device__ __forceinline__ uint32_t off_bf16(uint32_t w) { return lop_and_or(w, 0x000F000Fu, 0x43004300u); }
 
 // Swizzle of the activation tile: logical 16-byte chunk c of token row m is
 // stored at chunk c ^ (bit 3 of c | (m & 1) << 1).  The eight lanes of a
@@ -288,7 +294,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     const int total = M * per_tok;
     if (threadIdx.x < 16)
       *reinterpret_cast<uint4*>(xs + M * xstride + 16 * threadIdx.x) = make_uint4(0u, 0u, 0u, 0u);
-    for (int i = threadIdx.x; i < kbps * kMT; i += kThreads)
+    for (int i = threadIdx.x; i < kbps * 2 * kMT; i += kThreads)
       if (i % kMT >= M) asum[i] = 0.0f;
     const uint8_t* const xg = Xp;
     constexpr int kU = 8;  // one round trip for up to 16 k-blocks x 8 tokens x 16 chunks
@@ -316,21 +322,27 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
         const int idx0 = b + u * kThreads;
         if (idx0 >= total) break;  // uniform
         const int idx = idx0 + threadIdx.x;
-        float s = 0.0f;
+        float lo = 0.0f, hi = 0.0f;
         int m = 0, rem = 0;
         if (idx < total) {
           m = idx / per_tok;
           rem = idx - m * per_tok;
           *reinterpret_cast<uint4*>(xs + m * xstride + 16 * xswz(rem, m)) = v[u];
-          if (has_delta) s = sum_chunk<XK>(v[u]);
+          sum_chunk<XK>(v[u], lo, hi);
         }
-        if (has_delta) {
-          // the 16 chunks of one (token, k-block) are 16 consecutive lanes
-          s += __shfl_xor_sync(0xffffffffu, s, 1);
-          s += __shfl_xor_sync(0xffffffffu, s, 2);
-          s += __shfl_xor_sync(0xffffffffu, s, 4);
-          s += __shfl_xor_sync(0xffffffffu, s, 8);
-          if (idx < total && (rem & 15) == 0) asum[(rem >> 4) * kMT + m] = s;
+        // the 16 chunks of one (token, k-block) are 16 consecutive lanes
+#pragma unroll
+        for (int sh = 1; sh < 16; sh <<= 1) {
+          lo += __shfl_xor_sync(0xffffffffu, lo, sh);
+          hi += __shfl_xor_sync(0xffffffffu, hi, sh);
+        }
+        if (idx < total && (rem & 15) == 0) {
+          // block sum, and the offset the MMA's codes carry: fp16 codes are
+          // 1024 + v (lo k) or (1024 + 16 v) / 16 = 64 + v (hi k), so
+          // sum (v - 8) x = D - 1032 lo - 72 hi; bf16 codes are 128 + v
+          const int kb = rem >> 4;
+          asum[kb * 2 * kMT + m] = lo + hi;
+          asum[kb * 2 * kMT + kMT + m] = (XK == kXF16) ? fmaf(1032.0f, lo, 72.0f * hi) : 136.0f * (lo + hi);
         }
       }
     }
@@ -363,41 +375,54 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
       xr[4 * q + 2] = v.z;
       xr[4 * q + 3] = v.w;
     }
-    // Steps 0..3 (words 4t, 4t+1) and 4..7 (words 4t+2, 4t+3) accumulate into
-    // two independent chains, interleaved, and are added once per k-block.
-    uint32_t r0[2][4], r1[2][4], r2[2][4], r3[2][4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      dq_word<XK>(h ? a.z : a.x, r0[h]);  // row g, fragment k 2t..2t+1
-      dq_word<XK>(h ? c.z : c.x, r1[h]);  // row g + 8
-      dq_word<XK>(h ? a.w : a.y, r2[h]);  // row g, fragment k 2t+8..2t+9
-      dq_word<XK>(h ? c.w : c.y, r3[h]);  // row g + 8
-    }
-    // The ring slot has been read (the dequantized words exist, so both loads
-    // returned): refill it with k-block i + D.
-    asm volatile("" ::"r"(r0[0][0]), "r"(r1[0][0]), "r"(r2[1][3]), "r"(r3[1][3]) : "memory");
+    // Each step's fragments: pair p of words 4t + 2h (k 2t, 2t+1) and
+    // 4t + 2h + 1 (k 2t+8, 2t+9), rows g and g + 8, as offset codes.  fp16:
+    // steps with p even (low nibbles, 1024 + v) and p odd (high nibbles,
+    // 1024 + 16 v) accumulate into separate chains; bf16: chains by h.
+    const uint32_t wa[2][2] = {{a.x, a.y}, {a.z, a.w}};  // [h][fragment k half], row g
+    const uint32_t wc[2][2] = {{c.x, c.y}, {c.z, c.w}};  // row g + 8
+    // The ring slot has been read (the code words are in registers): refill it
+    // with k-block i + D.
+    asm volatile("" ::"r"(wa[0][0]), "r"(wa[1][1]), "r"(wc[0][0]), "r"(wc[1][1]) : "memory");
     if (i + D < nkb) issue_kb(i + D, slot);
     cp_async_commit();
     slot = (slot + 1 == D) ? 0 : slot + 1;
     float acc[2][4];
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      mma16816<XK>(acc[h], zero4, r0[h][0], r1[h][0], r2[h][0], r3[h][0], xr[8 * h], xr[8 * h + 4]);
+    for (int st = 0; st < 8; ++st) {
+      // issue order alternates the two chains: fp16 chains by p, so h outer;
+      // bf16 chains by h, so p outer
+      const int h = (XK == kXBF16) ? (st & 1) : (st >> 2);
+      const int pp = (XK == kXBF16) ? (st >> 1) : (st & 3);
+      {
+        uint32_t f[4];
 #pragma unroll
-    for (int pp = 1; pp < 4; ++pp)
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-        mma16816<XK>(acc[h], acc[h], r0[h][pp], r1[h][pp], r2[h][pp], r3[h][pp], xr[8 * h + pp], xr[8 * h + 4 + pp]);
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t w = (j & 1) ? wc[h][j >> 1] : wa[h][j >> 1];  // f0 row g, f1 row g+8, f2, f3 the k+8 half
+          if (XK == kXBF16) f[j] = off_bf16(w >> (4 * pp));
+          else f[j] = (pp & 1) ? off_hi_f16(pp >= 2 ? w >> 8 : w) : off_lo_f16(pp >= 2 ? w >> 8 : w);
+        }
+        const int ch = (XK == kXBF16) ? h : (pp & 1);
+        const bool first = (XK == kXBF16) ? (pp == 0) : (h == 0 && pp < 2);
+        if (first) mma16816<XK>(acc[ch], zero4, f[0], f[1], f[2], f[3], xr[8 * h + pp], xr[8 * h + 4 + pp]);
+        else mma16816<XK>(acc[ch], acc[ch], f[0], f[1], f[2], f[3], xr[8 * h + pp], xr[8 * h + 4 + pp]);
+      }
+    }
     const int gl = per_channel ? 0 : i;
     const float sA = __half2float(ssc[gl * kTileN + rA]);
     const float sB = __half2float(ssc[gl * kTileN + rB]);
+    // sum_k (v - 8) x for the block: the offset codes' product minus the offset term
+    const float2 ofs = *reinterpret_cast<const float2*>(asum + i * 2 * kMT + kMT + 2 * t);
     float d[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) d[e] = acc[0][e] + acc[1][e];
+    for (int e = 0; e < 4; ++e) {
+      const float o = (e & 1) ? ofs.y : ofs.x;
+      d[e] = (XK == kXBF16 ? acc[0][e] + acc[1][e] : fmaf(acc[1][e], 0.0625f, acc[0][e])) - o;
+    }
     if (has_delta) {
       const float dA = sdl[gl * kTileN + rA];
       const float dB = sdl[gl * kTileN + rB];
-      const float2 as = *reinterpret_cast<const float2*>(asum + i * kMT + 2 * t);
+      const float2 as = *reinterpret_cast<const float2*>(asum + i * 2 * kMT + 2 * t);
       tot[0] = fmaf(dA, as.x, fmaf(sA, d[0], tot[0]));
       tot[1] = fmaf(dA, as.y, fmaf(sA, d[1], tot[1]));
       tot[2] = fmaf(dB, as.x, fmaf(sB, d[2], tot[2]));
