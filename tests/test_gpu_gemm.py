@@ -492,3 +492,35 @@ def test_grouped_moe_parity(wq, E, K, N, counts, gs, adt, sym):
             Ye = wq.gemm_w4a16(X[r0:r1].contiguous(), Bp[e], S[e], None if sym else dl[e], gs)
             torch.cuda.synchronize()
             assert oracle.rel_fro(Y[r0:r1].double().cpu().numpy(), Ye.double().cpu().numpy()) <= 1e-3
+
+
+@pytest.mark.parametrize("idx", range(len(synth.shapes("c4"))))
+def test_w4a8_zero_point_and_in_call_quantization_full_size_sampled(wq, idx):
+    """The c4 shapes (M 16 / 256 / 2048, K 5120, N 17408) with zero-point weights, through
+    the in-call quantization entry, on sampled rows and column windows against the oracle;
+    the int8 codes and scales equal the stand-alone quantizer's."""
+    seed, s = synth.shapes("c4")[idx]
+    d = synth.make_inputs(seed + 900, s["M"], s["K"], s["N"])  # w4a16 recipe: scale + zero point
+    X = _cuda(d["A"])
+    Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
+    Y, xs = wq.gemm_w4a8_fp16(X, Bp, S, dl, 128)
+    torch.cuda.synchronize()
+    Xq_o, xs_o = oracle.quantize_per_token(d["A"])
+    assert np.array_equal(xs.cpu().numpy(), xs_o)
+    rows = _sample_rows(s["M"])
+    sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    for c in _sample_cols(s["N"]):
+        ref = oracle.gemm_w4a8_asym(Xq_o[rows], xs_o[rows], d["q"], sb, zb, 128, cols=c)
+        got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
+        assert oracle.rel_fro(got, ref) <= TOL_W4A8, c
+
+
+@pytest.mark.parametrize("M,K,N,gs,adt", [(3, 1024, 256, -1, "bf16"), (8, 768, 384, 128, "bf16"),
+                                          (5, 2048, 256, -1, "f16")])
+def test_decode_offset_codes_symmetric(wq, M, K, N, gs, adt):
+    """Symmetric weights (no correction) on the M <= 8 decode path: the offset the codes
+    carry is removed per block even without delta; fp16 and bf16, one group per column."""
+    d = synth.make_inputs(7300 + M + K, M, K, N, group_size=gs, a_dtype=adt)
+    Y, _ = _w4a16(wq, d, sym=True)
+    ref = _ref_w4a16(d, sym=True)
+    assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= TOL_W4A16
