@@ -1,24 +1,32 @@
 // wq_gemv.cu -- the weight-streaming decode path (M <= 8 tokens) of the W4A16
-// GEMM: the weight codes go from HBM straight into registers, are dequantized
-// there and contracted by warp-level MMAs, so no dequantized weight is ever
-// written to shared or tensor memory.
+// GEMM: each lane streams its own weight-code chunks from HBM into a per-warp
+// shared-memory ring (asynchronous copies), loads them into registers,
+// dequantizes them there and contracts them with warp-level MMAs, so no
+// dequantized weight is ever written to shared or tensor memory.
 //
 // Why not the tcgen05 pipeline here: with at most 8 tokens the MMA's N is tiny
 // and the work is the weight stream (the opening of "Marlin INT4 on Ada -- how
 // it works": with no reuse across outputs, the weight reads bound the kernel).
-// A tcgen05 MMA takes its weight operand
-// from TMEM or shared memory, so every dequantized 128 x 128 block (32 KB of
-// fp16) must first be stored there; on this part that staging, not HBM, paces a
-// per-SM pipeline at ~275 ns per 8 KB block.  A warp-level MMA takes the weight
-// fragment from registers, where the dequant leaves it.
+// A tcgen05 MMA takes its weight operand from TMEM or shared memory, so every
+// dequantized 128 x 128 block (32 KB of fp16) must first be stored there; on
+// this part that staging, not HBM, paces a per-SM pipeline at ~275 ns per 8 KB
+// block.  A warp-level MMA takes the weight fragment from registers, where the
+// dequant leaves it.
 //
 // Arithmetic (section "The core mismatch": W_sym = (q - 8) * scale, C = C_sym +
-// A_group_sum @ delta): each 128-k block is contracted with the exact integers
-// (q - 8) in fp16 / bf16 into fresh fp32 accumulators, then
-//     acc[n][m] += scale[g][n] * D_kb[n][m] + delta[g][n] * a_sum[kb][m]
-// in fp32, with a_sum the block sums of the token rows (fp32, computed while
-// the activation tile is staged).  The 8 token slots are the MMA's N = 8; slots
-// past M hold zeros.
+// A_group_sum @ delta).  The MMA operands are the codes with an exact offset,
+// one LOP3 per code pair: fp16 1024 + v for the low nibble of each code byte
+// and 1024 + 16 v for the high nibble (two accumulator chains), bf16 128 + v.
+// Per 128-k block, in fp32:
+//     D = D_lo + D_hi / 16 - (1032 * sum_lo x + 72 * sum_hi x)   (= sum (v - 8) x)
+//     acc[n][m] += scale[g][n] * D[n][m] + delta[g][n] * a_sum[kb][m]
+// (bf16: D = D_all - 136 * sum x), with the activation sums over the block's
+// low / high-nibble k formed while the activation tile is staged.  The 8 token
+// slots are the MMA's N = 8; slots past M read zeros.
+//
+// A grouped (mixture-of-experts) launch runs the same kernel over all experts:
+// blockIdx.z is the expert, whose token rows, weights, scales and delta the CTA
+// offsets to; an expert without tokens returns at once.
 //
 // Work split: one CTA per (128-row column tile, K segment); warp w owns rows
 // 16 w .. 16 w + 15 of the tile (one m16 strip) for the whole segment.  The K
