@@ -173,6 +173,39 @@ def dist_init():
     return ws, rank, local
 
 
+STEPS_PER_GRAPH = 8  # steps captured back to back in one CUDA graph (launch cost amortised)
+
+
+def build_step_graphs(torch, stream, reps: int, step_fn, steps_per_graph: int):
+    """CUDA graphs holding steps_per_graph consecutive steps each, the weight copy rotating
+    step by step (graph g runs copies g*spg .. g*spg+spg-1 mod reps), plus one single-step
+    graph per copy for a remainder.  Returns (multi, single)."""
+    multi, single = [], []
+    with torch.cuda.stream(stream):
+        for g in range(reps):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                for j in range(steps_per_graph):
+                    step_fn((g * steps_per_graph + j) % reps)
+            multi.append(gr)
+        for r in range(reps):
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=stream):
+                step_fn(r)
+            single.append(gr)
+    return multi, single
+
+
+def replay_steps(multi, single, steps: int, steps_per_graph: int):
+    """Run exactly `steps` steps: whole multi-step graphs, then single steps."""
+    full, rest = divmod(steps, steps_per_graph)
+    for i in range(full):
+        multi[i % len(multi)].replay()
+    base = full * steps_per_graph
+    for j in range(rest):
+        single[(base + j) % len(single)].replay()
+
+
 def max_over_ranks(ms: float, ws: int, device) -> float:
     """The job's time: the slowest rank's (all-reduce MAX over the process group)."""
     if ws <= 1:
@@ -320,21 +353,18 @@ def run_gpu(args, shapes, ws, rank, local):
 
     # --- one CUDA graph per weight replica: a whole step (all shapes)
     stream = torch.cuda.Stream(device=dev)
-    graphs = []
-    with torch.cuda.stream(stream):
-        for r in range(reps):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                for p in probs:
-                    call(p, r)
-            graphs.append(g)
+    def step(r):
+        for p in probs:
+            call(p, r)
+
+    spg = STEPS_PER_GRAPH
+    graphs, graphs1 = build_step_graphs(torch, stream, reps, step, spg)
     torch.cuda.synchronize()
 
     launches_per_step = sum(kernel_launches(p["s"]) for p in probs)
 
     with torch.cuda.stream(stream):
-        for i in range(args.warmup):
-            graphs[i % reps].replay()
+        replay_steps(graphs, graphs1, args.warmup, spg)
     torch.cuda.synchronize()
 
     # --- timed region
@@ -348,8 +378,7 @@ def run_gpu(args, shapes, ws, rank, local):
     ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for i in range(args.steps):
-            graphs[i % reps].replay()
+        replay_steps(graphs, graphs1, args.steps, spg)
         ev1.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -480,7 +509,7 @@ def run_gpu(args, shapes, ws, rank, local):
                    "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB "
                          f"> 3x L2); activations resident",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "graph": "one CUDA graph per weight copy holds one step",
+                   "graph": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps, the weight copy rotating step by step",
                    "launch": "programmatic dependent launch, weight prefetch enabled"},
         "roofline": roofline,
         "gpu_launches": launches_per_step * args.steps,
@@ -572,15 +601,11 @@ def run_moe(args, ws, rank, local):
         wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y)
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
-    graphs = []
+    spg = 4 * STEPS_PER_GRAPH
+    graphs, graphs1 = build_step_graphs(torch, stream, reps,
+                                        lambda r: wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y), spg)
     with torch.cuda.stream(stream):
-        for r in range(reps):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g, stream=stream):
-                wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y)
-            graphs.append(g)
-        for i in range(args.warmup):
-            graphs[i % reps].replay()
+        replay_steps(graphs, graphs1, args.warmup, spg)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     if ws > 1:
@@ -592,8 +617,7 @@ def run_moe(args, ws, rank, local):
     with torch.cuda.stream(stream):
         torch.cuda.synchronize()
         e0.record(stream)
-        for i in range(args.steps):
-            graphs[i % reps].replay()
+        replay_steps(graphs, graphs1, args.steps, spg)
         e1.record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -624,7 +648,7 @@ def run_moe(args, ws, rank, local):
         "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
         "config": {"workload": WORKLOAD_NAMES["moe"], "tokens_per_expert": [offs[e + 1] - offs[e] for e in range(E)],
                    "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
-                   "graph": "one CUDA graph per weight copy holds one grouped call",
+                   "graph": "CUDA graphs of 32 consecutive grouped calls, the weight copy rotating call by call",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
