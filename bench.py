@@ -45,6 +45,7 @@ WORKLOAD_NAMES = {
     "c3": "W4A16 asym prefill M4096 K5120 N17408 + M4096 K17408 N5120 g128 bf16",
     "c4": "W4A8 sym M{16,256,2048} K5120 N17408 g128 int8 per-token",
     "moe": "W4A16 asym grouped (mixture of experts): 16 tokens top-1 over 8 experts, K256 N7168 g128 fp16",
+    "swiglu": "W4A16 asym fused SwiGLU gate/up pair, decode M{1,4} K4096 N11008 (x2 projections) g128 fp16",
 }
 
 
@@ -670,6 +671,155 @@ def run_moe(args, ws, rank, local):
     return 0
 
 
+def swiglu_weight_bytes(d) -> int:
+    """Weight bytes of one pair call: codes, scales and delta of the gate and the up weight."""
+    K, N = d["gate"]["q"].shape
+    G = d["gate"]["scale"].shape[0]
+    return 2 * (K * N // 2 + G * N * 6)
+
+
+def swiglu_oracle(d, budget_s, cols: int = 512):
+    """The oracle on a column window of both projections, every token count, until budget_s."""
+    import oracle
+    gs = synth.SWIGLU["group_size"]
+    ws = []
+    for w in (d["gate"], d["up"]):
+        ws.append((np.ascontiguousarray(w["q"][:, :cols]), oracle.half_bits(w["scale"][:, :cols]),
+                   oracle.half_bits(w["zero"][:, :cols])))
+    K = d["gate"]["q"].shape[0]
+    G = d["gate"]["scale"].shape[0]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for A in d["A"]:
+            oracle.gemm_swiglu_pair(A.astype(np.float64), ws[0], ws[1], gs)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    wb = n * len(d["A"]) * 2 * (K * cols // 2 + G * cols * 6)
+    return wb / el / 1e9, el, threads, f"{n} pass(es) of both token counts on {cols} of {d['gate']['q'].shape[1]} columns, fp64 naive loops"
+
+
+def run_swiglu(args, ws, rank, local):
+    d = synth.swiglu_inputs()
+    name = WORKLOAD_NAMES["swiglu"]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        gbs, el, threads, sample = swiglu_oracle(d, max(2.0, min(20.0, 4.0 * args.steps)))
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+            "config": {"workload": name, "sampled": True},
+            "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return 0
+    import torch
+    import weight_only_int4_g128_gb300 as wq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wq.load_library(build_if_missing=True)
+    if not wq.device_supported(local):
+        raise RuntimeError("not an sm_103 device")
+    wq.set_weight_prefetch(True)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    gs = synth.SWIGLU["group_size"]
+    g, u = d["gate"], d["up"]
+    w0 = wq.pack_w4a16_pair(cu(g["q"]), cu(g["scale"]), cu(g["zero"]), cu(u["q"]), cu(u["scale"]), cu(u["zero"]), gs)
+    wb = swiglu_weight_bytes(d)
+    set_bytes = sum(t.numel() * t.element_size() for t in w0)
+    reps = max(1, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    W = [w0] + [tuple(t.clone() for t in w0) for _ in range(reps - 1)]
+    Xs = [cu(A) for A in d["A"]]
+    N = g["q"].shape[1]
+    Ys = [torch.empty((X.shape[0], N), dtype=torch.float16, device=dev) for X in Xs]
+    io_bytes = sum(X.numel() * 2 + Y.numel() * 2 for X, Y in zip(Xs, Ys))
+
+    def step(r):
+        for X, Y in zip(Xs, Ys):
+            wq.gemm_w4a16_swiglu(X, *W[r], gs, out=Y)
+
+    for r in range(reps):
+        step(r)
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream(device=dev)
+    graphs, graphs1 = build_step_graphs(torch, stream, reps, step, STEPS_PER_GRAPH)
+    with torch.cuda.stream(stream):
+        replay_steps(graphs, graphs1, args.warmup, STEPS_PER_GRAPH)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks.start()
+    time.sleep(0.3)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        torch.cuda.synchronize()
+        e0.record(stream)
+        replay_steps(graphs, graphs1, args.steps, STEPS_PER_GRAPH)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
+    calls = len(Xs)
+    value = job_rate(ws, calls * wb + io_bytes, ms)
+    peaks, src = load_peaks()
+    achieved = calls * wb / (ms * 1e-3) / 1e9
+    # end to end: pinned host X in, fused call, Y to pinned host, synchronised each step
+    hx = [torch.from_numpy(np.ascontiguousarray(A)).pin_memory() for A in d["A"]]
+    hy = [torch.empty(Y.shape, dtype=Y.dtype).pin_memory() for Y in Ys]
+    dx = [torch.empty_like(X) for X in Xs]
+    n_e2e = max(20, min(500, args.steps // 20))
+    with torch.cuda.stream(stream):
+        for i in range(3 + n_e2e):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            for j in range(calls):
+                dx[j].copy_(hx[j], non_blocking=True)
+                wq.gemm_w4a16_swiglu(dx[j], *W[i % reps], gs, out=Ys[j])
+                hy[j].copy_(Ys[j], non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+        "config": {"workload": name, "calls_per_step": calls, "us_per_call": round(1e3 * ms / calls, 3),
+                   "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
+                   "graph": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps, the weight copy rotating step by step",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "kernel": "wq::gemv_kernel, gate/up pair instance (SwiGLU epilogue); weight bytes of both projections",
+                     "peak_source": src},
+        "gpu_launches": args.steps * calls,
+        "clocks": clk,
+        "e2e": {"value": round(ws * calls * wb / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(h.numel() * 2 for h in hx), "d2h_bytes_per_step": sum(h.numel() * 2 for h in hy)},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, el, threads, sample = swiglu_oracle(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": sample, "seconds": round(el, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -689,6 +839,8 @@ def main():
     ws, rank, local = dist_init()
     if args.workload == "moe":
         return run_moe(args, ws, rank, local)
+    if args.workload == "swiglu":
+        return run_swiglu(args, ws, rank, local)
     shapes = synth.shapes(args.workload)
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]

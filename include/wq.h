@@ -68,6 +68,8 @@ extern "C" {
 #define WQ_VARIANT_W4A16_SYM 1  /* wq_gemm_w4a16 with delta == NULL */
 #define WQ_VARIANT_W4A8 2       /* wq_gemm_w4a8 */
 #define WQ_VARIANT_W4A8_ASYM 3  /* wq_gemm_w4a8_asym with delta (zero-point weights) */
+#define WQ_VARIANT_W4A16_SWIGLU 4      /* wq_gemm_w4a16_swiglu with delta; N = output width */
+#define WQ_VARIANT_W4A16_SWIGLU_SYM 5  /* wq_gemm_w4a16_swiglu with delta == NULL */
 
 /*
  * Load-time pack of asymmetric W4A16 weights ("Marlin INT4 on Ada", section
@@ -104,6 +106,24 @@ int wq_pack_w4a16(const uint8_t* q, const void* scale, const void* zero, uint32_
  */
 int wq_pack_w4a8(const uint8_t* q, const void* scale_signed, uint32_t* Bpacked, void* S_abs,
                  int K, int N, int group_size, void* stream);
+
+/*
+ * Load-time pack of a gate/up projection pair for the fused SwiGLU GEMM
+ * ("Marlin INT4 on Ada", section "Gaps and follow-ups": the fused SwiGLU
+ * dispatch runs mlp_gate and mlp_up in one kernel).  The two asymmetric
+ * [K][N] weights become one [K][2N] weight packed as wq_pack_w4a16 packs it,
+ * with the columns interleaved in groups of 16: combined columns 16i .. 16i+7
+ * are gate columns 8i .. 8i+7 and combined columns 16i+8 .. 16i+15 the same up
+ * columns.  S and delta follow the same column order.
+ *   q_gate, q_up           [K][N] uint8 device codes 0..15.
+ *   scale_gate, zero_gate, scale_up, zero_up   [G][N] fp16 device.
+ *   Bpacked                K*2N/8 uint32 device, output.
+ *   S, delta               [G][2N] fp16 / fp32 device, outputs.
+ * N must be a multiple of 64 (so that 2N is a multiple of 128).
+ */
+int wq_pack_w4a16_pair(const uint8_t* q_gate, const void* scale_gate, const void* zero_gate, const uint8_t* q_up,
+                       const void* scale_up, const void* zero_up, uint32_t* Bpacked, void* S, float* delta, int K,
+                       int N, int group_size, void* stream);
 
 /* Inverse of the packing: Bpacked (blocked layout) -> q [K][N] uint8 codes. */
 int wq_unpack_w4(const uint32_t* Bpacked, uint8_t* q, int K, int N, void* stream);
@@ -151,6 +171,28 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
                  void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Fused SwiGLU pair GEMM on a wq_pack_w4a16_pair weight:
+ *   Y[m][n] = silu(G[m][n]) * U[m][n],  silu(g) = g / (1 + exp(-g)),
+ * with G = X @ W_gate and U = X @ W_up the W4A16 products of wq_gemm_w4a16
+ * (zero-point correction included when delta is given; delta NULL gives the
+ * symmetric weights (q - 8) * scale).  Both products and the activation are
+ * in fp32; Y is rounded once to y_dtype.
+ *   X        [M][K] fp16/bf16 device.
+ *   Bpacked, S, delta: from wq_pack_w4a16_pair (2N columns).
+ *   Y        [M][N] device.
+ *   N        the width of each projection (a multiple of 64).
+ *   workspace  wq_workspace_size(WQ_VARIANT_W4A16_SWIGLU (delta given) or
+ *            WQ_VARIANT_W4A16_SWIGLU_SYM, M, N, K, group_size) bytes: 0 when
+ *            M <= 8 and the weight-streaming kernel takes the problem (one
+ *            launch, the activation in its epilogue); otherwise the GEMM's
+ *            scratch plus the fp32 pair product [M][2N], activated by one
+ *            elementwise launch after the GEMM.
+ */
+int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                         void* Y, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
  * Grouped (mixture-of-experts) W4A16 GEMM: the token rows of X are sorted by
  * expert, and expert e multiplies rows expert_offsets[e] .. expert_offsets[e+1]
  * by its own weights (the grouped GEMM of the SGLang W4A8 MoE article, section
@@ -172,6 +214,30 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
 int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
                           void* Y, int y_dtype, const int* expert_offsets, int experts, int N, int K,
                           int group_size, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Grouped (mixture-of-experts) W4A8 GEMM, the SGLang W4A8 MoE article's own
+ * case (section "task split": one GEMM per group): the int8 token rows of Xq
+ * are sorted by expert and expert e multiplies rows expert_offsets[e] ..
+ * expert_offsets[e+1] by its own weights,
+ *   Y[r][n] = x_scale[r] * sum_k Xq[r][k] W_e[k][n]   for r in expert e's rows,
+ * W_e either the folded symmetric weight of wq_gemm_w4a8 (delta NULL; S and
+ * Bpacked from wq_pack_w4a8) or the zero-point weight of wq_gemm_w4a8_asym
+ * (delta given; from wq_pack_w4a16).
+ *   Xq, x_scale   [M][K] int8 / [M] fp32 device, M = expert_offsets[experts].
+ *   Bpacked, S, delta: one weight per expert, stacked expert-major as in
+ *                 wq_gemm_w4a16_grouped.
+ *   expert_offsets HOST int array as in wq_gemm_w4a16_grouped.
+ *   workspace     the largest wq_workspace_size(variant, tokens of one
+ *                 expert, N, K, group_size) over the experts, variant
+ *                 WQ_VARIANT_W4A8_ASYM with delta, WQ_VARIANT_W4A8 without.
+ * One GEMM (activation pre-pass + GEMM) per expert that has tokens, all on
+ * `stream`; the workspace need of every expert is checked before anything is
+ * enqueued.  Other arguments as wq_gemm_w4a16.
+ */
+int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
+                         const float* delta, void* Y, int y_dtype, const int* expert_offsets, int experts, int N,
+                         int K, int group_size, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * W4A8 GEMM with zero-point (asymmetric) uint4 weights (HyperQwen W4A8

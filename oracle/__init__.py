@@ -320,6 +320,64 @@ def gemm_grouped_asym(A64, expert_offsets, q, scale_bits, zero_bits, group_size)
     return C
 
 
+def gemm_grouped_w4a8(Xq, x_scale, expert_offsets, q, scale_bits, zero_bits, group_size) -> np.ndarray:
+    """Mixture-of-experts W4A8 (SGLang W4A8 article, section "task split": one GEMM per group):
+    int8 rows expert_offsets[e] .. expert_offsets[e+1] of Xq, scaled per token, times expert
+    e's weight: (q[e] - 8)*scale[e] with non-negative (folded) scales when zero_bits is None,
+    else q[e]*scale[e] + zero[e].  q [E, K, N], scale/zero [E, G, N]; fp64."""
+    Xq = np.asarray(Xq)
+    xs = np.asarray(x_scale, np.float32)
+    E = len(expert_offsets) - 1
+    N = q.shape[2]
+    C = np.zeros((Xq.shape[0], N), np.float64)
+    wrong = _load().wq_o_get_mutation() == 7  # planted mistake: each segment takes the next expert
+    for e in range(E):
+        r0, r1 = int(expert_offsets[e]), int(expert_offsets[e + 1])
+        if r1 == r0:
+            continue
+        w = (e + 1) % E if wrong else e
+        if zero_bits is None:
+            C[r0:r1] = gemm_w4a8(Xq[r0:r1], xs[r0:r1], q[w], scale_bits[w], group_size)
+        else:
+            C[r0:r1] = gemm_w4a8_asym(Xq[r0:r1], xs[r0:r1], q[w], scale_bits[w], zero_bits[w], group_size)
+    return C
+
+
+def pair_interleave(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """Column order of the library's gate/up pair weight (its own layout choice): in every
+    group of 16 combined columns the first 8 are gate columns 8i .. 8i+7 and the next 8 the
+    same up columns.  gate/up [R, N] (N a multiple of 8) -> [R, 2N]."""
+    gate, up = np.asarray(gate), np.asarray(up)
+    R, N = gate.shape
+    out = np.empty((R, 2 * N), gate.dtype)
+    for i in range(N // 8):
+        out[:, 16 * i:16 * i + 8] = gate[:, 8 * i:8 * i + 8]
+        out[:, 16 * i + 8:16 * i + 16] = up[:, 8 * i:8 * i + 8]
+    return out
+
+
+def silu(x) -> np.ndarray:
+    """silu(x) = x * sigmoid(x) = x / (1 + e^-x), fp64 (e^-x = inf gives -0)."""
+    x = np.asarray(x, np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def gemm_swiglu_pair(A64, gate, up, group_size) -> np.ndarray:
+    """Fused SwiGLU pair ("Marlin INT4 on Ada", section "Gaps and follow-ups": mlp_gate and
+    mlp_up in one kernel): silu(A @ W_gate) * (A @ W_up), each product the plain W4A16 GEMM
+    (gate / up = (q, scale_bits, zero_bits); zero_bits None: (q - 8) * scale), fp64."""
+    def product(w):
+        q, sb, zb = w
+        if zb is None:
+            return gemm_asym_identity(A64, q, sb, None, group_size)
+        return gemm_asym_plain(A64, q, sb, zb, group_size)
+    G, U = product(gate), product(up)
+    if _load().wq_o_get_mutation() == 8:  # planted mistake: the activation on the up projection
+        G, U = U, G
+    return silu(G) * U
+
+
 def quantize_per_token(x_f16: np.ndarray):
     """Per-token absmax int8 quantization: returns (Xq int8 [M,K], x_scale fp32 [M])."""
     lib = _load()

@@ -121,3 +121,17 @@ def moe_inputs(seed: int = MOE["seed"], experts: int = MOE["experts"], tokens: i
     ws = [make_inputs(seed + 2 + e, 1, K, N, group_size=group_size, weights_only=True) for e in range(experts)]
     return {"offsets": offsets, "A": A, "q": np.stack([w["q"] for w in ws]),
             "scale": np.stack([w["scale"] for w in ws]), "zero": np.stack([w["zero"] for w in ws])}
+
+
+SWIGLU = dict(tokens=(1, 4), K=4096, N=11008, group_size=GROUP, seed=5100)
+
+
+def swiglu_inputs(seed: int = SWIGLU["seed"], tokens=SWIGLU["tokens"], K: int = SWIGLU["K"],
+                  N: int = SWIGLU["N"], group_size: int = SWIGLU["group_size"]):
+    """Decode-time gated MLP input projections: activations [m, K] fp16 for each token count
+    and one gate and one up weight [K, N] (make_inputs recipe, asymmetric, group 128)."""
+    A = [make_activations(seed + 1 + i, m, K) for i, m in enumerate(tokens)]
+    gate = make_inputs(seed + 10, 1, K, N, group_size=group_size, weights_only=True)
+    up = make_inputs(seed + 11, 1, K, N, group_size=group_size, weights_only=True)
+    return {"A": A, "gate": gate, "up": up}
+

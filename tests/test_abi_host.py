@@ -148,7 +148,7 @@ def test_w4a8_zero_point_entry_checks_and_workspace(lib):
         lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
     big = lib.wq_workspace_size(wq.VARIANT_W4A8_ASYM, 512, 4096, 4096, 128)
     assert big >= lib.wq_workspace_size(wq.VARIANT_W4A8, 512, 4096, 4096, 128) + (512 + 4096) * 128 * 2
-    assert lib.wq_workspace_size(4, 16, 4096, 4096, 128) == 0
+    assert lib.wq_workspace_size(6, 16, 4096, 4096, 128) == 0  # unknown variant
     f = lib.wq_gemm_w4a8_asym
     assert f(fake, fake, fake, fake, fake, fake, 0, 16, 256, 200, 128, fake, 1 << 20, None) == 2  # K % 128
     assert f(fake, fake, fake, fake, fake, fake, 0, 16, 256, 256, 64, fake, 1 << 20, None) == 2   # group
@@ -187,6 +187,43 @@ def test_grouped_entry_checks(lib):
     empty = (ctypes.c_int * 4)(0, 0, 0, 0)
     assert f(None, 0, None, None, None, None, 0, empty, 3, 256, 256, 128, None, 0, None) == 0     # no tokens
     assert f(fake, 0, P(0x10008), fake, fake, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 1
+
+
+def test_grouped_w4a8_entry_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    f = lib.wq_gemm_w4a8_grouped
+    offs = (ctypes.c_int * 4)(0, 2, 2, 5)
+    assert f(fake, fake, fake, fake, None, fake, 0, offs, 3, 256, 200, 128, None, 0, None) == 2   # K % 128
+    assert f(fake, fake, fake, fake, None, fake, 0, offs, 0, 256, 256, 128, None, 0, None) == 1   # experts
+    assert f(fake, fake, fake, fake, None, fake, 0, None, 3, 256, 256, 128, None, 0, None) == 1   # offsets
+    bad = (ctypes.c_int * 4)(0, 3, 2, 5)
+    assert f(fake, fake, fake, fake, None, fake, 0, bad, 3, 256, 256, 128, None, 0, None) == 1    # decreasing
+    empty = (ctypes.c_int * 4)(0, 0, 0, 0)
+    assert f(None, None, None, None, None, None, 0, empty, 3, 256, 256, 128, None, 0, None) == 0  # no tokens
+    assert f(fake, P(0x10002), fake, fake, None, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 1  # x_scale
+    # the workspace of the largest expert is checked before anything is enqueued
+    assert f(fake, fake, fake, fake, None, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 3
+
+
+def test_swiglu_pair_entry_checks(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)
+    pk = lib.wq_pack_w4a16_pair
+    assert pk(fake, fake, fake, fake, fake, fake, fake, fake, fake, 256, 96, 128, None) == 2    # N % 64
+    assert pk(fake, fake, fake, fake, fake, fake, fake, fake, fake, 200, 64, 128, None) == 2    # K % 128
+    assert pk(fake, fake, fake, None, fake, fake, fake, fake, fake, 256, 64, 128, None) == 1    # null
+    f = lib.wq_gemm_w4a16_swiglu
+    assert f(fake, 0, fake, fake, fake, fake, 0, 4, 96, 256, 128, None, 0, None) == 2          # N % 64
+    assert f(fake, 2, fake, fake, fake, fake, 0, 4, 64, 256, 128, None, 0, None) == 1          # x dtype
+    assert f(None, 0, None, None, None, None, 0, 0, 64, 256, 128, None, 0, None) == 0          # empty
+    assert f(P(0x10002), 0, fake, fake, fake, fake, 0, 4, 64, 256, 128, None, 0, None) == 1    # alignment
+    # beyond the weight-streaming kernel the fp32 pair product needs a workspace
+    assert f(fake, 0, fake, fake, fake, fake, 0, 40, 64, 256, 128, None, 0, None) == 3
+    ws = lib.wq_workspace_size
+    assert ws(4, 4, 64, 256, 128) == 0 and ws(5, 4, 64, 256, 128) == 0
+    assert ws(4, 40, 64, 256, 128) >= 40 * 128 * 4
+    assert ws(4, 40, 96, 256, 128) == 0  # N % 64
 
 
 def test_no_device_means_an_error_not_a_fallback(lib):

@@ -494,6 +494,54 @@ def test_grouped_moe_parity(wq, E, K, N, counts, gs, adt, sym):
             assert oracle.rel_fro(Y[r0:r1].double().cpu().numpy(), Ye.double().cpu().numpy()) <= 1e-3
 
 
+@pytest.mark.parametrize("E,K,N,counts,zero_point", [
+    (8, 256, 7168, (3, 1, 0, 4, 2, 2, 3, 1), False),   # the article's case: 16 tokens over 8 experts
+    (8, 256, 7168, (2, 2, 2, 2, 2, 2, 2, 2), True),
+    (3, 512, 384, (20, 0, 33), True),                   # large-M kernel per expert
+    (2, 1024, 256, (0, 5), False),
+])
+def test_grouped_w4a8_parity(wq, E, K, N, counts, zero_point):
+    """Mixture-of-experts W4A8 (folded symmetric or zero-point weights) against the oracle
+    within 2e-3; each expert's rows equal that expert's single-problem W4A8 call bit for bit."""
+    rng = np.random.default_rng(7100 + E + K)
+    offs = [0] + [int(v) for v in np.cumsum(counts)]
+    M = offs[-1]
+    x = rng.standard_normal((M, K)).astype(np.float16)
+    Xq_o, xs_o = oracle.quantize_per_token(x)
+    q = rng.integers(0, 16, size=(E, K, N)).astype(np.uint8)
+    s = rng.uniform(0.005, 0.02, size=(E, K // 128, N)).astype(np.float16)
+    if zero_point:
+        z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+        packs = [wq.pack_w4a16(_cuda(q[e]), _cuda(s[e]), _cuda(z[e]), 128) for e in range(E)]
+        dl = torch.stack([p_[2] for p_ in packs])
+        ref = oracle.gemm_grouped_w4a8(Xq_o, xs_o, offs, q, oracle.half_bits(s), oracle.half_bits(z), 128)
+    else:
+        s = np.where(rng.random(s.shape) < 0.5, -s, s).astype(np.float16)  # signed scales, folded at pack
+        packs = [wq.pack_w4a8(_cuda(q[e]), _cuda(s[e]), 128) for e in range(E)]
+        dl = None
+        folded = [oracle.fold(q[e], oracle.half_bits(s[e]), 128) for e in range(E)]
+        qf = np.stack([f[0] for f in folded])
+        sf = np.stack([f[1] for f in folded])
+        ref = oracle.gemm_grouped_w4a8(Xq_o, xs_o, offs, qf, sf, None, 128)
+    Bp = torch.stack([p_[0] for p_ in packs])
+    S = torch.stack([p_[1] for p_ in packs])
+    Xq, xs = _cuda(Xq_o), _cuda(xs_o)
+    Y = wq.gemm_w4a8_grouped(Xq, xs, Bp, S, dl, offs, 128)
+    torch.cuda.synchronize()
+    err = oracle.rel_fro(Y.double().cpu().numpy(), ref)
+    assert err <= TOL_W4A8, err
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        if r1 > r0:
+            Xe, xse = Xq[r0:r1].contiguous(), xs[r0:r1].contiguous()
+            if zero_point:
+                Ye = wq.gemm_w4a8_asym(Xe, xse, Bp[e], S[e], dl[e], 128)
+            else:
+                Ye = wq.gemm_w4a8(Xe, xse, Bp[e], S[e], 128)
+            torch.cuda.synchronize()
+            assert torch.equal(Y[r0:r1], Ye)
+
+
 @pytest.mark.parametrize("idx", range(len(synth.shapes("c4"))))
 def test_w4a8_zero_point_and_in_call_quantization_full_size_sampled(wq, idx):
     """The c4 shapes (M 16 / 256 / 2048, K 5120, N 17408) with zero-point weights, through
@@ -524,3 +572,80 @@ def test_decode_offset_codes_symmetric(wq, M, K, N, gs, adt):
     Y, _ = _w4a16(wq, d, sym=True)
     ref = _ref_w4a16(d, sym=True)
     assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= TOL_W4A16
+
+
+# --------------------------------------------------------------------------- SwiGLU gate/up pair
+
+def _pair_inputs(seed, M, K, N, gs=128, adt="f16", zero_point=True):
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((M, K))
+    if adt == "bf16":
+        A = oracle.double_to_bf16(a)
+        X = _cuda(A.view(np.int16)).view(torch.bfloat16)
+        A64 = oracle.bf16_to_double(A)
+    else:
+        A = a.astype(np.float16)
+        X = _cuda(A)
+        A64 = A.astype(np.float64)
+    G = K // (K if gs == -1 else gs)
+    ws = []
+    for _ in range(2):
+        q = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+        s = rng.uniform(0.005, 0.02, size=(G, N)).astype(np.float16)
+        z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+        ws.append((q, s, z))
+    return X, A64, ws
+
+
+def test_pair_pack_is_the_interleaved_pack(wq):
+    """pack_w4a16_pair: codes, scales and deltas of the gate/up pair in the interleaved
+    column order, bit for bit (unpack of the packed words, S, delta)."""
+    K, N = 256, 192
+    _, _, ((qg, sg, zg), (qu, su, zu)) = _pair_inputs(7200, 1, K, N)
+    Bp, S, dl = wq.pack_w4a16_pair(_cuda(qg), _cuda(sg), _cuda(zg), _cuda(qu), _cuda(su), _cuda(zu), 128)
+    q2 = wq.unpack_w4(Bp, K, 2 * N)
+    torch.cuda.synchronize()
+    assert np.array_equal(q2.cpu().numpy(), oracle.pair_interleave(qg, qu))
+    assert np.array_equal(oracle.half_bits(S.cpu().numpy()),
+                          oracle.pair_interleave(oracle.half_bits(sg), oracle.half_bits(su)))
+    dg = oracle.delta(oracle.half_bits(sg), oracle.half_bits(zg))
+    du = oracle.delta(oracle.half_bits(su), oracle.half_bits(zu))
+    assert np.array_equal(dl.cpu().numpy(), oracle.pair_interleave(dg, du))
+
+
+@pytest.mark.parametrize("M,K,N,gs,adt,zero_point", [
+    (1, 128, 192, 128, "f16", True),      # one k-block: no split, SwiGLU in registers
+    (3, 1024, 64, 128, "f16", True),      # one column tile, 8 K segments
+    (8, 1536, 5504, 128, "f16", True),    # 3 K segments: ownership rounded to 16 rows
+    (5, 1280, 3328, 128, "bf16", True),   # 5 K segments, the last owning no rows
+    (4, 2048, 320, -1, "f16", False),     # per-channel, symmetric
+    (12, 1024, 192, 128, "f16", True),    # M 9..16: tcgen05 decode kernel, then the activation pass
+    (40, 768, 320, 128, "bf16", True),    # large M
+])
+def test_swiglu_pair_parity(wq, M, K, N, gs, adt, zero_point):
+    """silu(X @ W_gate) * (X @ W_up) against the oracle, element by element within 2e-3."""
+    X, A64, ((qg, sg, zg), (qu, su, zu)) = _pair_inputs(7300 + M + K, M, K, N, gs, adt)
+    Bp, S, dl = wq.pack_w4a16_pair(_cuda(qg), _cuda(sg), _cuda(zg), _cuda(qu), _cuda(su), _cuda(zu), gs)
+    Y = wq.gemm_w4a16_swiglu(X, Bp, S, dl if zero_point else None, gs)
+    torch.cuda.synchronize()
+    gate = (qg, oracle.half_bits(sg), oracle.half_bits(zg) if zero_point else None)
+    up = (qu, oracle.half_bits(su), oracle.half_bits(zu) if zero_point else None)
+    ref = oracle.gemm_swiglu_pair(A64, gate, up, gs)
+    assert Y.shape == (M, N)
+    err = oracle.rel_fro(Y.double().cpu().numpy(), ref)
+    assert err <= TOL_W4A16, err
+
+
+def test_swiglu_pair_fp32_output_and_workspace_query(wq):
+    """fp32 output (no final rounding) within 1e-5 of the oracle on the fused path; the
+    workspace query is 0 for the fused path and covers the fp32 pair product otherwise."""
+    M, K, N = 2, 1024, 256
+    X, A64, ((qg, sg, zg), (qu, su, zu)) = _pair_inputs(7400, M, K, N)
+    Bp, S, dl = wq.pack_w4a16_pair(_cuda(qg), _cuda(sg), _cuda(zg), _cuda(qu), _cuda(su), _cuda(zu), 128)
+    Y = wq.gemm_w4a16_swiglu(X, Bp, S, dl, 128, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    ref = oracle.gemm_swiglu_pair(A64, (qg, oracle.half_bits(sg), oracle.half_bits(zg)),
+                                  (qu, oracle.half_bits(su), oracle.half_bits(zu)), 128)
+    assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= 1e-5
+    assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, M, N, K, 128) == 0
+    assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, 40, N, K, 128) >= 40 * 2 * N * 4

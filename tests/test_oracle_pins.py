@@ -452,6 +452,109 @@ def test_grouped_with_one_expert_is_the_plain_gemm():
     assert np.array_equal(got, oracle.gemm_asym_plain(A, q[0], sb[0], zb[0], 128))
 
 
+@pytest.mark.parametrize("zero_point", [False, True])
+def test_grouped_w4a8_equals_block_diagonal_gemm(zero_point):
+    """Grouped W4A8 (folded symmetric or zero-point weights): the int8 rows expanded
+    block-diagonally along K against the experts' weights stacked along K give the same
+    per-token-scaled product bit for bit (the zero blocks add exact zeros)."""
+    rng = _rng(52 + zero_point)
+    E, K, N, counts = 3, 256, 24, (2, 4, 0)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    M = int(offs[-1])
+    Xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    xs = rng.uniform(0.01, 0.05, size=M).astype(np.float32)
+    q = rng.integers(0, 16, size=(E, K, N)).astype(np.uint8)
+    s = rng.uniform(0.005, 0.02, size=(E, K // 128, N)).astype(np.float16)
+    z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+    sb, zb = oracle.half_bits(s), (oracle.half_bits(z) if zero_point else None)
+    Xblk = np.zeros((M, E * K), np.int8)
+    for e in range(E):
+        Xblk[offs[e]:offs[e + 1], e * K:(e + 1) * K] = Xq[offs[e]:offs[e + 1]]
+    qcat, scat = q.reshape(E * K, N), sb.reshape(-1, N)
+    if zero_point:
+        want = oracle.gemm_w4a8_asym(Xblk, xs, qcat, scat, zb.reshape(-1, N), 128)
+    else:
+        want = oracle.gemm_w4a8(Xblk, xs, qcat, scat, 128)
+    got = oracle.gemm_grouped_w4a8(Xq, xs, offs, q, sb, zb, 128)
+    assert np.array_equal(got, want)
+
+
+# --------------------------------------------------------------------------- SwiGLU gate/up pair
+
+def _pair_weights(rng, K, N, zero_point=True):
+    ws = []
+    for _ in range(2):
+        q = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+        s = rng.uniform(0.005, 0.02, size=(K // 128, N)).astype(np.float16)
+        z = (-s.astype(np.float64) * rng.uniform(6, 10, size=s.shape)).astype(np.float16)
+        ws.append((q, s, z if zero_point else None))
+    return ws
+
+
+def _weight_values(q, s, z):
+    """W[k, n] = q * s + z (or (q - 8) * s), fp64, one group of 128 along K."""
+    sr = np.repeat(s.astype(np.float64), 128, axis=0)
+    if z is None:
+        return (q.astype(np.float64) - 8.0) * sr
+    return q.astype(np.float64) * sr + np.repeat(z.astype(np.float64), 128, axis=0)
+
+
+@pytest.mark.parametrize("zero_point", [True, False])
+def test_swiglu_one_hot_rows_equal_library_sigmoid(zero_point):
+    """A row with a single 1 at k selects row k of each weight, so the pair gives
+    W_gate[k] * sigmoid(W_gate[k]) * W_up[k]; the sigmoid here is scipy's expit, not the
+    oracle's formula.  Swapping gate and up fails this (silu is not symmetric)."""
+    special = pytest.importorskip("scipy.special")
+    rng = _rng(60 + zero_point)
+    K, N = 256, 40
+    (qg, sg, zg), (qu, su, zu) = _pair_weights(rng, K, N, zero_point)
+    ks = np.array([0, 5, 127, 128, 255])
+    A = np.zeros((len(ks), K))
+    A[np.arange(len(ks)), ks] = 1.0
+    gate = (qg, oracle.half_bits(sg), None if zg is None else oracle.half_bits(zg))
+    up = (qu, oracle.half_bits(su), None if zu is None else oracle.half_bits(zu))
+    got = oracle.gemm_swiglu_pair(A, gate, up, 128)
+    Wg, Wu = _weight_values(qg, sg, zg)[ks], _weight_values(qu, su, zu)[ks]
+    want = Wg * special.expit(Wg) * Wu
+    assert np.allclose(got, want, rtol=1e-14, atol=0)
+
+
+def test_swiglu_zero_gate_and_large_gate():
+    """silu(0) = 0: a gate weight of exact zeros (q = 8, zero = -8 scale) gives Y = 0 for any
+    rows; a large positive gate (all activations 1, K = 1024, weights near +0.1) makes
+    sigmoid = 1 to fp64 precision, so Y = G * U."""
+    rng = _rng(62)
+    K, N = 1024, 24
+    A = rng.standard_normal((3, K))
+    (qg, sg, zg), up = _pair_weights(rng, K, N)
+    up = (up[0], oracle.half_bits(up[1]), oracle.half_bits(up[2]))
+    q8 = np.full((K, N), 8, np.uint8)
+    z8 = (-8.0 * sg.astype(np.float64)).astype(np.float16)  # exact: times a power of two
+    y0 = oracle.gemm_swiglu_pair(A, (q8, oracle.half_bits(sg), oracle.half_bits(z8)), up, 128)
+    assert np.all(y0 == 0.0)
+    ones = np.ones((2, K))
+    qh = np.full((K, N), 12, np.uint8)
+    sh = np.full((K // 128, N), 0.025, np.float16)
+    zh = np.zeros_like(sh)  # w = 12 * 0.025 = 0.3 each, G = 1024 * 0.3 ~ 307
+    gate = (qh, oracle.half_bits(sh), oracle.half_bits(zh))
+    G = oracle.gemm_asym_plain(ones, qh, oracle.half_bits(sh), oracle.half_bits(zh), 128)
+    U = oracle.gemm_asym_plain(ones, up[0], up[1], up[2], 128)
+    assert np.array_equal(oracle.gemm_swiglu_pair(ones, gate, up, 128), G * U)
+
+
+def test_pair_interleave_is_a_paired_permutation():
+    """The pair layout holds every gate and every up column exactly once, and gate column j
+    sits 8 columns before up column j inside one 16-column group."""
+    N = 64
+    gate = np.arange(N)[None, :]
+    up = 1000 + np.arange(N)[None, :]
+    c = oracle.pair_interleave(gate, up)[0]
+    assert sorted(c.tolist()) == list(range(N)) + list(range(1000, 1000 + N))
+    pos = {v: i for i, v in enumerate(c.tolist())}
+    for j in range(N):
+        assert pos[1000 + j] == pos[j] + 8 and pos[j] // 16 == pos[1000 + j] // 16
+
+
 # --------------------------------------------------------------------------- pin sensitivity
 
 def _pins_pass():
@@ -464,16 +567,19 @@ def _pins_pass():
         test_zero_weights_give_zero()
         test_w4a8_asym_integer_closed_form()
         test_grouped_equals_block_diagonal_gemm()
+        test_grouped_w4a8_equals_block_diagonal_gemm(True)
+        test_swiglu_one_hot_rows_equal_library_sigmoid(True)
     except AssertionError:
         return False
     return True
 
 
-@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("mid", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_planted_mistakes_are_caught(mid):
     """A plausible mistake planted in the oracle (wrong delta sign, wrong clamp, wrong
     offset, dropped correction, dropped activation scale, dropped W4A8 zero point, rows
-    multiplied by the wrong expert) fails at least one pin."""
+    multiplied by the wrong expert, the SwiGLU activation on the up projection) fails at
+    least one pin."""
     assert _pins_pass()
     with oracle.mutation(mid):
         assert not _pins_pass()

@@ -23,15 +23,17 @@ from . import build as _build
 __all__ = [
     "WQError", "load_library", "library_path", "pack_w4a16", "pack_w4a8", "unpack_w4",
     "dequant_w4", "quantize_per_token", "gemm_w4a16", "gemm_w4a16_host", "gemm_w4a8", "gemm_w4a8_asym",
-    "gemm_w4a8_fp16", "gemm_w4a16_grouped", "workspace_size",
+    "gemm_w4a8_fp16", "gemm_w4a16_grouped", "gemm_w4a8_grouped", "pack_w4a16_pair", "gemm_w4a16_swiglu", "workspace_size",
     "device_supported", "device_status", "debug_wait_probe", "version", "Workspace",
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
-    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "set_weight_prefetch",
+    "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "VARIANT_W4A16_SWIGLU",
+    "VARIANT_W4A16_SWIGLU_SYM", "set_weight_prefetch",
     "OPTION_WEIGHT_PREFETCH",
 ]
 
 DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
 VARIANT_W4A16, VARIANT_W4A16_SYM, VARIANT_W4A8, VARIANT_W4A8_ASYM = 0, 1, 2, 3
+VARIANT_W4A16_SWIGLU, VARIANT_W4A16_SWIGLU_SYM = 4, 5
 ERRORS = {1: "WQ_ERR_INVALID_ARG", 2: "WQ_ERR_UNSUPPORTED_SHAPE", 3: "WQ_ERR_WORKSPACE",
           4: "WQ_ERR_ARCH", 5: "WQ_ERR_CUDA", 6: "WQ_ERR_TIMEOUT"}
 
@@ -47,6 +49,9 @@ EXPORTS = {
     "wq_gemm_w4a8_asym": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a8_fp16": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_gemm_w4a16_grouped": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_gemm_w4a8_grouped": (_I, [_P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _P, _SZ, _P]),
+    "wq_pack_w4a16_pair": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
+    "wq_gemm_w4a16_swiglu": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_quantize_per_token": (_I, [_P, _P, _P, _I, _I, _P]),
     "wq_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "wq_device_supported": (_I, [_I]),
@@ -163,6 +168,25 @@ def pack_w4a16(q, scale, zero, group_size: int = 128):
     return Bp, S, d
 
 
+def pack_w4a16_pair(q_gate, scale_gate, zero_gate, q_up, scale_up, zero_up, group_size: int = 128):
+    """Gate/up projection pair ([K,N] codes, [G,N] fp16 scales and zeros each) -> the
+    (Bpacked, S, delta) of one [K,2N] weight with the columns interleaved in groups of 16
+    (8 gate columns, then the same 8 up columns), for gemm_w4a16_swiglu."""
+    torch = _torch()
+    _require_cuda(q_gate, scale_gate, zero_gate, q_up, scale_up, zero_up)
+    K, N = q_gate.shape
+    if tuple(q_up.shape) != (K, N):
+        raise ValueError("gate and up codes must have the same shape")
+    G = K // _gs(K, group_size)
+    Bp = torch.empty((2 * N // 128, K // 128, 128, 16), dtype=torch.int32, device=q_gate.device)
+    S = torch.empty((G, 2 * N), dtype=torch.float16, device=q_gate.device)
+    d = torch.empty((G, 2 * N), dtype=torch.float32, device=q_gate.device)
+    _check(load_library().wq_pack_w4a16_pair(_ptr(q_gate), _ptr(scale_gate), _ptr(zero_gate), _ptr(q_up),
+                                             _ptr(scale_up), _ptr(zero_up), _ptr(Bp), _ptr(S), _ptr(d), K, N,
+                                             group_size, _stream()), "wq_pack_w4a16_pair")
+    return Bp, S, d
+
+
 def pack_w4a8(q, scale_signed, group_size: int = 128):
     """q [K,N] uint4b8 codes, signed scale [G,N] fp16 -> (Bpacked, S_abs) with the sign fold."""
     torch = _torch()
@@ -272,6 +296,25 @@ def gemm_w4a16(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=
     variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
     lib = _lib or load_library()
     _call_gemm(lib.wq_gemm_w4a16, "wq_gemm_w4a16",
+               (X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
+                delta.data_ptr() if delta is not None else None, Y.data_ptr(), _dtype_code(Y.dtype),
+                M, N, K, group_size), (), workspace, variant, M, N, K, group_size, X.device,
+               _raw_stream(X.device.index))
+    return Y
+
+
+def gemm_w4a16_swiglu(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=None,
+                      workspace=None):
+    """Y = silu(X @ W_gate) * (X @ W_up) on a pack_w4a16_pair weight (delta None: symmetric).
+    X [M,K] fp16/bf16; Y [M,N] with N half the pair weight's columns."""
+    torch = _torch()
+    _require_cuda(X, Bpacked, S, delta, out)
+    M, K = X.shape
+    N = Bpacked.numel() * 8 // K // 2
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=X.device)
+    variant = VARIANT_W4A16_SWIGLU if delta is not None else VARIANT_W4A16_SWIGLU_SYM
+    lib = _lib or load_library()
+    _call_gemm(lib.wq_gemm_w4a16_swiglu, "wq_gemm_w4a16_swiglu",
                (X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
                 delta.data_ptr() if delta is not None else None, Y.data_ptr(), _dtype_code(Y.dtype),
                 M, N, K, group_size), (), workspace, variant, M, N, K, group_size, X.device,
@@ -394,6 +437,37 @@ def gemm_w4a16_grouped(X, Bpacked, S, delta, expert_offsets, group_size: int = 1
                                    workspace.numel() if workspace is not None else 0, stream)
     if rc != 0:
         raise WQError(rc, "wq_gemm_w4a16_grouped", lib.wq_last_error().decode())
+    return Y
+
+
+def gemm_w4a8_grouped(Xq, x_scale, Bpacked, S, delta, expert_offsets, group_size: int = 128, out_dtype=None,
+                      out=None, workspace=None):
+    """Mixture-of-experts W4A8: int8 rows expert_offsets[e] .. expert_offsets[e+1] of Xq (sorted
+    by expert, per-token scales x_scale) times expert e's weights: stacked pack_w4a8 outputs
+    (delta None) or stacked pack_w4a16 outputs (zero-point weights, delta [E, G, N])."""
+    torch = _torch()
+    _require_cuda(Xq, x_scale, Bpacked, S, delta, out)
+    M, K = Xq.shape
+    E = int(S.shape[0])
+    N = int(S.shape[-1])
+    offs = (ctypes.c_int * (E + 1))(*[int(v) for v in expert_offsets])
+    if len(expert_offsets) != E + 1 or offs[E] != M:
+        raise ValueError("expert_offsets must have experts + 1 entries ending at Xq.shape[0]")
+    Y = out if out is not None else torch.empty((M, N), dtype=out_dtype or torch.float16, device=Xq.device)
+    lib = _lib or load_library()
+    stream = _raw_stream(Xq.device.index)
+    if workspace is None:
+        max_m = max((offs[e + 1] - offs[e] for e in range(E)), default=0)
+        variant = VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8
+        need = workspace_size(variant, max_m, N, K, group_size) if max_m > 0 else 0
+        workspace = _stream_workspace(Xq.device, stream).get(need) if need > 0 else None
+    rc = lib.wq_gemm_w4a8_grouped(Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S.data_ptr(),
+                                  delta.data_ptr() if delta is not None else None, Y.data_ptr(),
+                                  _dtype_code(Y.dtype), offs, E, N, K, group_size,
+                                  workspace.data_ptr() if workspace is not None else None,
+                                  workspace.numel() if workspace is not None else 0, stream)
+    if rc != 0:
+        raise WQError(rc, "wq_gemm_w4a8_grouped", lib.wq_last_error().decode())
     return Y
 
 

@@ -219,6 +219,32 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   return p;
 }
 
+// One launch of the weight-streaming decode kernel (M <= 8) on a plan from
+// gemv_plan; pair: N columns of a gate/up pair weight, Y [M][N/2] = silu(gate) * up.
+int launch_gemv_call(const void* X, int x_kind, const uint32_t* Bpacked, const void* S, const float* delta, void* Y,
+                     int y_kind, int M, int N, int K, int gs, int splits, int kbps, bool pair, cudaStream_t st,
+                     const char* name) {
+  wq::GemmParams p{};
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.group_size = gs;
+  p.G = K / gs;
+  p.kb_total = K / 128;
+  p.kb_per_split = kbps;
+  p.splits = splits;
+  p.X = X;
+  p.B = Bpacked;
+  p.S = static_cast<const __half*>(S);
+  p.delta = delta;
+  p.Y = Y;
+  p.y_kind = y_kind;
+  p.timeout_ns = timeout_ns();
+  p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+  p.swiglu = pair ? 1 : 0;
+  return after_launch(wq::launch_gemv(x_kind, p, st), name, st);
+}
+
 // ---------------------------------------------------------------- GEMM core
 // quant_in (W4A8 variants only): X is fp16 [M][K], quantized per token by the
 // activation pre-pass, which also writes x_scale (then an output).
@@ -241,27 +267,9 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     // takes every problem whose segment fits its shared memory; 9..16 tokens,
     // where the MMA work doubles, and the rest go to the tcgen05 decode kernel.
     int gv_splits = 0, gv_kbps = 0;
-    if (wq::gemv_plan(M, N, K, gs, delta != nullptr, &gv_splits, &gv_kbps)) {
-      wq::GemmParams p{};
-      p.M = M;
-      p.N = N;
-      p.K = K;
-      p.group_size = gs;
-      p.G = G;
-      p.kb_total = K / 128;
-      p.kb_per_split = gv_kbps;
-      p.splits = gv_splits;
-      p.X = X;
-      p.B = Bpacked;
-      p.S = static_cast<const __half*>(S);
-      p.delta = delta;
-      p.Y = Y;
-      p.y_kind = y_kind;
-      p.timeout_ns = timeout_ns();
-      p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
-      e = wq::launch_gemv(x_kind, p, st);
-      return after_launch(e, name, st);
-    }
+    if (wq::gemv_plan(M, N, K, gs, delta != nullptr, &gv_splits, &gv_kbps))
+      return launch_gemv_call(X, x_kind, Bpacked, S, delta, Y, y_kind, M, N, K, gs, gv_splits, gv_kbps, false, st,
+                              name);
     CUtensorMap tm_x, tm_s, tm_d;
     const CUtensorMapDataType xdt =
         x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -452,12 +460,90 @@ int wq_get_option(int option, long long* value) {
 
 const char* wq_version(void) { return "wq 0.1.0 (sm_103a, tcgen05)"; }
 
+// Gate/up pair GEMM, output width N (the pair weight has 2N columns): the
+// weight-streaming kernel with the SwiGLU epilogue when it takes the problem
+// (no workspace); else the GEMM's own scratch, then the fp32 product [M][2N].
+struct SwigluPlan {
+  bool fused;
+  int splits, kbps;
+  size_t off_prod, bytes;
+};
+
+SwigluPlan make_swiglu_plan(int M, int N, int K, int gs, bool has_delta) {
+  SwigluPlan sp{};
+  const int Nc = 2 * N;
+  sp.fused = wq::gemv_plan(M, Nc, K, gs, has_delta, &sp.splits, &sp.kbps, true) != 0;
+  if (sp.fused) return sp;
+  const int variant = has_delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
+  sp.off_prod = align256(make_plan(variant, M, Nc, K, gs).bytes);
+  sp.bytes = sp.off_prod + static_cast<size_t>(M) * Nc * 4;
+  return sp;
+}
+
 size_t wq_workspace_size(int variant, int M, int N, int K, int group_size) {
-  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
+  const bool pair = variant == WQ_VARIANT_W4A16_SWIGLU || variant == WQ_VARIANT_W4A16_SWIGLU_SYM;
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % (pair ? 64 : 128)) return 0;
   int gs = (group_size == -1) ? K : group_size;
   if (gs != 128 && gs != K) return 0;
+  if (pair) return make_swiglu_plan(M, N, K, gs, variant == WQ_VARIANT_W4A16_SWIGLU).bytes;
   if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8_ASYM) return 0;
   return make_plan(variant, M, N, K, gs).bytes;
+}
+
+int wq_pack_w4a16_pair(const uint8_t* q_gate, const void* scale_gate, const void* zero_gate, const uint8_t* q_up,
+                       const void* scale_up, const void* zero_up, uint32_t* Bpacked, void* S, float* delta, int K,
+                       int N, int group_size, void* stream) {
+  if (N <= 0 || N % 64) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_pack_w4a16_pair: N=%d (a multiple of 64)", N);
+  int rc = check_kn(K, 2 * N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (!q_gate || !scale_gate || !zero_gate || !q_up || !scale_up || !zero_up || !Bpacked || !S || !delta)
+    return fail(WQ_ERR_INVALID_ARG, "wq_pack_w4a16_pair: null pointer");
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = wq::launch_pack_pair(q_gate, static_cast<const __half*>(scale_gate),
+                                       static_cast<const __half*>(zero_gate), q_up,
+                                       static_cast<const __half*>(scale_up), static_cast<const __half*>(zero_up),
+                                       Bpacked, static_cast<__half*>(S), delta, K, N, gs, st);
+  return after_launch(e, "wq_pack_w4a16_pair", st);
+}
+
+int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
+                         void* Y, int y_dtype, int M, int N, int K, int group_size, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (M < 0) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a16_swiglu: M=%d", M);
+  if (N <= 0 || N % 64) return fail(WQ_ERR_UNSUPPORTED_SHAPE, "wq_gemm_w4a16_swiglu: N=%d (a multiple of 64)", N);
+  int rc = check_kn(K, 2 * N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  if (x_dtype != WQ_DTYPE_F16 && x_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: x_dtype must be F16 or BF16");
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: bad y_dtype %d", y_dtype);
+  if (M == 0) return WQ_OK;
+  if (!X || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: null pointer");
+  if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S) || (delta && !aligned16(delta)))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: X, Bpacked, S, delta and Y must be 16-byte aligned");
+  const SwigluPlan sp = make_swiglu_plan(M, N, K, gs, delta != nullptr);
+  if (sp.bytes > 0 && (!workspace || workspace_bytes < sp.bytes))
+    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a16_swiglu: workspace of %zu bytes given, %zu needed", workspace_bytes,
+                sp.bytes);
+  if (workspace && !aligned16(workspace))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: workspace must be 16-byte aligned");
+  if ((rc = check_device())) return rc;
+  const int xk = x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (sp.fused)
+    return launch_gemv_call(X, xk, Bpacked, S, delta, Y, yk, M, 2 * N, K, gs, sp.splits, sp.kbps, true, st,
+                            "wq_gemm_w4a16_swiglu");
+  // the pair product in fp32, then the activation in one elementwise pass
+  float* prod = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + sp.off_prod);
+  rc = gemm_core(X, xk, Bpacked, S, delta, nullptr, prod, wq::kYF32, M, 2 * N, K, gs,
+                 delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM, workspace, sp.off_prod, st, "wq_gemm_w4a16_swiglu");
+  if (rc) return rc;
+  return after_launch(wq::launch_swiglu_pairs(prod, Y, yk, M, N, st), "wq_gemm_w4a16_swiglu", st);
 }
 
 int wq_pack_w4a16(const uint8_t* q, const void* scale, const void* zero, uint32_t* Bpacked, void* S,
@@ -701,6 +787,59 @@ int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, c
                    static_cast<const __half*>(S) + e * sd_stride, delta ? delta + e * sd_stride : nullptr, nullptr,
                    static_cast<uint8_t*>(Y) + static_cast<size_t>(r0) * N * ysz, yk, me, N, K, gs, variant, workspace,
                    workspace_bytes, st, "wq_gemm_w4a16_grouped");
+    if (rc) return rc;
+  }
+  return WQ_OK;
+}
+
+int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
+                         const float* delta, void* Y, int y_dtype, const int* expert_offsets, int experts, int N,
+                         int K, int group_size, void* workspace, size_t workspace_bytes, void* stream) {
+  int rc = check_kn(K, N);
+  if (rc) return rc;
+  int gs;
+  if ((rc = norm_group(K, group_size, &gs))) return rc;
+  const int yk = y_kind_of(y_dtype);
+  if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: bad y_dtype %d", y_dtype);
+  if (experts < 1 || experts > wq::kMaxExperts)
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: experts=%d (1..%d)", experts, wq::kMaxExperts);
+  if (!expert_offsets) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: null expert_offsets");
+  if (expert_offsets[0] != 0) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: expert_offsets[0] != 0");
+  for (int e = 0; e < experts; ++e)
+    if (expert_offsets[e + 1] < expert_offsets[e])
+      return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: expert_offsets decrease at %d", e);
+  if (expert_offsets[experts] == 0) return WQ_OK;
+  if (!Xq || !x_scale || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: null pointer");
+  if (!aligned16(Xq) || !aligned16(Bpacked) || !aligned16(S) || !aligned16(Y) || (delta && !aligned16(delta)) ||
+      (reinterpret_cast<uintptr_t>(x_scale) & 3u))
+    return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: Xq, Bpacked, S, delta and Y must be 16-byte aligned, "
+                                    "x_scale 4-byte aligned");
+  const int variant = delta ? WQ_VARIANT_W4A8_ASYM : WQ_VARIANT_W4A8;
+  const long long b_stride = static_cast<long long>(K) * N / 8;
+  const long long sd_stride = static_cast<long long>(K / gs) * N;
+  const size_t ysz = (yk == wq::kYF32) ? 4 : 2;
+  // every expert's workspace need is checked before anything is enqueued
+  size_t need = 0;
+  for (int e = 0; e < experts; ++e) {
+    const int me = expert_offsets[e + 1] - expert_offsets[e];
+    if (me > 0) {
+      const size_t b = make_plan(variant, me, N, K, gs).bytes;
+      need = b > need ? b : need;
+    }
+  }
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a8_grouped: workspace of %zu bytes given, %zu needed", workspace_bytes,
+                need);
+  if ((rc = check_device())) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int e = 0; e < experts; ++e) {
+    const int r0 = expert_offsets[e];
+    const int me = expert_offsets[e + 1] - r0;
+    if (me == 0) continue;
+    rc = gemm_core(Xq + static_cast<size_t>(r0) * K, wq::kXF16, Bpacked + e * b_stride,
+                   static_cast<const __half*>(S) + e * sd_stride, delta ? delta + e * sd_stride : nullptr,
+                   x_scale + r0, static_cast<uint8_t*>(Y) + static_cast<size_t>(r0) * N * ysz, yk, me, N, K, gs,
+                   variant, workspace, workspace_bytes, st, "wq_gemm_w4a8_grouped");
     if (rc) return rc;
   }
   return WQ_OK;

@@ -446,4 +446,13 @@ __device__ __forceinline__ void store_y_any(void* Y, int yk, size_t idx, float v
   }
 }
 
+// SwiGLU activation of a gate/up pair in fp32: silu(g) * u, silu(g) = g / (1 + e^-g)
+// (a very negative g gives e^-g = inf and silu = -0).
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Gate/up pair interleave of the combined weight: in every 16-column group the
+// first 8 columns are gate columns and the next 8 the same up columns, so
+// combined column c holds projection column 8 * (c / 16) + c % 8.
+__host__ __device__ __forceinline__ int pair_source_col(int c) { return 8 * (c >> 4) + (c & 7); }
+
 }  // namespace wq

@@ -75,9 +75,18 @@ struct Layout {
 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 
-__host__ __device__ inline Layout layout(int M, int kbps, int splits, int gseg, bool has_delta, int depth) {
-  Layout L;
+// Weight rows of a column tile whose split-K reduction rank r owns: rows
+// [r * rpr, (r + 1) * rpr).  A gate/up pair rounds rpr up to 16 rows so that the
+// gate row and its up row 8 rows further on always fall to the same owner.
+__host__ __device__ inline int reduce_rows(int splits, bool pair) {
   const int rpr = (kTileN + splits - 1) / splits;
+  return pair ? (rpr + 15) & ~15 : rpr;
+}
+
+__host__ __device__ inline Layout layout(int M, int kbps, int splits, int gseg, bool has_delta, int depth,
+                                         bool pair) {
+  Layout L;
+  const int rpr = reduce_rows(splits, pair);
   int off = 0;
   L.ring = off;
   off = align128(off + kWarps * depth * kRingSlot);  // >= the partials [128][8] fp32
@@ -173,7 +182,7 @@ __device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) |
 // MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
 // wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
 // per column tile and expert) then fit in one wave.
-template <int XK, int D, int MINB>
+template <int XK, int D, int MINB, bool PAIR>
 __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmParams p, unsigned* status) {
   using namespace gv;
   extern __shared__ uint8_t smem_raw[];
@@ -216,8 +225,9 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
   const bool per_channel = p.G == 1;  // one group spans the whole K
   const int g0 = per_channel ? 0 : kb0;
   const int gseg = per_channel ? 1 : nkb;
-  const Layout L = layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, D);
-  const int rpr = (kTileN + splits - 1) / splits;
+  const Layout L = layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, D, PAIR);
+  constexpr bool pair = PAIR;  // gate/up pair weight, SwiGLU epilogue
+  const int rpr = reduce_rows(splits, pair);
   const int own_rows = max(0, min(kTileN - seg * rpr, rpr));
 
   uint8_t* const xs = sm + L.xs;
@@ -459,6 +469,16 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     __syncthreads();
   }
   if (splits == 1) {
+    if (pair) {
+      // row rA is a gate column and rB = rA + 8 the up column of the same output
+      const int j = ((n0 + 16 * warp) >> 1) + g;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tok = 2 * t + e;
+        if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * (N >> 1) + j, silu_mul(tot[e], tot[2 + e]));
+      }
+      return;
+    }
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int tok = 2 * t + (e & 1);
@@ -495,6 +515,22 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     const WaitCtx wred{&never, p.timeout_ns, kDevTimeoutFixup, status};
     mbar_wait(red_full, 0, wred);
   }
+  if (pair) {
+    // own_rows is a multiple of 16: pairs (16 * (i / 8) + i % 8, that row + 8)
+    const int npair = own_rows >> 1;
+    for (int i = threadIdx.x; i < npair * M; i += kThreads) {
+      const int m = i / npair;
+      const int pi = i - m * npair;
+      const int lr = 16 * (pi >> 3) + (pi & 7);
+      float gs = 0.0f, us = 0.0f;
+      for (int src = 0; src < splits; ++src) {
+        gs += red[(src * rpr + lr) * kMT + m];
+        us += red[(src * rpr + lr + 8) * kMT + m];
+      }
+      store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * (N >> 1) + ((n0 + seg * rpr) >> 1) + pi, silu_mul(gs, us));
+    }
+    return;
+  }
   for (int i = threadIdx.x; i < total; i += kThreads) {
     const int m = i / own_rows;
     const int lr = i - m * own_rows;
@@ -509,7 +545,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
 // wave of two CTAs per SM, so that every SM streams with 16 warps.  Returns 0
 // when the problem is not for this path (M > 8) or no split fits the shared
 // memory limit.
-int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_out, int* kbps_out) {
+int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_out, int* kbps_out, bool pair) {
   if (M < 1 || M > gv::kMaxM) return 0;
   const int kb = K / kKBlock;
   const int tiles = N / kTileN;
@@ -518,7 +554,7 @@ int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_o
     const int kbps = (kb + s - 1) / s;
     const int sp = (kb + kbps - 1) / kbps;
     const int gseg = (group_size == K) ? 1 : kbps;
-    if (gv::layout(M, kbps, sp, gseg, has_delta, gv::kRingDepth).bytes > gv::kMaxSmem) continue;
+    if (gv::layout(M, kbps, sp, gseg, has_delta, gv::kRingDepth, pair).bytes > gv::kMaxSmem) continue;
     if (best < 0 || tiles * sp <= 2 * kNumSMs) best = sp;
   }
   if (best < 0) return 0;
@@ -528,12 +564,12 @@ int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits_o
 }
 
 // Whether a launch with these segments fits the shared memory limit.
-bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta) {
+bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta, bool pair) {
   return M >= 1 && M <= gv::kMaxM &&
-         gv::layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, gv::kRingDepth).bytes <= gv::kMaxSmem;
+         gv::layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, gv::kRingDepth, pair).bytes <= gv::kMaxSmem;
 }
 
-template <int XK, int D, int MINB>
+template <int XK, int D, int MINB, bool PAIR>
 static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   int dev = 0;
@@ -541,12 +577,12 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_mask & bit)) {
-    e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
+    e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
     if (e != cudaSuccess) return e;
     attr_mask |= bit;
   }
   const int gseg = (p.G == 1) ? 1 : p.kb_per_split;
-  const gv::Layout L = gv::layout(p.M, p.kb_per_split, p.splits, gseg, p.delta != nullptr, D);
+  const gv::Layout L = gv::layout(p.M, p.kb_per_split, p.splits, gseg, p.delta != nullptr, D, PAIR);
   if (L.bytes > gv::kMaxSmem) return cudaErrorInvalidValue;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, p.splits, p.experts > 0 ? p.experts : 1);
@@ -562,7 +598,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D, MINB>, p, status);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D, MINB, PAIR>, p, status);
 }
 
 cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
@@ -573,11 +609,16 @@ cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
       p.kb_per_split < 1 || (p.splits - 1) * p.kb_per_split >= p.kb_total)
     return cudaErrorInvalidValue;
   if (p.experts > 0) {
-    if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 3>(p, status, stream);
-    return launch_gemv_t<kXF16, gv::kRingDepth, 3>(p, status, stream);
+    if (p.swiglu) return cudaErrorInvalidValue;
+    if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 3, false>(p, status, stream);
+    return launch_gemv_t<kXF16, gv::kRingDepth, 3, false>(p, status, stream);
   }
-  if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 2>(p, status, stream);
-  return launch_gemv_t<kXF16, gv::kRingDepth, 2>(p, status, stream);
+  if (p.swiglu) {
+    if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 2, true>(p, status, stream);
+    return launch_gemv_t<kXF16, gv::kRingDepth, 2, true>(p, status, stream);
+  }
+  if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 2, false>(p, status, stream);
+  return launch_gemv_t<kXF16, gv::kRingDepth, 2, false>(p, status, stream);
 }
 
 }  // namespace wq

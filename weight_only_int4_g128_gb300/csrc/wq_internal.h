@@ -54,6 +54,10 @@ struct GemmParams {
   int experts;
   long long b_stride, sd_stride;
   int goff[kMaxExperts + 1];
+  // Gate/up pair (weight-streaming decode kernel): the N columns are the
+  // pair-interleaved gate and up projections (each 16-column group: 8 gate
+  // columns, then the same 8 up columns) and Y is [M][N/2] = silu(gate) * up.
+  int swiglu;
 };
 
 // Record the message for wq_last_error() on this thread and return `code`.
@@ -72,8 +76,10 @@ cudaError_t launch_decode16(int x_kind, const CUtensorMap& tm_x, const CUtensorM
                             const GemmParams& p, cudaStream_t stream);
 int decode16_max_splits();
 cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream);
-int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits, int* kb_per_split);
-bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta);
+// pair: a gate/up pair weight (SwiGLU epilogue), whose split-K ownership is rounded to 16 rows
+int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits, int* kb_per_split,
+              bool pair = false);
+bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta, bool pair = false);
 int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
@@ -84,6 +90,10 @@ size_t gemm_smem_bytes(int bt);
 cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int M, int K, int N, int group_size,
                              int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, cudaStream_t stream);
 cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t stream);
+cudaError_t launch_pack_pair(const uint8_t* q_gate, const __half* scale_gate, const __half* zero_gate,
+                             const uint8_t* q_up, const __half* scale_up, const __half* zero_up, uint32_t* Bpacked,
+                             __half* S, float* delta, int K, int N, int group_size, cudaStream_t stream);
+cudaError_t launch_swiglu_pairs(const float* Yc, void* Y, int y_kind, int M, int N, cudaStream_t stream);
 cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zero, int fold,
                         uint32_t* Bpacked, __half* S, float* delta, int K, int N, int group_size,
                         cudaStream_t stream);

@@ -74,6 +74,51 @@ __global__ void pack_scales_kernel(const __half* __restrict__ scale, const __hal
   if (delta) delta[i] = __fmaf_rn(8.0f, __half2float(s), __half2float(zero[i]));
 }
 
+// Gate/up pair pack (the fused SwiGLU pair of "Marlin INT4 on Ada", section
+// "Gaps and follow-ups": mlp_gate and mlp_up in one kernel): the two [K][N]
+// projections become one [K][2N] weight whose 16-column groups hold 8 gate
+// columns and then the same 8 up columns (pair_source_col), packed in the
+// layout above, with its scales and deltas in the same column order.
+__global__ void pack_pair_kernel(const uint8_t* __restrict__ q_gate, const uint8_t* __restrict__ q_up,
+                                 uint32_t* __restrict__ Bpacked, int K, int N) {
+  const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (idx >= static_cast<long long>(K / 8) * 2 * N) return;
+  int n, w;
+  word_coords(idx, K, n, w);
+  const uint8_t* src = (n & 8) ? q_up : q_gate;
+  const int j = pair_source_col(n);
+  uint32_t word = 0;
+#pragma unroll
+  for (int jj = 0; jj < 8; ++jj) word |= (src[static_cast<size_t>(8 * w + jj) * N + j] & 0xFu) << code_shift(jj);
+  Bpacked[idx] = word;
+}
+
+__global__ void pack_pair_scales_kernel(const __half* __restrict__ scale_gate, const __half* __restrict__ zero_gate,
+                                        const __half* __restrict__ scale_up, const __half* __restrict__ zero_up,
+                                        __half* __restrict__ S, float* __restrict__ delta, int G, int N) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= static_cast<long long>(G) * 2 * N) return;
+  const int g = static_cast<int>(i / (2 * N));
+  const int c = static_cast<int>(i - static_cast<long long>(g) * 2 * N);
+  const size_t si = static_cast<size_t>(g) * N + pair_source_col(c);
+  const __half s = (c & 8) ? scale_up[si] : scale_gate[si];
+  const __half z = (c & 8) ? zero_up[si] : zero_gate[si];
+  S[i] = s;
+  delta[i] = __fmaf_rn(8.0f, __half2float(s), __half2float(z));
+}
+
+// Y[m][j] = silu(gate) * up from the fp32 product of the pair-interleaved
+// weight, Yc [M][2N] (the path for problems outside the weight-streaming
+// kernel, whose epilogue does this itself).
+__global__ void swiglu_pairs_kernel(const float* __restrict__ Yc, void* __restrict__ Y, int yk, int M, int N) {
+  const long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
+  if (i >= static_cast<long long>(M) * N) return;
+  const int m = static_cast<int>(i / N);
+  const int j = static_cast<int>(i - static_cast<long long>(m) * N);
+  const size_t c = static_cast<size_t>(m) * 2 * N + 16 * (j >> 3) + (j & 7);
+  store_y_any(Y, yk, static_cast<size_t>(i), silu_mul(Yc[c], Yc[c + 8]));
+}
+
 __global__ void unpack_kernel(const uint32_t* __restrict__ Bpacked, uint8_t* __restrict__ q, int K,
                               int N) {
   const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
@@ -323,6 +368,26 @@ cudaError_t launch_pack(const uint8_t* q, const __half* scale, const __half* zer
   const long long count = static_cast<long long>(K / group_size) * N;
   pack_scales_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(
       scale, zero, fold, S, zero ? delta : nullptr, count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_pair(const uint8_t* q_gate, const __half* scale_gate, const __half* zero_gate,
+                             const uint8_t* q_up, const __half* scale_up, const __half* zero_up, uint32_t* Bpacked,
+                             __half* S, float* delta, int K, int N, int group_size, cudaStream_t st) {
+  const long long words = static_cast<long long>(K / 8) * 2 * N;
+  pack_pair_kernel<<<static_cast<unsigned>((words + 255) / 256), 256, 0, st>>>(q_gate, q_up, Bpacked, K, N);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int G = K / group_size;
+  const long long count = static_cast<long long>(G) * 2 * N;
+  pack_pair_scales_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(
+      scale_gate, zero_gate, scale_up, zero_up, S, delta, G, N);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_pairs(const float* Yc, void* Y, int y_kind, int M, int N, cudaStream_t st) {
+  const long long count = static_cast<long long>(M) * N;
+  swiglu_pairs_kernel<<<static_cast<unsigned>((count + 255) / 256), 256, 0, st>>>(Yc, Y, y_kind, M, N);
   return cudaGetLastError();
 }
 
