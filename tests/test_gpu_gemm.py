@@ -597,6 +597,23 @@ def _pair_inputs(seed, M, K, N, gs=128, adt="f16", zero_point=True):
     return X, A64, ws
 
 
+def _swiglu_tol(A64, gate, up, gs):
+    """The GEMM bar (2e-3 relative Frobenius on each of G and U) carried to first order
+    through Y = silu(G) * U: dY = silu'(G) U dG + silu(G) dU, with each product's error
+    spread evenly over its elements (|dG| ~ 2e-3 rms(G), |dU| ~ 2e-3 rms(U), independent).
+    On these inputs the factor over the GEMM bar is about 1.45 to 1.55."""
+    def product(w):
+        q, sb, zb = w
+        return (oracle.gemm_asym_identity(A64, q, sb, None, gs) if zb is None
+                else oracle.gemm_asym_plain(A64, q, sb, zb, gs))
+    G, U = product(gate), product(up)
+    sig = 1.0 / (1.0 + np.exp(-np.clip(G, -700, 700)))
+    silu, dsilu = G * sig, sig * (1.0 + G * (1.0 - sig))
+    rg, ru = np.sqrt(np.mean(G ** 2)), np.sqrt(np.mean(U ** 2))
+    amp = np.sqrt((np.sum((dsilu * U) ** 2) * rg ** 2 + np.sum(silu ** 2) * ru ** 2) / np.sum((silu * U) ** 2))
+    return TOL_W4A16 * amp
+
+
 def test_pair_pack_is_the_interleaved_pack(wq):
     """pack_w4a16_pair: codes, scales and deltas of the gate/up pair in the interleaved
     column order, bit for bit (unpack of the packed words, S, delta)."""
@@ -633,7 +650,7 @@ def test_swiglu_pair_parity(wq, M, K, N, gs, adt, zero_point):
     ref = oracle.gemm_swiglu_pair(A64, gate, up, gs)
     assert Y.shape == (M, N)
     err = oracle.rel_fro(Y.double().cpu().numpy(), ref)
-    assert err <= TOL_W4A16, err
+    assert err <= _swiglu_tol(A64, gate, up, gs), err
 
 
 def test_swiglu_pair_fp32_output_and_workspace_query(wq):
