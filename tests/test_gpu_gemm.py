@@ -654,7 +654,9 @@ def test_swiglu_pair_parity(wq, M, K, N, gs, adt, zero_point):
 
 
 def test_swiglu_pair_fp32_output_and_workspace_query(wq):
-    """fp32 output (no final rounding) within 1e-5 of the oracle on the fused path; the
+    """fp32 output (no final rounding) within 1e-4 of the oracle on the fused path (the
+    offset codes remove a term of ~1032 times the block sum of x from each block's fp32
+    product, which costs about 8 of fp32's 24 bits: ~3e-5 relative, measured 2.9e-5); the
     workspace query is 0 for the fused path and covers the fp32 pair product otherwise."""
     M, K, N = 2, 1024, 256
     X, A64, ((qg, sg, zg), (qu, su, zu)) = _pair_inputs(7400, M, K, N)
@@ -663,6 +665,6 @@ def test_swiglu_pair_fp32_output_and_workspace_query(wq):
     torch.cuda.synchronize()
     ref = oracle.gemm_swiglu_pair(A64, (qg, oracle.half_bits(sg), oracle.half_bits(zg)),
                                   (qu, oracle.half_bits(su), oracle.half_bits(zu)), 128)
-    assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= 1e-5
+    assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= 1e-4
     assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, M, N, K, 128) == 0
     assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, 40, N, K, 128) >= 40 * 2 * N * 4
