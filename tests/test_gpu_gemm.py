@@ -668,3 +668,53 @@ def test_swiglu_pair_fp32_output_and_workspace_query(wq):
     assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= 1e-4
     assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, M, N, K, 128) == 0
     assert wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, 40, N, K, 128) >= 40 * 2 * N * 4
+
+
+def test_every_entry_family_replays_in_a_cuda_graph(wq):
+    """Large-M W4A16, in-call-quantized W4A8 (decode and large M), the SwiGLU pair (fused and
+    through the fp32 product) and both grouped entries, captured into one CUDA graph with
+    caller workspaces and replayed: each result equals its eager call bit for bit (no entry
+    allocates or synchronises inside the capture)."""
+    K, N = 1024, 256
+    d = synth.make_inputs(7500, 64, K, N)
+    Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
+    X = _cuda(d["A"])
+    _, _, ((qg, sg, zg), (qu, su, zu)) = _pair_inputs(7501, 1, K, N // 2)
+    Bp2, S2, dl2 = wq.pack_w4a16_pair(_cuda(qg), _cuda(sg), _cuda(zg), _cuda(qu), _cuda(su), _cuda(zu), 128)
+    Bg, Sg, dg = Bp.unsqueeze(0).repeat(2, 1, 1, 1, 1), S.unsqueeze(0).repeat(2, 1, 1), dl.unsqueeze(0).repeat(2, 1, 1)
+    offs = [0, 3, 7]
+    Xq, xs = wq.quantize_per_token(X[:7].contiguous())
+    ws_bytes = max(wq.workspace_size(v, 64, N, K, 128) for v in (wq.VARIANT_W4A16, wq.VARIANT_W4A8_ASYM))
+    ws_bytes = max(ws_bytes, wq.workspace_size(wq.VARIANT_W4A16_SWIGLU, 40, N // 2, K, 128))
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device="cuda")
+    calls = [
+        lambda o: wq.gemm_w4a16(X, Bp, S, dl, 128, out=o, workspace=ws),
+        lambda o: wq.gemm_w4a8_fp16(X[:5].contiguous(), Bp, S, dl, 128, out=o, workspace=ws)[0],
+        lambda o: wq.gemm_w4a8_fp16(X[:40].contiguous(), Bp, S, dl, 128, out=o, workspace=ws)[0],
+        lambda o: wq.gemm_w4a16_swiglu(X[:4].contiguous(), Bp2, S2, dl2, 128, out=o, workspace=ws),
+        lambda o: wq.gemm_w4a16_swiglu(X[:40].contiguous(), Bp2, S2, dl2, 128, out=o, workspace=ws),
+        lambda o: wq.gemm_w4a16_grouped(X[:7].contiguous(), Bg, Sg, dg, offs, 128, out=o, workspace=ws),
+        lambda o: wq.gemm_w4a8_grouped(Xq, xs, Bg, Sg, dg, offs, 128, out=o, workspace=ws),
+    ]
+    shapes = [(64, N), (5, N), (40, N), (4, N // 2), (40, N // 2), (7, N), (7, N)]
+    eager = []
+    for f, sh in zip(calls, shapes):
+        o = torch.empty(sh, dtype=torch.float16, device="cuda")
+        f(o)
+        torch.cuda.synchronize()
+        eager.append(o.clone())
+    outs = [torch.empty(sh, dtype=torch.float16, device="cuda") for sh in shapes]
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for f, o in zip(calls, outs):
+                f(o)
+        for _ in range(2):
+            for o in outs:
+                o.zero_()
+            g.replay()
+    torch.cuda.synchronize()
+    for i, (o, e) in enumerate(zip(outs, eager)):
+        assert torch.equal(o, e), i
