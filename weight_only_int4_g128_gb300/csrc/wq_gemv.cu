@@ -469,7 +469,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     __syncthreads();
   }
   if (splits == 1) {
-    if (pair) {
+    if constexpr (pair) {
       // row rA is a gate column and rB = rA + 8 the up column of the same output
       const int j = ((n0 + 16 * warp) >> 1) + g;
 #pragma unroll
@@ -477,13 +477,13 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
         const int tok = 2 * t + e;
         if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * (N >> 1) + j, silu_mul(tot[e], tot[2 + e]));
       }
-      return;
-    }
+    } else {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int tok = 2 * t + (e & 1);
-      const int row = (e < 2) ? rA : rB;
-      if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
+      for (int e = 0; e < 4; ++e) {
+        const int tok = 2 * t + (e & 1);
+        const int row = (e < 2) ? rA : rB;
+        if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
+      }
     }
     return;
   }
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     const WaitCtx wred{&never, p.timeout_ns, kDevTimeoutFixup, status};
     mbar_wait(red_full, 0, wred);
   }
-  if (pair) {
+  if constexpr (pair) {
     // own_rows is a multiple of 16: pairs (16 * (i / 8) + i % 8, that row + 8)
     const int npair = own_rows >> 1;
     for (int i = threadIdx.x; i < npair * M; i += kThreads) {
@@ -529,14 +529,14 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
       }
       store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * (N >> 1) + ((n0 + seg * rpr) >> 1) + pi, silu_mul(gs, us));
     }
-    return;
-  }
-  for (int i = threadIdx.x; i < total; i += kThreads) {
-    const int m = i / own_rows;
-    const int lr = i - m * own_rows;
-    float sum = 0.0f;
-    for (int src = 0; src < splits; ++src) sum += red[(src * rpr + lr) * kMT + m];
-    store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
+  } else {
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+      const int m = i / own_rows;
+      const int lr = i - m * own_rows;
+      float sum = 0.0f;
+      for (int src = 0; src < splits; ++src) sum += red[(src * rpr + lr) * kMT + m];
+      store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
+    }
   }
 }
 
