@@ -9,7 +9,7 @@ weights from HBM.  The metric is weight GB/s (codes + fp16 scales + fp32 delta
 per second) for the whole job; TFLOPS is reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wq|reference]
-                    [--workload c1|c0|c2|c3|c4]
+                    [--workload c1|c0|c2|c3|c4|moe|swiglu]
 
 --impl reference times the CPU oracle (plain C, fp64, naive loops) on a bounded
 sample of the same workload.  Under torchrun each rank runs an independent
@@ -459,34 +459,39 @@ def run_gpu(args, shapes, ws, rank, local):
                             "source": traffic["capture"]} if traffic else None),
         "per_shape": shape_rows})
 
-    # --- end to end through the public API: pinned host X -> device, GEMM, Y -> pinned host.
-    # W4A16: one call with host buffers (wq.gemm_w4a16_host copies X in and Y out on the
-    # stream).  W4A8: the fp16 activations are copied in, quantized per token inside
-    # the GEMM call (gemm_w4a8_fp16), and Y is copied back.
+    # --- end to end through the public API.  The step's activations (every shape) sit in
+    # one pinned host buffer that one cudaMemcpyAsync copies in; each GEMM call reads its
+    # view of the device copy (W4A8 shapes: the fp16 rows, quantized per token inside the
+    # call by gemm_w4a8_fp16) and writes its view of one device output buffer, which one
+    # copy brings back to pinned host memory; synchronised every step.
     e2e_steps = max(20, min(200, args.steps // 50))
-    hx, hy, dx = [], [], []
-    for p in probs:
+    sizes_x = [p["s"]["M"] * p["s"]["K"] for p in probs]
+    sizes_y = [p["s"]["M"] * p["s"]["N"] for p in probs]
+    hx_all = torch.empty(sum(sizes_x), dtype=torch.int16).pin_memory()
+    hy_all = torch.empty(sum(sizes_y), dtype=torch.float16).pin_memory()
+    dx_all = torch.empty_like(hx_all, device=dev)
+    dy_all = torch.empty_like(hy_all, device=dev)
+    xv, yv = [], []
+    ox = oy = 0
+    for p, nx, ny in zip(probs, sizes_x, sizes_y):
         s = p["s"]
-        a = p["A_host"]
-        t = torch.from_numpy(a.view(np.int16) if s["a_dtype"] == "bf16" else a)
-        if s["a_dtype"] == "bf16":
-            t = t.view(torch.bfloat16)
-        hx.append(t.pin_memory())
-        hy.append(torch.empty((s["M"], s["N"]), dtype=torch.float16).pin_memory())
-        dx.append(torch.empty(hx[-1].shape, dtype=hx[-1].dtype, device=dev) if s["mode"] == "w4a8" else None)
+        hx_all[ox:ox + nx].copy_(torch.from_numpy(np.ascontiguousarray(p["A_host"]).view(np.int16).reshape(-1)))
+        x = dx_all[ox:ox + nx].view(s["M"], s["K"])
+        xv.append(x.view(torch.bfloat16) if s["a_dtype"] == "bf16" else x.view(torch.float16))
+        yv.append(dy_all[oy:oy + ny].view(s["M"], s["N"]))
         p["xs"] = torch.empty((s["M"],), dtype=torch.float32, device=dev)
-    h2d = sum(t.numel() * t.element_size() for t in hx)
-    d2h = sum(t.numel() * t.element_size() for t in hy)
+        ox += nx
+        oy += ny
+    h2d = hx_all.numel() * hx_all.element_size()
+    d2h = hy_all.numel() * hy_all.element_size()
 
     def e2e_call(j, p, r):
         s = p["s"]
         Bp, S, dl = p["w"][r]
         if s["mode"] == "w4a8":
-            dx[j].copy_(hx[j], non_blocking=True)
-            wq.gemm_w4a8_fp16(dx[j], Bp, S, None, s["group_size"], out=p["Y"], x_scale=p["xs"], workspace=p["ws"])
-            hy[j].copy_(p["Y"], non_blocking=True)
+            wq.gemm_w4a8_fp16(xv[j], Bp, S, None, s["group_size"], out=yv[j], x_scale=p["xs"], workspace=p["ws"])
         else:
-            wq.gemm_w4a16_host(hx[j], Bp, S, dl, s["group_size"], out=hy[j])
+            wq.gemm_w4a16(xv[j], Bp, S, dl, s["group_size"], out=yv[j], workspace=p["ws"])
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
@@ -494,8 +499,10 @@ def run_gpu(args, shapes, ws, rank, local):
             if i == 3:
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
+            dx_all.copy_(hx_all, non_blocking=True)
             for j, p in enumerate(probs):
                 e2e_call(j, p, i % reps)
+            hy_all.copy_(dy_all, non_blocking=True)
             stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / e2e_steps
     e2e_val = ws * step_wbytes / e2e_s / 1e9
@@ -517,9 +524,10 @@ def run_gpu(args, shapes, ws, rank, local):
         "clocks": clk,
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
-                "note": "pinned host X -> device, GEMM, Y -> pinned host through the public API "
-                        "(gemm_w4a16_host; W4A8: copy, gemm_w4a8_fp16 quantizing inside, copy), "
-                        "synchronised every step"},
+                "note": "every step: the step's activations copied from one pinned host buffer, the "
+                        "GEMM calls of the public API on the device copy (gemm_w4a16; W4A8: "
+                        "gemm_w4a8_fp16 quantizing inside), the outputs copied back to pinned host "
+                        "memory, synchronised"},
     }
     if rank == 0 and not args.no_cpu_baseline:
         gbs, tfl, el, threads, sample = oracle_sample(shapes, args.cpu_seconds)
@@ -776,20 +784,28 @@ def run_swiglu(args, ws, rank, local):
     value = job_rate(ws, calls * wb + io_bytes, ms)
     peaks, src = load_peaks()
     achieved = calls * wb / (ms * 1e-3) / 1e9
-    # end to end: pinned host X in, fused call, Y to pinned host, synchronised each step
-    hx = [torch.from_numpy(np.ascontiguousarray(A)).pin_memory() for A in d["A"]]
-    hy = [torch.empty(Y.shape, dtype=Y.dtype).pin_memory() for Y in Ys]
-    dx = [torch.empty_like(X) for X in Xs]
+    # end to end: the step's activations copied in from one pinned host buffer, the fused
+    # calls on views of the device copy, the outputs copied back in one piece; synchronised
+    # each step
+    hx = torch.from_numpy(np.concatenate([np.ascontiguousarray(A).reshape(-1) for A in d["A"]])).pin_memory()
+    hy = torch.empty(sum(Y.numel() for Y in Ys), dtype=torch.float16).pin_memory()
+    dx, dy = torch.empty_like(hx, device=dev), torch.empty_like(hy, device=dev)
+    xv, yv, ox, oy = [], [], 0, 0
+    for X, Y in zip(Xs, Ys):
+        xv.append(dx[ox:ox + X.numel()].view(X.shape))
+        yv.append(dy[oy:oy + Y.numel()].view(Y.shape))
+        ox += X.numel()
+        oy += Y.numel()
     n_e2e = max(20, min(500, args.steps // 20))
     with torch.cuda.stream(stream):
         for i in range(3 + n_e2e):
             if i == 3:
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
+            dx.copy_(hx, non_blocking=True)
             for j in range(calls):
-                dx[j].copy_(hx[j], non_blocking=True)
-                wq.gemm_w4a16_swiglu(dx[j], *W[i % reps], gs, out=Ys[j])
-                hy[j].copy_(Ys[j], non_blocking=True)
+                wq.gemm_w4a16_swiglu(xv[j], *W[i % reps], gs, out=yv[j])
+            hy.copy_(dy, non_blocking=True)
             stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / n_e2e
     line = {
@@ -807,7 +823,7 @@ def run_swiglu(args, ws, rank, local):
         "gpu_launches": args.steps * calls,
         "clocks": clk,
         "e2e": {"value": round(ws * calls * wb / e2e_s / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": sum(h.numel() * 2 for h in hx), "d2h_bytes_per_step": sum(h.numel() * 2 for h in hy)},
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 2},
     }
     if rank == 0 and not args.no_cpu_baseline:
         gbs, el, threads, sample = swiglu_oracle(d, args.cpu_seconds)
