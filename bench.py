@@ -9,7 +9,7 @@ weights from HBM.  The metric is weight GB/s (codes + fp16 scales + fp32 delta
 per second) for the whole job; TFLOPS is reported beside it.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wq|reference]
-                    [--workload c1|c0|c2|c3|c4|moe|swiglu]
+                    [--workload c1|c0|c2|c3|c4|moe|moe8|swiglu]
 
 --impl reference times the CPU oracle (plain C, fp64, naive loops) on a bounded
 sample of the same workload.  Under torchrun each rank runs an independent
@@ -45,6 +45,7 @@ WORKLOAD_NAMES = {
     "c3": "W4A16 asym prefill M4096 K5120 N17408 + M4096 K17408 N5120 g128 bf16",
     "c4": "W4A8 sym M{16,256,2048} K5120 N17408 g128 int8 per-token",
     "moe": "W4A16 asym grouped (mixture of experts): 16 tokens top-1 over 8 experts, K256 N7168 g128 fp16",
+    "moe8": "W4A8 zero-point grouped (mixture of experts): 16 int8 per-token rows top-1 over 8 experts, K256 N7168 g128",
     "swiglu": "W4A16 asym fused SwiGLU gate/up pair, decode M{1,4} K4096 N11008 (x2 projections) g128 fp16",
 }
 
@@ -550,14 +551,19 @@ def moe_weight_bytes(d) -> int:
     return live * (K * N // 2 + G * N * 6)
 
 
-def moe_oracle(d, budget_s):
+def moe_oracle(d, budget_s, w4a8=False):
     import oracle
     A = d["A"].astype(np.float64)
     sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    if w4a8:
+        Xq, xs = oracle.quantize_per_token(d["A"])
     n = 0
     t0 = time.perf_counter()
     while True:
-        oracle.gemm_grouped_asym(A, d["offsets"], d["q"], sb, zb, synth.MOE["group_size"])
+        if w4a8:
+            oracle.gemm_grouped_w4a8(Xq, xs, d["offsets"], d["q"], sb, zb, synth.MOE["group_size"])
+        else:
+            oracle.gemm_grouped_asym(A, d["offsets"], d["q"], sb, zb, synth.MOE["group_size"])
         n += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
@@ -568,16 +574,18 @@ def moe_oracle(d, budget_s):
 
 def run_moe(args, ws, rank, local):
     d = synth.moe_inputs()
+    w4a8 = args.workload == "moe8"
+    name = WORKLOAD_NAMES[args.workload]
     if args.impl == "reference":
         if rank != 0:
             return 0
-        gbs, el, threads, sample = moe_oracle(d, max(2.0, min(20.0, 4.0 * args.steps)))
+        gbs, el, threads, sample = moe_oracle(d, max(2.0, min(20.0, 4.0 * args.steps)), w4a8)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
-            "config": {"workload": WORKLOAD_NAMES["moe"], "sampled": False},
+            "config": {"workload": name, "sampled": False},
             "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
@@ -606,13 +614,25 @@ def run_moe(args, ws, rank, local):
     offs = [int(v) for v in d["offsets"]]
     X = cu(d["A"])
     Y = torch.empty((X.shape[0], w0[1].shape[-1]), dtype=torch.float16, device=dev)
+    if w4a8:
+        Xq, xs = wq.quantize_per_token(X)
+        gws = torch.zeros(max(2 * X.numel(), max(wq.workspace_size(wq.VARIANT_W4A8_ASYM, offs[e + 1] - offs[e],
+                                                                       Y.shape[1], X.shape[1], gs)
+                                                     for e in range(E) if offs[e + 1] > offs[e])),
+                          dtype=torch.uint8, device=dev)
+
+    def grouped(r, x=None, out=None):
+        if w4a8:
+            xq, xsc = (Xq, xs) if x is None else x
+            return wq.gemm_w4a8_grouped(xq, xsc, *W[r], offs, gs, out=Y if out is None else out, workspace=gws)
+        return wq.gemm_w4a16_grouped(X if x is None else x, *W[r], offs, gs, out=Y if out is None else out)
+
     for r in range(reps):
-        wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y)
+        grouped(r)
     torch.cuda.synchronize()
     stream = torch.cuda.Stream(device=dev)
     spg = 4 * STEPS_PER_GRAPH
-    graphs, graphs1 = build_step_graphs(torch, stream, reps,
-                                        lambda r: wq.gemm_w4a16_grouped(X, *W[r], offs, gs, out=Y), spg)
+    graphs, graphs1 = build_step_graphs(torch, stream, reps, grouped, spg)
     with torch.cuda.stream(stream):
         replay_steps(graphs, graphs1, args.warmup, spg)
     torch.cuda.synchronize()
@@ -633,21 +653,27 @@ def run_moe(args, ws, rank, local):
         torch.distributed.barrier()
     clk = clocks.stop()
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
-    value = job_rate(ws, wb + X.numel() * 2 + Y.numel() * 2, ms)
+    xbytes = X.numel() * (1 if w4a8 else 2) + (X.shape[0] * 4 if w4a8 else 0)
+    value = job_rate(ws, wb + xbytes + Y.numel() * 2, ms)
     peaks, src = load_peaks()
     achieved = wb / (ms * 1e-3) / 1e9
-    # end to end: pinned host X in, grouped call, Y to pinned host, synchronised each step
-    hx = torch.from_numpy(np.ascontiguousarray(d["A"])).pin_memory()
+    # end to end: pinned host rows in (W4A8: the int8 rows and their scales), grouped
+    # call, Y to pinned host, synchronised each step
+    if w4a8:
+        hx = [Xq.cpu().pin_memory(), xs.cpu().pin_memory()]
+    else:
+        hx = [torch.from_numpy(np.ascontiguousarray(d["A"])).pin_memory()]
     hy = torch.empty(Y.shape, dtype=Y.dtype).pin_memory()
-    dx = torch.empty_like(X)
+    dx = [torch.empty_like(h, device=dev) for h in hx]
     n_e2e = max(20, min(500, args.steps // 20))
     with torch.cuda.stream(stream):
         for i in range(3 + n_e2e):
             if i == 3:
                 torch.cuda.synchronize()
                 t0 = time.perf_counter()
-            dx.copy_(hx, non_blocking=True)
-            wq.gemm_w4a16_grouped(dx, *W[i % reps], offs, gs, out=Y)
+            for a, h in zip(dx, hx):
+                a.copy_(h, non_blocking=True)
+            grouped(i % reps, x=tuple(dx) if w4a8 else dx[0])
             hy.copy_(Y, non_blocking=True)
             stream.synchronize()
     e2e_s = (time.perf_counter() - t0) / n_e2e
@@ -655,21 +681,23 @@ def run_moe(args, ws, rank, local):
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
-        "config": {"workload": WORKLOAD_NAMES["moe"], "tokens_per_expert": [offs[e + 1] - offs[e] for e in range(E)],
+        "config": {"workload": name, "tokens_per_expert": [offs[e + 1] - offs[e] for e in range(E)],
                    "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
                    "graph": "CUDA graphs of 32 consecutive grouped calls, the weight copy rotating call by call",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
-                     "kernel": "wq::gemv_kernel, grouped launch (grid.z = expert); weight bytes of experts with tokens",
+                     "kernel": "wq::gemv_kernel, grouped launch (grid.z = expert); weight bytes of experts with tokens"
+                               + ("; after one int8 -> fp16 pass over the rows" if w4a8 else ""),
                      "peak_source": src},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if w4a8 else 1),
         "clocks": clk,
-        "e2e": {"value": round(ws * wb / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": hx.numel() * 2,
+        "e2e": {"value": round(ws * wb / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hx),
                 "d2h_bytes_per_step": hy.numel() * 2},
     }
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, el, threads, sample = moe_oracle(d, args.cpu_seconds)
+        gbs, el, threads, sample = moe_oracle(d, args.cpu_seconds, w4a8)
         line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": sample, "seconds": round(el, 2)}
     if ws > 1:
@@ -853,7 +881,7 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     ws, rank, local = dist_init()
-    if args.workload == "moe":
+    if args.workload in ("moe", "moe8"):
         return run_moe(args, ws, rank, local)
     if args.workload == "swiglu":
         return run_swiglu(args, ws, rank, local)

@@ -205,8 +205,9 @@ int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, co
  *   S, delta      experts x [G][N] device (delta NULL: symmetric).
  *   expert_offsets HOST int array of experts + 1 entries, offsets[0] == 0,
  *                 non-decreasing; experts in 1..64.
- *   workspace     wq_workspace_size(variant, max tokens of one expert, N, K,
- *                 group_size) bytes (0 when every expert has <= 8 tokens).
+ *   workspace     the largest wq_workspace_size(variant, tokens of one
+ *                 expert, N, K, group_size) over the experts (0 when every
+ *                 expert has <= 8 tokens).
  * With at most 8 tokens per expert this is one launch over all experts (an
  * expert without tokens costs nothing); otherwise one GEMM per expert.
  * Other arguments as wq_gemm_w4a16.
@@ -228,12 +229,15 @@ int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, c
  *   Bpacked, S, delta: one weight per expert, stacked expert-major as in
  *                 wq_gemm_w4a16_grouped.
  *   expert_offsets HOST int array as in wq_gemm_w4a16_grouped.
- *   workspace     the largest wq_workspace_size(variant, tokens of one
- *                 expert, N, K, group_size) over the experts, variant
- *                 WQ_VARIANT_W4A8_ASYM with delta, WQ_VARIANT_W4A8 without.
- * One GEMM (activation pre-pass + GEMM) per expert that has tokens, all on
- * `stream`; the workspace need of every expert is checked before anything is
- * enqueued.  Other arguments as wq_gemm_w4a16.
+ *   workspace     at least 2*M*K bytes and at least the largest
+ *                 wq_workspace_size(variant, tokens of one expert, N, K,
+ *                 group_size) over the experts, variant WQ_VARIANT_W4A8_ASYM
+ *                 with delta, WQ_VARIANT_W4A8 without; 16-byte aligned.
+ * With at most 8 tokens per expert: one int8 -> fp16 pass over the rows, then
+ * one weight-streaming launch over all experts (per-token scale applied at
+ * the store).  Otherwise one W4A8 GEMM (activation pre-pass + GEMM) per expert
+ * that has tokens.  All on `stream`; the workspace is checked before anything
+ * is enqueued.  Other arguments as wq_gemm_w4a16.
  */
 int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
                          const float* delta, void* Y, int y_dtype, const int* expert_offsets, int experts, int N,

@@ -214,6 +214,24 @@ def test_w4a8_parity(wq, M, K, N):
     assert oracle.rel_fro(y, ref16) <= TOL_W4A8_VS_F16
 
 
+@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (8, 2048), (12, 1024)])
+def test_w4a8_decode_integer_problems_exact(wq, M, K):
+    """Unit scales and unit per-token scales make Y = Xq @ (q - 8), an integer below 2^24:
+    both decode paths (weight-streaming kernel on exact fp16 copies of the int8 rows for
+    M <= 8, the e4m3 tcgen05 kernel for M 9..16) give it exactly in fp32."""
+    rng = np.random.default_rng(990 + M)
+    N = 256
+    Xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
+    q = rng.integers(0, 16, size=(K, N)).astype(np.uint8)
+    ones = np.ones((K // 128, N), np.float16)
+    Bp, S = wq.pack_w4a8(_cuda(q), _cuda(ones), 128)
+    Y = wq.gemm_w4a8(_cuda(Xq), _cuda(np.ones(M, np.float32)), Bp, S, 128, torch.float32)
+    torch.cuda.synchronize()
+    want = Xq.astype(np.int64) @ (q.astype(np.int64) - 8)
+    assert np.array_equal(Y.cpu().numpy().astype(np.int64), want)
+    assert np.array_equal(Y.cpu().numpy(), want.astype(np.float32))
+
+
 def test_w4a8_gpu_quantizer_end_to_end(wq):
     d = synth.make_inputs(950, 24, 1024, 256, mode="w4a8")
     Xq, xs = wq.quantize_per_token(_cuda(d["A"]))
@@ -718,3 +736,25 @@ def test_every_entry_family_replays_in_a_cuda_graph(wq):
     torch.cuda.synchronize()
     for i, (o, e) in enumerate(zip(outs, eager)):
         assert torch.equal(o, e), i
+
+
+def test_swiglu_pair_bench_size_sampled(wq):
+    """The bench's SwiGLU workload (M 1 and 4, K 4096, two N = 11008 projections), in the
+    bench's launch configuration (one launch of the pair instance), on sampled output
+    columns against the oracle on the same gate and up columns."""
+    d = synth.swiglu_inputs()
+    g, u = d["gate"], d["up"]
+    Bp, S, dl = wq.pack_w4a16_pair(_cuda(g["q"]), _cuda(g["scale"]), _cuda(g["zero"]),
+                                   _cuda(u["q"]), _cuda(u["scale"]), _cuda(u["zero"]), 128)
+    N = g["q"].shape[1]
+    hb = oracle.half_bits
+    for A in d["A"]:
+        Y = wq.gemm_w4a16_swiglu(_cuda(A), Bp, S, dl, 128)
+        torch.cuda.synchronize()
+        A64 = A.astype(np.float64)
+        for c0, c1 in _sample_cols(N):
+            gate = (np.ascontiguousarray(g["q"][:, c0:c1]), hb(g["scale"][:, c0:c1]), hb(g["zero"][:, c0:c1]))
+            up = (np.ascontiguousarray(u["q"][:, c0:c1]), hb(u["scale"][:, c0:c1]), hb(u["zero"][:, c0:c1]))
+            ref = oracle.gemm_swiglu_pair(A64, gate, up, 128)
+            err = oracle.rel_fro(Y[:, c0:c1].double().cpu().numpy(), ref)
+            assert err <= _swiglu_tol(A64, gate, up, 128), (c0, err)

@@ -426,9 +426,9 @@ def gemm_w4a16_grouped(X, Bpacked, S, delta, expert_offsets, group_size: int = 1
     lib = _lib or load_library()
     stream = _raw_stream(X.device.index)
     if workspace is None:
-        max_m = max((offs[e + 1] - offs[e] for e in range(E)), default=0)
         variant = VARIANT_W4A16 if delta is not None else VARIANT_W4A16_SYM
-        need = workspace_size(variant, max_m, N, K, group_size) if max_m > 0 else 0
+        counts = {offs[e + 1] - offs[e] for e in range(E)} - {0}
+        need = max(workspace_size(variant, m, N, K, group_size) for m in counts) if counts else 0
         workspace = _stream_workspace(X.device, stream).get(need) if need > 0 else None
     rc = lib.wq_gemm_w4a16_grouped(X.data_ptr(), _dtype_code(X.dtype), Bpacked.data_ptr(), S.data_ptr(),
                                    delta.data_ptr() if delta is not None else None, Y.data_ptr(),
@@ -457,9 +457,9 @@ def gemm_w4a8_grouped(Xq, x_scale, Bpacked, S, delta, expert_offsets, group_size
     lib = _lib or load_library()
     stream = _raw_stream(Xq.device.index)
     if workspace is None:
-        max_m = max((offs[e + 1] - offs[e] for e in range(E)), default=0)
         variant = VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8
-        need = workspace_size(variant, max_m, N, K, group_size) if max_m > 0 else 0
+        counts = {offs[e + 1] - offs[e] for e in range(E)} - {0}
+        need = max([2 * M * K] + [workspace_size(variant, m, N, K, group_size) for m in counts]) if counts else 0
         workspace = _stream_workspace(Xq.device, stream).get(need) if need > 0 else None
     rc = lib.wq_gemm_w4a8_grouped(Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S.data_ptr(),
                                   delta.data_ptr() if delta is not None else None, Y.data_ptr(),

@@ -24,6 +24,11 @@
 // low / high-nibble k formed while the activation tile is staged.  The 8 token
 // slots are the MMA's N = 8; slots past M read zeros.
 //
+// W4A8 rows run through the same kernel: the int8 activations arrive as fp16
+// (exact, |x| <= 127), so every offset-code product and block sum is an
+// integer below 2^24 and each block's D is exact in fp32; the per-token scale
+// multiplies the result at the store.
+//
 // A grouped (mixture-of-experts) launch runs the same kernel over all experts:
 // blockIdx.z is the expert, whose token rows, weights, scales and delta the CTA
 // offsets to; an expert without tokens returns at once.
@@ -182,7 +187,7 @@ __device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) |
 // MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
 // wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
 // per column tile and expert) then fit in one wave.
-template <int XK, int D, int MINB, bool PAIR>
+template <int XK, int D, int MINB, bool PAIR, bool XS>
 __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmParams p, unsigned* status) {
   using namespace gv;
   extern __shared__ uint8_t smem_raw[];
@@ -207,6 +212,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
   // token rows and weights.  An expert without tokens has nothing to do.
   int M = p.M;
   const uint8_t* Xp = static_cast<const uint8_t*>(p.X);
+  const float* Xsp = p.x_scale;  // XS: per-token scale of int8 rows given as fp16 (W4A8)
   uint8_t* Yp = static_cast<uint8_t*>(p.Y);
   const uint32_t* Bp = p.B;
   const __half* Sp = p.S;
@@ -217,6 +223,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     M = p.goff[e + 1] - r0;
     if (M <= 0) return;
     Xp += static_cast<size_t>(r0) * p.K * 2;
+    if (XS) Xsp += r0;
     Yp += static_cast<size_t>(r0) * N * (p.y_kind == kYF32 ? 4 : 2);
     Bp += e * p.b_stride;
     Sp += e * p.sd_stride;
@@ -482,7 +489,8 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
       for (int e = 0; e < 4; ++e) {
         const int tok = 2 * t + (e & 1);
         const int row = (e < 2) ? rA : rB;
-        if (tok < M) store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, tot[e]);
+        if (tok < M)
+          store_y_any(Yp, p.y_kind, static_cast<size_t>(tok) * N + n0 + row, XS ? tot[e] * Xsp[tok] : tot[e]);
       }
     }
     return;
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
       const int lr = i - m * own_rows;
       float sum = 0.0f;
       for (int src = 0; src < splits; ++src) sum += red[(src * rpr + lr) * kMT + m];
-      store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, sum);
+      store_y_any(Yp, p.y_kind, static_cast<size_t>(m) * N + n0 + seg * rpr + lr, XS ? sum * Xsp[m] : sum);
     }
   }
 }
@@ -569,7 +577,7 @@ bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delt
          gv::layout(M, kbps, splits, per_channel ? 1 : kbps, has_delta, gv::kRingDepth, pair).bytes <= gv::kMaxSmem;
 }
 
-template <int XK, int D, int MINB, bool PAIR>
+template <int XK, int D, int MINB, bool PAIR, bool XS = false>
 static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
   static unsigned long long attr_mask = 0;
   int dev = 0;
@@ -577,7 +585,7 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   if (e != cudaSuccess) return e;
   const unsigned long long bit = 1ull << (dev & 63);
   if (!(attr_mask & bit)) {
-    e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
+    e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB, PAIR, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
     if (e != cudaSuccess) return e;
     attr_mask |= bit;
   }
@@ -598,16 +606,21 @@ static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStre
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D, MINB, PAIR>, p, status);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<XK, D, MINB, PAIR, XS>, p, status);
 }
 
 cudaError_t launch_gemv(int x_kind, const GemmParams& p, cudaStream_t stream) {
   unsigned* status = status_word();
   if (!status) return cudaErrorInvalidSymbol;
-  if (p.splits < 1 || p.splits > gv::kMaxSplits || p.M < 1 || p.M > gv::kMaxM || p.x_scale || !p.X ||
+  if (p.splits < 1 || p.splits > gv::kMaxSplits || p.M < 1 || p.M > gv::kMaxM || (p.x_scale && p.swiglu) || !p.X ||
       p.experts < 0 || p.experts > kMaxExperts ||
       p.kb_per_split < 1 || (p.splits - 1) * p.kb_per_split >= p.kb_total)
     return cudaErrorInvalidValue;
+  if (p.x_scale) {  // W4A8 rows as fp16
+    if (x_kind != kXF16) return cudaErrorInvalidValue;
+    if (p.experts > 0) return launch_gemv_t<kXF16, gv::kRingDepth, 3, false, true>(p, status, stream);
+    return launch_gemv_t<kXF16, gv::kRingDepth, 2, false, true>(p, status, stream);
+  }
   if (p.experts > 0) {
     if (p.swiglu) return cudaErrorInvalidValue;
     if (x_kind == kXBF16) return launch_gemv_t<kXBF16, gv::kRingDepth, 3, false>(p, status, stream);
