@@ -229,15 +229,15 @@ int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, c
  *   Bpacked, S, delta: one weight per expert, stacked expert-major as in
  *                 wq_gemm_w4a16_grouped.
  *   expert_offsets HOST int array as in wq_gemm_w4a16_grouped.
- *   workspace     at least 2*M*K bytes and at least the largest
- *                 wq_workspace_size(variant, tokens of one expert, N, K,
- *                 group_size) over the experts, variant WQ_VARIANT_W4A8_ASYM
- *                 with delta, WQ_VARIANT_W4A8 without; 16-byte aligned.
- * With at most 8 tokens per expert: one int8 -> fp16 pass over the rows, then
- * one weight-streaming launch over all experts (per-token scale applied at
- * the store).  Otherwise one W4A8 GEMM (activation pre-pass + GEMM) per expert
- * that has tokens.  All on `stream`; the workspace is checked before anything
- * is enqueued.  Other arguments as wq_gemm_w4a16.
+ *   workspace     the largest wq_workspace_size(variant, tokens of one
+ *                 expert, N, K, group_size) over the experts, variant
+ *                 WQ_VARIANT_W4A8_ASYM with delta, WQ_VARIANT_W4A8 without
+ *                 (not used when every expert has <= 8 tokens).
+ * With at most 8 tokens per expert: one weight-streaming launch over all
+ * experts, which reads the int8 rows and applies the per-token scale at its
+ * store.  Otherwise one W4A8 GEMM (activation pre-pass + GEMM) per expert that
+ * has tokens, every expert's workspace need checked before anything is
+ * enqueued.  All on `stream`.  Other arguments as wq_gemm_w4a16.
  */
 int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked, const void* S,
                          const float* delta, void* Y, int y_dtype, const int* expert_offsets, int experts, int N,

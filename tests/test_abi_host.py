@@ -202,8 +202,10 @@ def test_grouped_w4a8_entry_checks(lib):
     empty = (ctypes.c_int * 4)(0, 0, 0, 0)
     assert f(None, None, None, None, None, None, 0, empty, 3, 256, 256, 128, None, 0, None) == 0  # no tokens
     assert f(fake, P(0x10002), fake, fake, None, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 1  # x_scale
-    # the workspace of the largest expert is checked before anything is enqueued
-    assert f(fake, fake, fake, fake, None, fake, 0, offs, 3, 256, 256, 128, None, 0, None) == 3
+    # beyond 8 tokens per expert (one GEMM per expert) every expert's workspace is checked
+    # before anything is enqueued
+    big = (ctypes.c_int * 4)(0, 2, 2, 15)
+    assert f(fake, fake, fake, fake, None, fake, 0, big, 3, 256, 256, 128, None, 0, None) == 3
 
 
 def test_swiglu_pair_entry_checks(lib):

@@ -459,7 +459,7 @@ def gemm_w4a8_grouped(Xq, x_scale, Bpacked, S, delta, expert_offsets, group_size
     if workspace is None:
         variant = VARIANT_W4A8_ASYM if delta is not None else VARIANT_W4A8
         counts = {offs[e + 1] - offs[e] for e in range(E)} - {0}
-        need = max([2 * M * K] + [workspace_size(variant, m, N, K, group_size) for m in counts]) if counts else 0
+        need = max(workspace_size(variant, m, N, K, group_size) for m in counts) if counts else 0
         workspace = _stream_workspace(Xq.device, stream).get(need) if need > 0 else None
     rc = lib.wq_gemm_w4a8_grouped(Xq.data_ptr(), x_scale.data_ptr(), Bpacked.data_ptr(), S.data_ptr(),
                                   delta.data_ptr() if delta is not None else None, Y.data_ptr(),

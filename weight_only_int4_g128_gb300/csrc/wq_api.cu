@@ -304,16 +304,19 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
     return after_launch(e, name, st);
   }
   if (plan.gemv) {
-    // decode W4A8 with at most 8 tokens: the int8 rows converted exactly to fp16
-    // (or quantized straight to fp16 codes), then the weight-streaming kernel
-    // with the per-token scale applied at its store
+    // decode W4A8 with at most 8 tokens: the weight-streaming kernel reads the
+    // int8 rows (fp16 rows are first quantized per token into the workspace)
+    // and applies the per-token scale at its store
     int gv_splits = 0, gv_kbps = 0;
     if (wq::gemv_plan(M, N, K, gs, corr, &gv_splits, &gv_kbps)) {
-      __half* x16 = reinterpret_cast<__half*>(wsb + plan.off_x8);  // M * K * 2 bytes <= the e4m3 rows' room
-      e = quant_in ? wq::launch_quant_f16(static_cast<const __half*>(X), M, K, x16, const_cast<float*>(x_scale), st)
-                   : wq::launch_i8_to_f16(static_cast<const int8_t*>(X), x16, static_cast<long long>(M) * K, st);
-      if (e != cudaSuccess) return cuda_fail(e, "int8 -> fp16 pre-pass");
-      return launch_gemv_call(x16, wq::kXF16, Bpacked, S, corr ? delta : nullptr, Y, y_kind, M, N, K, gs, gv_splits,
+      const void* xq = X;
+      if (quant_in) {
+        int8_t* x8q = reinterpret_cast<int8_t*>(wsb + plan.off_x8);  // M * K bytes <= the e4m3 rows' room
+        e = wq::launch_quantize_per_token(static_cast<const __half*>(X), x8q, const_cast<float*>(x_scale), M, K, st);
+        if (e != cudaSuccess) return cuda_fail(e, "per-token quantization");
+        xq = x8q;
+      }
+      return launch_gemv_call(xq, wq::kXF16, Bpacked, S, corr ? delta : nullptr, Y, y_kind, M, N, K, gs, gv_splits,
                               gv_kbps, false, st, name, x_scale);
     }
     // decode W4A8: activation pre-pass (e4m3 components, block sums and factors), then the GEMM
@@ -831,34 +834,18 @@ int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t*
   const long long b_stride = static_cast<long long>(K) * N / 8;
   const long long sd_stride = static_cast<long long>(K / gs) * N;
   const size_t ysz = (yk == wq::kYF32) ? 4 : 2;
-  const int M = expert_offsets[experts];
-  // the whole workspace need (the fp16 copy of the rows, every expert's GEMM) is
-  // checked before anything is enqueued
-  size_t need = static_cast<size_t>(M) * K * 2;
   int max_m = 0;
   for (int e = 0; e < experts; ++e) {
     const int me = expert_offsets[e + 1] - expert_offsets[e];
     max_m = me > max_m ? me : max_m;
-    if (me > 0) {
-      const size_t b = make_plan(variant, me, N, K, gs).bytes;
-      need = b > need ? b : need;
-    }
   }
-  if (!workspace || workspace_bytes < need)
-    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a8_grouped: workspace of %zu bytes given, %zu needed", workspace_bytes,
-                need);
-  if (!aligned16(workspace)) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a8_grouped: workspace must be 16-byte aligned");
-  if ((rc = check_device())) return rc;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int g_splits = 0, g_kbps = 0;
   if (wq::gemv_plan(max_m, N, K, gs, delta != nullptr, &g_splits, &g_kbps) &&
       wq::gemv_plan_fits(max_m, K / 128, 1, gs == K, delta != nullptr)) {
-    // every expert has at most 8 tokens: the rows converted exactly to fp16 once,
-    // then one weight-streaming launch over all experts, the per-token scale
-    // applied at its store
-    __half* x16 = static_cast<__half*>(workspace);
-    cudaError_t e = wq::launch_i8_to_f16(Xq, x16, static_cast<long long>(M) * K, st);
-    if (e != cudaSuccess) return cuda_fail(e, "int8 -> fp16 pre-pass");
+    // every expert has at most 8 tokens: one weight-streaming launch over all
+    // experts reads the int8 rows and applies the per-token scale at its store
+    if ((rc = check_device())) return rc;
     wq::GemmParams p{};
     p.M = max_m;
     p.N = N;
@@ -868,7 +855,7 @@ int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t*
     p.kb_total = K / 128;
     p.kb_per_split = K / 128;
     p.splits = 1;
-    p.X = x16;
+    p.X = Xq;
     p.B = Bpacked;
     p.S = static_cast<const __half*>(S);
     p.delta = delta;
@@ -883,6 +870,19 @@ int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t*
     for (int i = 0; i <= experts; ++i) p.goff[i] = expert_offsets[i];
     return after_launch(wq::launch_gemv(wq::kXF16, p, st), "wq_gemm_w4a8_grouped", st);
   }
+  // every expert's workspace need is checked before anything is enqueued
+  size_t need = 0;
+  for (int e = 0; e < experts; ++e) {
+    const int me = expert_offsets[e + 1] - expert_offsets[e];
+    if (me > 0) {
+      const size_t b = make_plan(variant, me, N, K, gs).bytes;
+      need = b > need ? b : need;
+    }
+  }
+  if (need > 0 && (!workspace || workspace_bytes < need))
+    return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a8_grouped: workspace of %zu bytes given, %zu needed", workspace_bytes,
+                need);
+  if ((rc = check_device())) return rc;
   for (int e = 0; e < experts; ++e) {
     const int r0 = expert_offsets[e];
     const int me = expert_offsets[e + 1] - r0;

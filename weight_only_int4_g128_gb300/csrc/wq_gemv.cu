@@ -24,10 +24,10 @@
 // low / high-nibble k formed while the activation tile is staged.  The 8 token
 // slots are the MMA's N = 8; slots past M read zeros.
 //
-// W4A8 rows run through the same kernel: the int8 activations arrive as fp16
-// (exact, |x| <= 127), so every offset-code product and block sum is an
-// integer below 2^24 and each block's D is exact in fp32; the per-token scale
-// multiplies the result at the store.
+// W4A8 rows run through the same kernel: the int8 activations are turned into
+// fp16 (exact, |x| <= 127) as they are staged, so every offset-code product
+// and block sum is an integer below 2^24 and each block's D is exact in fp32;
+// the per-token scale multiplies the result at the store.
 //
 // A grouped (mixture-of-experts) launch runs the same kernel over all experts:
 // blockIdx.z is the expert, whose token rows, weights, scales and delta the CTA
@@ -187,6 +187,21 @@ __device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) |
 // MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
 // wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
 // per column tile and expert) then fit in one wave.
+// Eight int8 activations (one 8-byte load) as the 16-byte chunk of their fp16
+// values, element e in half e of the chunk (|x| <= 128: exact).
+__device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t word = (i < 2) ? w.x : w.y;
+    const int sh = 16 * (i & 1);
+    const __half2 h = __halves2half2(__short2half_rn(static_cast<short>(static_cast<int8_t>(word >> sh))),
+                                     __short2half_rn(static_cast<short>(static_cast<int8_t>(word >> (sh + 8)))));
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 template <int XK, int D, int MINB, bool PAIR, bool XS>
 __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmParams p, unsigned* status) {
   using namespace gv;
@@ -212,7 +227,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
   // token rows and weights.  An expert without tokens has nothing to do.
   int M = p.M;
   const uint8_t* Xp = static_cast<const uint8_t*>(p.X);
-  const float* Xsp = p.x_scale;  // XS: per-token scale of int8 rows given as fp16 (W4A8)
+  const float* Xsp = p.x_scale;  // XS: X holds int8 rows (W4A8), this their per-token scales
   uint8_t* Yp = static_cast<uint8_t*>(p.Y);
   const uint32_t* Bp = p.B;
   const __half* Sp = p.S;
@@ -222,7 +237,7 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
     const int r0 = p.goff[e];
     M = p.goff[e + 1] - r0;
     if (M <= 0) return;
-    Xp += static_cast<size_t>(r0) * p.K * 2;
+    Xp += static_cast<size_t>(r0) * p.K * (XS ? 1 : 2);
     if (XS) Xsp += r0;
     Yp += static_cast<size_t>(r0) * N * (p.y_kind == kYF32 ? 4 : 2);
     Bp += e * p.b_stride;
@@ -332,7 +347,12 @@ __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmPara
         if (idx < total) {
           const int m = idx / per_tok;
           const int rem = idx - m * per_tok;
-          v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
+          if constexpr (XS) {
+            v[u] = i8x8_to_f16x8(
+                *reinterpret_cast<const uint2*>(xg + static_cast<size_t>(m) * p.K + kb0 * kKBlock + rem * 8));
+          } else {
+            v[u] = *reinterpret_cast<const uint4*>(xg + (static_cast<size_t>(m) * p.K + kb0 * kKBlock) * 2 + rem * 16);
+          }
         }
       }
       if (b == 0) {
