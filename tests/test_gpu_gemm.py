@@ -398,8 +398,10 @@ def test_weight_streaming_decode_segments(wq, M, K, N, gs, adt):
 
 
 @pytest.mark.parametrize("M,K,N,gs,odt", [
-    (1, 1024, 384, 128, torch.float16),    # decode path (e4m3 components)
+    (1, 1024, 384, 128, torch.float16),    # M <= 8: weight-streaming kernel on the int8 rows
+    (3, 1024, 256, 128, torch.bfloat16),
     (5, 2048, 256, -1, torch.float16),
+    (12, 1024, 256, 128, torch.float32),   # M 9..16: e4m3 decode kernel
     (16, 1280, 256, 128, torch.bfloat16),
     (33, 768, 256, 128, torch.float16),    # large-M path (int8 -> fp16, correction columns)
     (200, 1024, 384, 128, torch.float32),
