@@ -56,3 +56,25 @@ def test_reference_arm_prints_on_rank_0_only():
     with redirect_stdout(buf):
         assert bench.run_reference(A, synth.shapes("c0"), 2, 1) == 0
     assert buf.getvalue() == ""
+
+
+@pytest.mark.parametrize("workload", ["moe", "moe8", "swiglu"])
+def test_grouped_and_pair_reference_arms_print_one_line(workload):
+    """The oracle arms of the grouped (W4A16, W4A8) and SwiGLU pair workloads print one JSON
+    line on rank 0 with the contract's keys; other ranks print nothing."""
+    import json
+
+    class A:
+        steps, warmup, impl = 1, 3, "reference"
+    A.workload = workload
+    run = bench.run_swiglu if workload == "swiglu" else bench.run_moe
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert run(A, 2, 1, 0) == 0
+    assert buf.getvalue() == ""
+    with redirect_stdout(buf):
+        assert run(A, 1, 0, 0) == 0
+    line = json.loads(buf.getvalue().strip())
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
+    assert line["config"]["workload"] == bench.WORKLOAD_NAMES[workload]
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
