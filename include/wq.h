@@ -270,9 +270,10 @@ int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bp
  * to int8).  x_scale[m] = RN32(max_k |X[m][k]| / 127) and the codes
  * clamp(round_half_even(RN32(X / x_scale)), -127, 127) are exactly those of
  * wq_quantize_per_token; Y is then that of wq_gemm_w4a8_asym (delta given) or
- * wq_gemm_w4a8 (delta NULL), bit for bit.  The codes are never written out:
- * the activation pre-pass of the GEMM quantizes them on the way (one launch
- * instead of two).
+ * wq_gemm_w4a8 (delta NULL), bit for bit.  The quantization is the GEMM's own
+ * activation pre-pass: for M 9..16 it splits the codes into e4m3 components
+ * on the way (the codes are never written out), for M <= 8 it writes them to
+ * the workspace for the weight-streaming kernel, for larger M as fp16.
  *   X        [M][K] fp16 device.
  *   x_scale  [M] fp32 device, output: the per-token scales.
  *   Bpacked, S, delta: from wq_pack_w4a16 (zero-point weights; delta may be

@@ -217,8 +217,8 @@ def test_w4a8_parity(wq, M, K, N):
 @pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (8, 2048), (12, 1024)])
 def test_w4a8_decode_integer_problems_exact(wq, M, K):
     """Unit scales and unit per-token scales make Y = Xq @ (q - 8), an integer below 2^24:
-    both decode paths (weight-streaming kernel on exact fp16 copies of the int8 rows for
-    M <= 8, the e4m3 tcgen05 kernel for M 9..16) give it exactly in fp32."""
+    both decode paths (the weight-streaming kernel, which stages the int8 rows as exact fp16,
+    for M <= 8; the e4m3 tcgen05 kernel for M 9..16) give it exactly in fp32."""
     rng = np.random.default_rng(990 + M)
     N = 256
     Xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
@@ -441,7 +441,7 @@ def test_w4a8_zero_point_without_delta_is_symmetric(wq, M):
 def test_w4a8_quantize_inside_equals_two_steps(wq, M, K, N, zero_point):
     """gemm_w4a8_fp16 (per-token quantization inside the activation pre-pass) gives the
     x_scale of quantize_per_token and the Y of quantize_per_token + the int8 GEMM, bit for
-    bit, on both kernel paths; and the oracle's value within 2e-3."""
+    bit, on every kernel path (M <= 8, M 9..16, large M); and the oracle's value within 2e-3."""
     if zero_point:
         d = synth.make_inputs(6300 + M, M, K, N)
         Bp, S, dl = wq.pack_w4a16(_cuda(d["q"]), _cuda(d["scale"]), _cuda(d["zero"]), 128)
