@@ -33,6 +33,10 @@
 // blockIdx.z is the expert, whose token rows, weights, scales and delta the CTA
 // offsets to; an expert without tokens returns at once.
 //
+// A gate/up pair weight (16-column groups of 8 gate and the same 8 up columns)
+// puts a gate row and its up row 8 rows apart in one m16 strip, which the MMA
+// accumulator hands to the same lane: that instance stores silu(gate) * up.
+//
 // Work split: one CTA per (128-row column tile, K segment); warp w owns rows
 // 16 w .. 16 w + 15 of the tile (one m16 strip) for the whole segment.  The K
 // segments of a tile form a thread-block cluster and are reduced through
