@@ -214,11 +214,12 @@ def test_w4a8_parity(wq, M, K, N):
     assert oracle.rel_fro(y, ref16) <= TOL_W4A8_VS_F16
 
 
-@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (8, 2048), (12, 1024)])
-def test_w4a8_decode_integer_problems_exact(wq, M, K):
+@pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (8, 2048), (12, 1024), (40, 1024), (300, 2048)])
+def test_w4a8_integer_problems_exact(wq, M, K):
     """Unit scales and unit per-token scales make Y = Xq @ (q - 8), an integer below 2^24:
-    both decode paths (the weight-streaming kernel, which stages the int8 rows as exact fp16,
-    for M <= 8; the e4m3 tcgen05 kernel for M 9..16) give it exactly in fp32."""
+    every path (the weight-streaming kernel, which stages the int8 rows as exact fp16, for
+    M <= 8; the e4m3 tcgen05 kernel for M 9..16; the large-M kernel on exact fp16 rows and
+    weights) gives it exactly in fp32, so no low bit of an integer sum is dropped."""
     rng = np.random.default_rng(990 + M)
     N = 256
     Xq = rng.integers(-127, 128, size=(M, K)).astype(np.int8)
