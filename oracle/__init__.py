@@ -10,9 +10,12 @@ product package: the two share no code.  Every stored expected value under
 The arithmetic lives in ``wq_oracle.c`` (plain C, IEEE binary64, naive loops);
 this module compiles it with ``gcc`` on first use and marshals numpy arrays to
 it.  Sources: "Marlin INT4 on Ada -- how it works" (TinyLoop docs), sections
-"The core mismatch: symmetric vs asymmetric" and "The pipeline, end to end";
-the HyperQwen W4A8 article, sections "hidden mine: the negative group scale
-bug" and "int8 tensor cores: how the numbers were verified".
+"The core mismatch: symmetric vs asymmetric", "The pipeline, end to end" and
+"Gaps and follow-ups" (the fused SwiGLU pair); the HyperQwen W4A8 article,
+sections "hidden mine: the negative group scale bug" and "int8 tensor cores:
+how the numbers were verified"; the SGLang W4A8 article, section "task split"
+(the grouped mixture-of-experts GEMM).  The grouped and SwiGLU functions are
+plain Python loops over the C routines.
 
 Parity status: every function here is pinned by ``tests/test_oracle_pins.py``
 against closed forms, library routines, brute force or printed values.
