@@ -1,8 +1,9 @@
 """GPU GEMM parity against the fp64 oracle, through the C ABI.
 
-Bar (from the benchmark spec): ||Y - C_ref||_F / ||C_ref||_F <= 2e-3 for
-W4A16 (fp32 accumulate); W4A8 <= 2e-3 against the oracle over the int8
-activations and <= 5 % against the fp16-activation oracle.  Special cases whose
+Bars: ||Y - C_ref||_F / ||C_ref||_F <= 2e-3 for W4A16 (fp32 accumulate); W4A8
+<= 2e-3 against the oracle over the int8 activations and <= 5 % against the
+fp16-activation oracle (the acceptance level of the HyperQwen article, section
+"int8 tensor cores: how the numbers were verified").  Special cases whose
 result is exact (one-hot rows, integer weights, zero weights) are compared bit
 for bit, and repeated runs must be bitwise identical.
 """
