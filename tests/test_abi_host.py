@@ -206,6 +206,13 @@ def test_grouped_w4a8_entry_checks(lib):
     # before anything is enqueued
     big = (ctypes.c_int * 4)(0, 2, 2, 15)
     assert f(fake, fake, fake, fake, None, fake, 0, big, 3, 256, 256, 128, None, 0, None) == 3
+    # the binding's sizing (the largest per-expert wq_workspace_size) is exactly what the
+    # entry checks: one byte less fails the check, that size passes it (then: no device)
+    need = max(lib.wq_workspace_size(2, m, 256, 256, 128) for m in (2, 13))
+    assert f(fake, fake, fake, fake, None, fake, 0, big, 3, 256, 256, 128, fake, need - 1, None) == 3
+    import torch
+    if not torch.cuda.is_available():  # with a GPU present this call would launch on fake pointers
+        assert f(fake, fake, fake, fake, None, fake, 0, big, 3, 256, 256, 128, fake, need, None) in (4, 5)
 
 
 def test_swiglu_pair_entry_checks(lib):
