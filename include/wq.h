@@ -204,7 +204,9 @@ int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, co
  *                 stacked, expert-major.
  *   S, delta      experts x [G][N] device (delta NULL: symmetric).
  *   expert_offsets HOST int array of experts + 1 entries, offsets[0] == 0,
- *                 non-decreasing; experts in 1..64.
+ *                 non-decreasing; experts in 1..64.  Read at the call and
+ *                 passed by value in the launch parameters: a CUDA graph that
+ *                 captures the call replays the offsets it was captured with.
  *   workspace     the largest wq_workspace_size(variant, tokens of one
  *                 expert, N, K, group_size) over the experts (0 when every
  *                 expert has <= 8 tokens).
