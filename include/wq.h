@@ -119,7 +119,8 @@ int wq_pack_w4a8(const uint8_t* q, const void* scale_signed, uint32_t* Bpacked, 
  *   scale_gate, zero_gate, scale_up, zero_up   [G][N] fp16 device.
  *   Bpacked                K*2N/8 uint32 device, output.
  *   S, delta               [G][2N] fp16 / fp32 device, outputs.
- * N must be a multiple of 64 (so that 2N is a multiple of 128).
+ * N must be a multiple of 64 (so that 2N is a multiple of 128), else
+ * WQ_ERR_UNSUPPORTED_SHAPE.
  */
 int wq_pack_w4a16_pair(const uint8_t* q_gate, const void* scale_gate, const void* zero_gate, const uint8_t* q_up,
                        const void* scale_up, const void* zero_up, uint32_t* Bpacked, void* S, float* delta, int K,
@@ -180,7 +181,8 @@ int wq_gemm_w4a8(const int8_t* Xq, const float* x_scale, const uint32_t* Bpacked
  *   X        [M][K] fp16/bf16 device.
  *   Bpacked, S, delta: from wq_pack_w4a16_pair (2N columns).
  *   Y        [M][N] device.
- *   N        the width of each projection (a multiple of 64).
+ *   N        the width of each projection (a multiple of 64, else
+ *            WQ_ERR_UNSUPPORTED_SHAPE).
  *   workspace  wq_workspace_size(WQ_VARIANT_W4A16_SWIGLU (delta given) or
  *            WQ_VARIANT_W4A16_SWIGLU_SYM, M, N, K, group_size) bytes: 0 when
  *            M <= 8 and the weight-streaming kernel takes the problem (one
