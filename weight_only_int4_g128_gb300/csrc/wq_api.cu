@@ -306,9 +306,11 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   if (plan.gemv) {
     // decode W4A8 with at most 8 tokens: the weight-streaming kernel reads the
     // int8 rows (fp16 rows are first quantized per token into the workspace)
-    // and applies the per-token scale at its store
+    // and applies the per-token scale at its store -- when its plan keeps one
+    // wave of two CTAs per SM; otherwise (long K segments whose activation
+    // tile does not fit) the e4m3 decode kernel below is faster
     int gv_splits = 0, gv_kbps = 0;
-    if (wq::gemv_plan(M, N, K, gs, corr, &gv_splits, &gv_kbps)) {
+    if (wq::gemv_plan(M, N, K, gs, corr, &gv_splits, &gv_kbps) && (N / 128) * gv_splits <= 2 * wq::kNumSMs) {
       const void* xq = X;
       if (quant_in) {
         int8_t* x8q = reinterpret_cast<int8_t*>(wsb + plan.off_x8);  // M * K bytes <= the e4m3 rows' room
