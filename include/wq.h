@@ -275,9 +275,10 @@ int wq_gemm_w4a8_asym(const int8_t* Xq, const float* x_scale, const uint32_t* Bp
  * clamp(round_half_even(RN32(X / x_scale)), -127, 127) are exactly those of
  * wq_quantize_per_token; Y is then that of wq_gemm_w4a8_asym (delta given) or
  * wq_gemm_w4a8 (delta NULL), bit for bit.  The quantization is the GEMM's own
- * activation pre-pass: for M 9..16 it splits the codes into e4m3 components
- * on the way (the codes are never written out), for M <= 8 it writes them to
- * the workspace for the weight-streaming kernel, for larger M as fp16.
+ * activation pre-pass: for the e4m3 decode kernel (M <= 16) it splits the
+ * codes into e4m3 components on the way (the codes are never written out),
+ * for the weight-streaming kernel (M <= 8, when its plan keeps one wave) it
+ * writes them to the workspace, for larger M as fp16.
  *   X        [M][K] fp16 device.
  *   x_scale  [M] fp32 device, output: the per-token scales.
  *   Bpacked, S, delta: from wq_pack_w4a16 (zero-point weights; delta may be
