@@ -1,15 +1,22 @@
 #!/usr/bin/env python
-"""Benchmark of the W4A16 group-quantized INT4-weight GEMM on GB300.
+"""Benchmark of the group-quantized INT4-weight GEMM (W4A16 / W4A8) on GB300.
 
-Default workload: the decode GEMV shapes, M in {1, 4, 16} x N in {4096, 11008},
-K = 4096, group 128, asymmetric weights, fp16 activations and output.  One
-"step" runs all six GEMMs (each on its own resident copy of the packed
-weights); the weight copies rotate over >3x the L2 size so every GEMM reads its
-weights from HBM.  The metric is weight GB/s (codes + fp16 scales + fp32 delta
-per second) for the whole job; TFLOPS is reported beside it.
+Default workload ("sweep"): every shape of the five configurations in one run.
+  c0  W4A16 asym M16 K256 N256 g128 fp16 (a launch-latency case)
+  c1  W4A16 asym decode M{1,4,16} x N{4096,11008}, K4096 (weight-bandwidth bound)
+  c2  W4A16 asym batched M{64,128,256}, K = N = 8192, g128 and per-channel
+  c3  W4A16 asym prefill, bf16 activations: M4096 K5120 N17408 and M4096 K17408 N5120
+  c4  W4A8 per-token int8 activations, folded signed scales, M{16,256,2048} K5120 N17408
+One "step" runs all 18 GEMMs once.  Each shape has its own resident copies of the
+packed weights, enough of them to span more than twice the L2 size, and a step
+uses the next copy.  `value` is the c3 prefill rate in TFLOP/s: 2*M*N*K of the c3
+calls over their device time inside the K timed steps.  `per_shape` gives every
+shape's TFLOP/s and weight GB/s, each the median of 20 windows of >= 50 ms of
+CUDA-graph replays.  `roofline` is the prefill kernel against the dense bf16
+tensor peak; `rooflines` holds each regime's kernel against its own bound.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wq|reference]
-                    [--workload c1|c0|c2|c3|c4|moe|moe8|swiglu]
+                    [--workload sweep|c0|c1|c2|c3|c4|moe|moe8|swiglu]
 
 --impl reference times the CPU oracle (plain C, fp64, naive loops) on a bounded
 sample of the same workload.  Under torchrun each rank runs an independent
@@ -19,7 +26,9 @@ line.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -38,7 +47,10 @@ import synth  # noqa: E402
 METRIC = "W4A16 GEMM TFLOPS & weight GB/s vs M on 1 GB300; % of HBM / tensor-core roofline"
 L2_BYTES = 129 * 2 ** 20
 PEAK_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SWEEP = ("c0", "c1", "c2", "c3", "c4")
+HEADLINE = "c3"
 WORKLOAD_NAMES = {
+    "sweep": "sweep of c0-c4 (18 GEMM shapes), headline c3 prefill",
     "c0": "W4A16 asym M16 K256 N256 g128 fp16",
     "c1": "W4A16 asym decode GEMV M{1,4,16} x N{4096,11008} K4096 g128 fp16",
     "c2": "W4A16 asym batched M{64,128,256} K8192 N8192 g128 and per-channel fp16",
@@ -48,9 +60,34 @@ WORKLOAD_NAMES = {
     "moe8": "W4A8 zero-point grouped (mixture of experts): 16 int8 per-token rows top-1 over 8 experts, K256 N7168 g128",
     "swiglu": "W4A16 asym fused SwiGLU gate/up pair, decode M{1,4} K4096 N11008 (x2 projections) g128 fp16",
 }
+# The unit of a single-configuration workload's `value`: TFLOP/s where the tensor cores
+# bound most of its shapes, weight GB/s where the weight stream does.
+TENSOR_CONFIGS = ("c2", "c3", "c4")
+SHAPE_KEYS = ("M", "K", "N", "group_size", "a_dtype", "a_std", "mode")
 
 
 # ----------------------------------------------------------------------------- helpers
+def workload_shapes(workload: str):
+    """(seed, shape) pairs of a workload; each shape carries its configuration name."""
+    cfgs = SWEEP if workload == "sweep" else (workload,)
+    out = []
+    for c in cfgs:
+        for seed, s in synth.shapes(c):
+            d = dict(s)
+            d["cfg"] = c
+            out.append((seed, d))
+    return out
+
+
+def inputs_of(seed, s, **kw):
+    return synth.make_inputs(seed, **{k: s[k] for k in SHAPE_KEYS}, **kw)
+
+
+def label(s) -> str:
+    t = f"{s.get('cfg', '?')} M{s['M']} K{s['K']} N{s['N']}"
+    return t + (" per-channel" if s["group_size"] in (-1, s["K"]) else "")
+
+
 def weight_bytes(s) -> int:
     K, N = s["K"], s["N"]
     G = synth.num_groups(K, s["group_size"])
@@ -65,40 +102,55 @@ def io_bytes(s) -> int:
     return s["M"] * s["K"] * xb + s["M"] * s["N"] * 2 + (s["M"] * 4 if s["mode"] == "w4a8" else 0)
 
 
-def kernel_launches(s) -> int:
-    """Kernels one GEMM call enqueues (the decode kernel is a single launch for W4A16;
-    the large-M path adds one correction pre-pass (group sums and delta columns), W4A8
-    an activation pre-pass)."""
-    if s["mode"] == "w4a8":
-        return 2
-    return 1 if s["M"] <= 16 else 2
-
-
 def flops(s) -> int:
     return 2 * s["M"] * s["N"] * s["K"]
 
 
-def load_traffic(shapes):
-    """DRAM bytes of one launch of the decode kernel from the committed ncu capture
-    (profiles/traffic.json), or None when the kernel's sources changed since the
-    capture or the captured shape is not part of this workload."""
-    import hashlib
+def kernels_for(s):
+    """The kernels one GEMM call of this shape launches, as the library dispatches it:
+    W4A16 up to 8 tokens the weight-streaming kernel, 9..16 tokens the tcgen05 decode
+    kernel, beyond that the correction pre-pass and the large-M kernel; W4A8 with
+    9..16 tokens the activation pre-pass and the e4m3 decode kernel, beyond that the
+    int8 -> fp16 pre-pass and the large-M kernel."""
+    M = s["M"]
+    if s["mode"] == "w4a8":
+        return ["decode_prep_kernel", "decode_kernel"] if M <= 16 else ["i8_to_f16_kernel", "gemm_kernel"]
+    if M <= 8:
+        return ["gemv_kernel"]
+    if M <= 16:
+        return ["decode16_kernel"]
+    return ["corr_prep_kernel", "gemm_kernel"]
+
+
+def kernel_launches(s) -> int:
+    return len(kernels_for(s))
+
+
+def source_hash(sources) -> str:
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(ROOT, src), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def load_traffic(kernel: str, shape):
+    """DRAM bytes of one launch of `kernel` on `shape` from a committed ncu capture
+    (profiles/traffic.json), or None when no record matches or the kernel's sources
+    changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        rec = json.load(f)
-    h = hashlib.sha256()
-    for src in rec["sources"]:
-        with open(os.path.join(ROOT, src), "rb") as f:
-            h.update(f.read())
-    if h.hexdigest() != rec["source_sha256"]:
-        return None
-    sh = rec["shape"]
-    if not any(s["M"] == sh["M"] and s["K"] == sh["K"] and s["N"] == sh["N"] and s["group_size"] == sh["group_size"]
-               and s["mode"] == "w4a16" for _, s in shapes):
-        return None
-    return rec
+        recs = json.load(f)
+    for rec in recs.get("records", []):
+        sh = rec["shape"]
+        if rec["kernel"] != kernel or any(sh[k] != shape[k] for k in ("M", "K", "N", "group_size")):
+            continue
+        if source_hash(rec["sources"]) != rec["source_sha256"]:
+            return None
+        return rec
+    return None
 
 
 def load_peaks():
@@ -137,11 +189,14 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self) -> float:
+        return time.perf_counter()
 
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -149,9 +204,16 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
+
+    def summary(self, t0: float = None, t1: float = None):
+        """Median SM clock, max clock and the throttle reasons seen between t0 and t1."""
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        for ts, line in self.lines:
+            if (t0 is not None and ts < t0) or (t1 is not None and ts > t1):
+                continue
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -223,68 +285,204 @@ def job_rate(ws: int, units_per_rank_step: float, ms_per_step: float, scale: flo
     return ws * units_per_rank_step / (ms_per_step * 1e-3) / scale
 
 
+def cpu_threads() -> int:
+    env = os.environ.get("OMP_NUM_THREADS")
+    if env and env.isdigit():
+        return int(env)
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def headline_unit(workload: str) -> str:
+    return "TFLOP/s" if workload == "sweep" or workload in TENSOR_CONFIGS else "GB/s"
+
+
 # ----------------------------------------------------------------------------- oracle arm
-def oracle_sample(shapes, budget_s: float, cols: int = 2048):
-    """Time the CPU oracle on column windows of every shape until budget_s has passed."""
-    import oracle
-    probs = []
-    for seed, s in shapes:
-        d = synth.make_inputs(seed, **s)
-        w = min(cols, s["N"])
+class OracleProblem:
+    """One shape's seeded inputs in the oracle's form, and its fp64 product on a column
+    window (the oracle as it stands: plain C, naive loops, OpenMP over rows)."""
+
+    def __init__(self, seed, s):
+        import oracle
+        self.s = s
+        d = inputs_of(seed, s)
+        self.q = d["q"]
+        if s["mode"] == "w4a8":
+            self.Xq, self.xs = oracle.quantize_per_token(d["A"])
+            self.qf, self.sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), s["group_size"])
+        else:
+            self.A = oracle.activations_to_double(d["A"], s["a_dtype"])
+            self.sb = oracle.half_bits(d["scale"])
+            self.zb = oracle.half_bits(d["zero"])
+
+    def run(self, c0: int, c1: int):
+        """Columns [c0, c1) of the product; returns (flops, weight bytes) of that window."""
+        import oracle
+        s = self.s
+        N = s["N"]
+        c0, c1 = c0 % N, c0 % N + min(c1 - c0, N)
+        c1 = min(c1, N)
+        if s["mode"] == "w4a8":
+            oracle.gemm_w4a8(self.Xq, self.xs, self.qf, self.sf, s["group_size"], cols=(c0, c1))
+        else:
+            oracle.gemm_asym_plain(self.A, self.q, self.sb, self.zb, s["group_size"], cols=(c0, c1))
+        w = c1 - c0
         G = synth.num_groups(s["K"], s["group_size"])
         wb = s["K"] * w // 2 + G * w * 2 + (G * w * 4 if s["mode"] == "w4a16" else 0)
-        probs.append((s, d, w, wb))
-    done_bytes = 0
-    done_flops = 0
+        return 2 * s["M"] * s["K"] * w, wb
+
+
+def oracle_rate(shapes, budget_s: float, cols: int):
+    """Run the oracle on successive column windows of every shape until budget_s has
+    passed; returns (TFLOP/s, weight GB/s, seconds, windows per shape)."""
+    probs = [OracleProblem(seed, s) for seed, s in shapes]
+    done_f = done_b = 0
     passes = 0
     t0 = time.perf_counter()
     while True:
-        for s, d, w, wb in probs:
-            if s["mode"] == "w4a8":
-                Xq, xs = oracle.quantize_per_token(d["A"])
-                qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), s["group_size"])
-                oracle.gemm_w4a8(Xq, xs, qf, sf, s["group_size"], cols=(0, w))
-            else:
-                A = oracle.activations_to_double(d["A"], s["a_dtype"])
-                oracle.gemm_asym_plain(A, d["q"], oracle.half_bits(d["scale"]),
-                                       oracle.half_bits(d["zero"]), s["group_size"], cols=(0, w))
-            done_bytes += wb
-            done_flops += 2 * s["M"] * s["K"] * w
+        for p in probs:
+            f, b = p.run(passes * cols, passes * cols + cols)
+            done_f += f
+            done_b += b
         passes += 1
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    sample = (f"{passes} pass(es) over the {len(probs)} shapes, columns [0, {cols}) of each, "
-              f"all rows and the full K, fp64 naive loops")
-    return done_bytes / el / 1e9, done_flops / el / 1e12, el, threads, sample
+    return done_f / el / 1e12, done_b / el / 1e9, el, passes
 
 
 def run_reference(args, shapes, ws, rank):
+    """The CPU oracle on the arm's own metric: every step computes one column window of
+    every shape of the headline configuration (the whole workload's, for a single
+    configuration) and the rate is counted over the K timed steps."""
     if rank != 0:
         return 0
-    budget = max(2.0, min(20.0, 4.0 * args.steps))
-    steps = []
-    for _ in range(args.warmup and 1):
-        oracle_sample(shapes, 0.5, cols=256)
-    gbs, tfl, el, threads, sample = oracle_sample(shapes, budget)
+    workload = getattr(args, "workload", "sweep")
+    unit = headline_unit(workload)
+    head = [(seed, s) for seed, s in shapes if s.get("cfg", workload) == HEADLINE] if workload == "sweep" else shapes
+    probs = [OracleProblem(seed, s) for seed, s in head]
+    cols = 64 if unit == "TFLOP/s" else 256
+    for i in range(args.warmup):
+        for p in probs:
+            p.run(i * 8, i * 8 + 8)
+    done_f = done_b = 0
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        for p in probs:
+            f, b = p.run(i * cols, i * cols + cols)
+            done_f += f
+            done_b += b
+    el = time.perf_counter() - t0
+    val = done_f / el / 1e12 if unit == "TFLOP/s" else done_b / el / 1e9
+    threads = cpu_threads()
+    sample = (f"{args.steps} steps, step i the columns [{cols} i, {cols} i + {cols}) of "
+              + ", ".join(label(p.s) for p in probs) + "; all rows and the full K, fp64 naive loops")
     line = {
-        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
-        "tflops": round(tfl, 9), "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": None, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
-        "config": {"workload": WORKLOAD_NAMES[args.workload], "sampled": True},
-        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads,
-                         "kind": "oracle", "sample": sample},
-        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
+        "impl": "reference", "metric": METRIC, "value": round(val, 9), "unit": unit,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * el / max(1, args.steps), 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+        "config": {"workload": WORKLOAD_NAMES.get(workload, workload), "sampled": True,
+                   "shapes": [label(p.s) for p in probs]},
+        "cpu_baseline": {"value": round(val, 9), "unit": unit, "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(val, 9), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
-    del steps
     print(json.dumps(line), flush=True)
     return 0
 
 
 # ----------------------------------------------------------------------------- GPU arm
+def setup_problem(torch, wq, dev, seed, s, min_rot_bytes: int, max_copies: int = 64):
+    """Pack one shape's seeded inputs on the device: the activations, enough copies of the
+    packed weights to span min_rot_bytes (so that consecutive calls read their weights
+    from HBM), the output and the GEMM workspace."""
+    d = inputs_of(seed, s)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    gs = s["group_size"]
+    if s["mode"] == "w4a8":
+        Bp, S = wq.pack_w4a8(cu(d["q"]), cu(d["scale"]), gs)
+        dl = None
+        Xq, xs = wq.quantize_per_token(cu(d["A"]))
+        X = (Xq, xs)
+    else:
+        Bp, S, dl = wq.pack_w4a16(cu(d["q"]), cu(d["scale"]), cu(d["zero"]), gs)
+        X = cu(d["A"].view(np.int16)).view(torch.bfloat16) if s["a_dtype"] == "bf16" else cu(d["A"])
+    wb = weight_bytes(s)
+    copies = min(max_copies, max(1, math.ceil(min_rot_bytes / wb) + 1))
+    w = [(Bp, S, dl)] + [(Bp.clone(), S.clone(), dl.clone() if dl is not None else None)
+                         for _ in range(copies - 1)]
+    variant = wq.VARIANT_W4A8 if s["mode"] == "w4a8" else wq.VARIANT_W4A16
+    need = wq.workspace_size(variant, s["M"], s["N"], s["K"], gs)
+    return {"s": s, "seed": seed, "w": w, "X": X,
+            "Y": torch.empty((s["M"], s["N"]), dtype=torch.float16, device=dev),
+            "ws": torch.zeros(max(need, 4096), dtype=torch.uint8, device=dev),
+            "A_host": d["A"] if s.get("cfg") == HEADLINE else None}
+
+
+def call(wq, p, r):
+    """One GEMM call of problem p on weight copy r (mod the copies it has)."""
+    s = p["s"]
+    Bp, S, dl = p["w"][r % len(p["w"])]
+    if s["mode"] == "w4a8":
+        return wq.gemm_w4a8(p["X"][0], p["X"][1], Bp, S, s["group_size"], out=p["Y"], workspace=p["ws"])
+    return wq.gemm_w4a16(p["X"], Bp, S, dl, s["group_size"], out=p["Y"], workspace=p["ws"])
+
+
+def time_shape(torch, wq, stream, p, windows: int, min_window_ms: float):
+    """Per-call device time of one shape: a CUDA graph of consecutive calls on rotating
+    weight copies, replayed in `windows` windows of at least min_window_ms each;
+    returns (median, min, max) microseconds per call over the windows."""
+    per = max(8, 2 * len(p["w"]))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(per):
+                call(wq, p, j)
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    reps = max(1, math.ceil(min_window_ms / max(1e-3, e0.elapsed_time(e1))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(windows)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+    torch.cuda.synchronize()
+    us = sorted(a.elapsed_time(b) * 1e3 / (reps * per) for a, b in evs)
+    del g
+    return statistics.median(us), us[0], us[-1], reps * per
+
+
+def regime_roofline(rows, kernel, bound, peaks, peaks_src, what):
+    """Aggregate fraction of a kernel over its shapes: algorithmic bytes (bound "hbm") or
+    FLOPs (bound "tensor") over the summed per-call times."""
+    sel = [r for r in rows if r["kernel"] == kernel and r["_use"](bound)]
+    if not sel:
+        return None
+    t = sum(r["us"] for r in sel) * 1e-6
+    if bound == "hbm":
+        ach = sum(r["_alg"] for r in sel) / t / 1e9
+        pk = peaks["hbm_gbs"]
+        src = f"{peaks_src} hbm_gbs (copy)"
+        unit = "GB/s"
+    else:
+        ach = sum(r["_flops"] for r in sel) / t / 1e12
+        pk = peaks["bf16_tflops"]
+        src = f"{peaks_src} bf16_tflops (burst, cuBLAS bf16; fp16 runs at the bf16 rate)"
+        unit = "TFLOP/s"
+    return {"bound": bound, "kernel": kernel, "achieved": round(ach, 1), "peak": pk, "unit": unit,
+            "frac": round(ach / pk, 4), "peak_source": src, "shapes": [r["shape"] for r in sel], "what": what}
+
+
 def run_gpu(args, shapes, ws, rank, local):
     import torch
 
@@ -299,241 +497,219 @@ def run_gpu(args, shapes, ws, rank, local):
     if not wq.device_supported(local):
         raise RuntimeError("not an sm_103 device")
     # The weights are packed once before the timed region and never written again, so
-    # the decode kernel may start copying them before the preceding GEMM finishes.
+    # the decode kernels may start copying them before the preceding GEMM finishes.
     wq.set_weight_prefetch(True)
+    workload = args.workload
+    unit = headline_unit(workload)
 
-    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    # --- problems: inputs resident in HBM, weights replicated to rotate past L2
-    probs = []
-    set_bytes = 0
-    for seed, s in shapes:
-        d = synth.make_inputs(seed, **s)
-        gs = s["group_size"]
-        if s["mode"] == "w4a8":
-            Bp, S = wq.pack_w4a8(cu(d["q"]), cu(d["scale"]), gs)
-            dl = None
-            X16 = cu(d["A"])
-            Xq, xs = wq.quantize_per_token(X16)
-            X = (Xq, xs)
-        else:
-            Bp, S, dl = wq.pack_w4a16(cu(d["q"]), cu(d["scale"]), cu(d["zero"]), gs)
-            if s["a_dtype"] == "bf16":
-                X = cu(d["A"].view(np.int16)).view(torch.bfloat16)
-            else:
-                X = cu(d["A"])
-        probs.append({"s": s, "w": [(Bp, S, dl)], "X": X, "A_host": d["A"]})
-        set_bytes += weight_bytes(s)
-        del d
-    reps = max(1, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
-    for p in probs:
-        Bp, S, dl = p["w"][0]
-        for _ in range(reps - 1):
-            p["w"].append((Bp.clone(), S.clone(), dl.clone() if dl is not None else None))
-    for p in probs:
-        s = p["s"]
-        p["Y"] = torch.empty((s["M"], s["N"]), dtype=torch.float16, device=dev)
-        variant = wq.VARIANT_W4A8 if s["mode"] == "w4a8" else wq.VARIANT_W4A16
-        need = wq.workspace_size(variant, s["M"], s["N"], s["K"], s["group_size"])
-        p["ws"] = torch.zeros(max(need, 4096), dtype=torch.uint8, device=dev)
-
-    def call(p, r, out=None, X=None):
-        s = p["s"]
-        Bp, S, dl = p["w"][r]
-        X = p["X"] if X is None else X
-        if s["mode"] == "w4a8":
-            return wq.gemm_w4a8(X[0], X[1], Bp, S, s["group_size"], out=p["Y"] if out is None else out,
-                                workspace=p["ws"])
-        return wq.gemm_w4a16(X, Bp, S, dl, s["group_size"], out=p["Y"] if out is None else out,
-                             workspace=p["ws"])
-
-    # eager warm-up (sets kernel attributes, checks the calls work)
-    for p in probs:
-        for r in range(reps):
-            call(p, r)
+    probs = [setup_problem(torch, wq, dev, seed, s, 2 * L2_BYTES) for seed, s in shapes]
+    cfg_order = [c for c in SWEEP if any(p["s"]["cfg"] == c for p in probs)]
+    groups = {c: [p for p in probs if p["s"]["cfg"] == c] for c in cfg_order}
+    head_cfg = HEADLINE if workload == "sweep" else workload
     torch.cuda.synchronize()
 
-    # --- one CUDA graph per weight replica: a whole step (all shapes)
     stream = torch.cuda.Stream(device=dev)
-    def step(r):
-        for p in probs:
-            call(p, r)
 
-    spg = STEPS_PER_GRAPH
-    graphs, graphs1 = build_step_graphs(torch, stream, reps, step, spg)
-    torch.cuda.synchronize()
-
-    launches_per_step = sum(kernel_launches(p["s"]) for p in probs)
+    def step(r, evs=None):
+        for i, c in enumerate(cfg_order):
+            if evs is not None:
+                evs[i].record(stream)
+            for p in groups[c]:
+                call(wq, p, r)
+        if evs is not None:
+            evs[-1].record(stream)
 
     with torch.cuda.stream(stream):
-        replay_steps(graphs, graphs1, args.warmup, spg)
+        for r in range(args.warmup):
+            step(r)
     torch.cuda.synchronize()
 
-    # --- timed region
+    # --- timed region: exactly K steps, one event at each configuration boundary
     clocks = ClockSampler(local)
-    if ws > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_timed0 = clocks.mark()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(cfg_order) + 1)] for _ in range(args.steps)]
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        replay_steps(graphs, graphs1, args.steps, spg)
-        ev1.record(stream)
+        for t in range(args.steps):
+            step(args.warmup + t, evs[t])
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
-    ms = max_over_ranks(ev0.elapsed_time(ev1), ws, dev)
-    ms_per_step = ms / args.steps
-    step_wbytes = sum(weight_bytes(p["s"]) for p in probs)
-    step_flops = sum(flops(p["s"]) for p in probs)
-    value = job_rate(ws, step_wbytes, ms_per_step)
-    tflops = job_rate(ws, step_flops, ms_per_step, 1e12)
-
+    t_timed1 = clocks.mark()
+    ms_total = max_over_ranks(evs[0][0].elapsed_time(evs[-1][-1]), ws, dev)
+    ms_per_step = ms_total / args.steps
+    cfg_ms = {c: sum(e[i].elapsed_time(e[i + 1]) for e in evs) / args.steps for i, c in enumerate(cfg_order)}
+    cfg_ms = {c: max_over_ranks(v, ws, dev) for c, v in cfg_ms.items()}
+    head_probs = groups[head_cfg]
+    head_flops = sum(flops(p["s"]) for p in head_probs)
+    head_wb = sum(weight_bytes(p["s"]) for p in head_probs)
+    if unit == "TFLOP/s":
+        value = job_rate(ws, head_flops, cfg_ms[head_cfg], 1e12)
+    else:
+        value = job_rate(ws, head_wb, cfg_ms[head_cfg])
+    launches_per_step = sum(kernel_launches(p["s"]) for p in probs)
     peaks, peaks_src = load_peaks()
+
     if args.quick:
+        clocks.stop()
         if rank == 0:
-            print(json.dumps({"metric": METRIC, "value": round(value, 2), "unit": "GB/s",
-                              "tflops": round(tflops, 3), "ms_per_step": round(ms_per_step, 6),
-                              "quick": True, "clocks": clk}), flush=True)
+            print(json.dumps({"metric": METRIC, "value": round(value, 3), "unit": unit,
+                              "ms_per_step": round(ms_per_step, 6), "quick": True,
+                              "config_ms_per_step": {c: round(v, 6) for c, v in cfg_ms.items()},
+                              "clocks": clocks.summary(t_timed0, t_timed1)}), flush=True)
         return 0
 
-    # --- per-shape launch timing of the GEMM call (graphs of `per` calls on rotating weights)
-    per = 2 * reps
-    shape_rows = []
-    tot_alg = 0
-    tot_ms = 0.0
+    # --- per-shape device time: median of 20 windows of >= 50 ms of graph replays
+    rows = []
     for p in probs:
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for j in range(per):
-                    call(p, j % reps)
-            for _ in range(3):
-                g.replay()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            nrep = 20
-            for _ in range(nrep):
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) * 1e3 / (nrep * per)
         s = p["s"]
+        us, us_lo, us_hi, calls = time_shape(torch, wq, stream, p, args.windows, args.window_ms)
         alg = weight_bytes(s) + io_bytes(s)
-        tot_alg += alg
-        tot_ms += us * 1e-3
-        shape_rows.append({"M": s["M"], "N": s["N"], "K": s["K"], "us": round(us, 3),
-                           "weight_GBps": round(weight_bytes(s) / (us * 1e-6) / 1e9, 1),
-                           "tflops": round(flops(s) / (us * 1e-6) / 1e12, 3)})
+        t = us * 1e-6
+        t_hbm = alg / (peaks["hbm_gbs"] * 1e9)
+        t_tc = flops(s) / (peaks["bf16_tflops"] * 1e12)
+        kern = kernels_for(s)[-1]
+        row = {"shape": label(s), "config": s["cfg"], "M": s["M"], "K": s["K"], "N": s["N"],
+               "group_size": s["group_size"], "kernels": kernels_for(s), "kernel": kern,
+               "us": round(us, 3), "us_min": round(us_lo, 3), "us_max": round(us_hi, 3),
+               "calls_per_window": calls, "windows": args.windows,
+               "tflops": round(flops(s) / t / 1e12, 3),
+               "weight_GBps": round(weight_bytes(s) / t / 1e9, 1),
+               "alg_GBps": round(alg / t / 1e9, 1),
+               "frac_hbm": round(alg / t / 1e9 / peaks["hbm_gbs"], 4),
+               "frac_tensor": round(flops(s) / t / 1e12 / peaks["bf16_tflops"], 4),
+               "bound": "latency" if s["cfg"] == "c0" else ("hbm" if t_hbm >= t_tc else "tensor"),
+               "copies": len(p["w"])}
+        row["_alg"], row["_flops"] = alg, flops(s)
+        rows.append(row)
+    t_shapes1 = clocks.mark()
 
-    traffic = load_traffic(shapes)
-    tot_flops = sum(flops(p["s"]) for p in probs)
-    # Which roofline bounds the workload: its bytes at the measured HBM copy rate
-    # against its FLOPs at the measured dense bf16/fp16 rate (fp16 runs at the bf16
-    # rate on this part; W4A8 is computed in fp16 or e4m3, never at an int8 rate).
-    # The per-shape loops run for seconds, so the sustained tensor figure applies.
-    t_hbm = tot_alg / (peaks["hbm_gbs"] * 1e9)
-    t_tc = tot_flops / (peaks["bf16_tflops_sustained"] * 1e12)
-    if t_hbm >= t_tc:
-        achieved = tot_alg / (tot_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(achieved / peaks["hbm_gbs"], 4),
-                    "peak_source": f"{peaks_src} (MEASURED_PEAKS.json hbm_gbs, copy)"
-                    if peaks_src == "measured" else "fallback 6.8 TB/s"}
-    else:
-        achieved = tot_flops / (tot_ms * 1e-3) / 1e12
-        pk = peaks["bf16_tflops_sustained"]
+    def use(r, b):
+        return r["bound"] == b or (b == "hbm" and r["M"] <= 16 and r["config"] != "c0")
+    for r in rows:
+        r["_use"] = (lambda b, r=r: use(r, b))
+    rooflines = {}
+    for name, kern, bound, what in [
+            ("decode_w4a16_le8", "gemv_kernel", "hbm", "W4A16 decode, M <= 8 (c1)"),
+            ("decode_w4a16_9to16", "decode16_kernel", "hbm", "W4A16 decode, M 9..16 (c1 M16)"),
+            ("decode_w4a8_9to16", "decode_kernel", "hbm", "W4A8 decode, M 16 (c4 M16)"),
+            ("large_m_tensor", "gemm_kernel", "tensor", "large M: c2 M128/M256, c3, c4 M256/M2048")]:
+        rl = regime_roofline(rows, kern, bound, peaks, peaks_src, what)
+        if rl:
+            rooflines[name] = rl
+    # the headline configuration's own rows
+    for c in cfg_order:
+        crow = [r for r in rows if r["config"] == c]
+        t = sum(r["us"] for r in crow) * 1e-6
+        rooflines.setdefault("per_config", {})[c] = {
+            "tflops": round(sum(r["_flops"] for r in crow) / t / 1e12, 3),
+            "weight_GBps": round(sum(weight_bytes(p["s"]) for p in groups[c]) / t / 1e9, 1),
+            "us_per_step": round(t * 1e6, 3)}
+    for r in rows:
+        del r["_alg"], r["_flops"], r["_use"]
+
+    # --- the headline kernel's roofline, from the timed steps themselves
+    hk = kernels_for(head_probs[0]["s"])[-1]
+    n_launch = len(head_probs)
+    if unit == "TFLOP/s":
+        achieved = head_flops / (cfg_ms[head_cfg] * 1e-3) / 1e12
+        pk = peaks["bf16_tflops"]
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": pk, "unit": "TFLOP/s",
                     "frac": round(achieved / pk, 4),
-                    "frac_of_burst": round(achieved / peaks["bf16_tflops"], 4),
-                    "peak_source": f"{peaks_src} (MEASURED_PEAKS.json bf16_tflops_sustained, cuBLAS bf16)"
-                    if peaks_src == "measured" else "fallback 1.7 PFLOP/s sustained"}
+                    "peak_source": f"{peaks_src} bf16_tflops (burst, cuBLAS bf16 8192^3)"}
+    else:
+        alg = sum(weight_bytes(p["s"]) + io_bytes(p["s"]) for p in head_probs)
+        achieved = alg / (cfg_ms[head_cfg] * 1e-3) / 1e9
+        pk = peaks["hbm_gbs"]
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk, "unit": "GB/s",
+                    "frac": round(achieved / pk, 4), "peak_source": f"{peaks_src} hbm_gbs (copy)"}
+    tr = load_traffic(hk, head_probs[0]["s"])
     roofline.update({
-        "traffic": traffic["dram_bytes_per_launch"] if traffic else None,
-        "kernel": "wq::gemv_kernel (W4A16, M <= 8) / wq::decode16_kernel (M 9..16) / wq::gemm_kernel; time per GEMM call",
-        "traffic_launch": ({"shape": traffic["shape"], "algorithmic_bytes": traffic["algorithmic_bytes_per_launch"],
-                            "source": traffic["capture"]} if traffic else None),
-        "per_shape": shape_rows})
+        "kernel": f"wq::{hk}",
+        "launches_per_step": n_launch,
+        "time": (f"device time of the {head_cfg} calls inside the {args.steps} timed steps "
+                 f"(CUDA events on the launching stream), {1e3 * cfg_ms[head_cfg] / n_launch:.1f} us per call"
+                 + (" including its pre-pass launch" if len(kernels_for(head_probs[0]['s'])) > 1 else "")),
+        "traffic": tr["dram_bytes_per_launch"] if tr else None,
+        "traffic_launch": ({"shape": tr["shape"], "algorithmic_bytes": tr["algorithmic_bytes_per_launch"],
+                            "capture": tr["capture"]} if tr else None)})
 
-    # --- end to end through the public API.  The step's activations (every shape) sit in
-    # one pinned host buffer that one cudaMemcpyAsync copies in; each GEMM call reads its
-    # view of the device copy (W4A8 shapes: the fp16 rows, quantized per token inside the
-    # call by gemm_w4a8_fp16) and writes its view of one device output buffer, which one
-    # copy brings back to pinned host memory; synchronised every step.
-    e2e_steps = max(20, min(200, args.steps // 50))
-    sizes_x = [p["s"]["M"] * p["s"]["K"] for p in probs]
-    sizes_y = [p["s"]["M"] * p["s"]["N"] for p in probs]
-    hx_all = torch.empty(sum(sizes_x), dtype=torch.int16).pin_memory()
-    hy_all = torch.empty(sum(sizes_y), dtype=torch.float16).pin_memory()
-    dx_all = torch.empty_like(hx_all, device=dev)
-    dy_all = torch.empty_like(hy_all, device=dev)
-    xv, yv = [], []
-    ox = oy = 0
-    for p, nx, ny in zip(probs, sizes_x, sizes_y):
-        s = p["s"]
-        hx_all[ox:ox + nx].copy_(torch.from_numpy(np.ascontiguousarray(p["A_host"]).view(np.int16).reshape(-1)))
-        x = dx_all[ox:ox + nx].view(s["M"], s["K"])
-        xv.append(x.view(torch.bfloat16) if s["a_dtype"] == "bf16" else x.view(torch.float16))
-        yv.append(dy_all[oy:oy + ny].view(s["M"], s["N"]))
-        p["xs"] = torch.empty((s["M"],), dtype=torch.float32, device=dev)
-        ox += nx
-        oy += ny
-    h2d = hx_all.numel() * hx_all.element_size()
-    d2h = hy_all.numel() * hy_all.element_size()
-
-    def e2e_call(j, p, r):
-        s = p["s"]
-        Bp, S, dl = p["w"][r]
-        if s["mode"] == "w4a8":
-            wq.gemm_w4a8_fp16(xv[j], Bp, S, None, s["group_size"], out=yv[j], x_scale=p["xs"], workspace=p["ws"])
-        else:
-            wq.gemm_w4a16(xv[j], Bp, S, dl, s["group_size"], out=yv[j], workspace=p["ws"])
-
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        for i in range(3 + e2e_steps):
-            if i == 3:
-                torch.cuda.synchronize()
-                t0 = time.perf_counter()
-            dx_all.copy_(hx_all, non_blocking=True)
-            for j, p in enumerate(probs):
-                e2e_call(j, p, i % reps)
-            hy_all.copy_(dy_all, non_blocking=True)
-            stream.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_val = ws * step_wbytes / e2e_s / 1e9
+    # --- end to end through the host-buffer C-ABI entry: per step, every headline call
+    # copies its activations in from pinned host memory, runs and copies Y back out;
+    # synchronised each step
+    e2e = None
+    if all(p["s"]["mode"] == "w4a16" for p in head_probs):
+        hx, hy, hws = [], [], []
+        for p in head_probs:
+            s = p["s"]
+            a = torch.from_numpy(np.ascontiguousarray(p["A_host"] if p["A_host"] is not None
+                                                      else inputs_of(p["seed"], s)["A"]).view(np.int16))
+            hx.append((a.view(torch.bfloat16) if s["a_dtype"] == "bf16" else a.view(torch.float16)).pin_memory())
+            hy.append(torch.empty((s["M"], s["N"]), dtype=torch.float16).pin_memory())
+            need = int(wq.load_library().wq_host_workspace_size(wq.VARIANT_W4A16, s["M"], s["N"], s["K"],
+                                                                 s["group_size"], wq.DTYPE_F16))
+            hws.append(torch.empty(need, dtype=torch.uint8, device=dev))
+        n_e2e = max(10, args.steps)
+        with torch.cuda.stream(stream):
+            for i in range(2 + n_e2e):
+                if i == 2:
+                    torch.cuda.synchronize()
+                    t0 = time.perf_counter()
+                for j, p in enumerate(head_probs):
+                    Bp, S, dl = p["w"][i % len(p["w"])]
+                    wq.gemm_w4a16_host(hx[j], Bp, S, dl, p["s"]["group_size"], out=hy[j], workspace=hws[j])
+                stream.synchronize()
+        e2e_s = (time.perf_counter() - t0) / n_e2e
+        e2e_val = (job_rate(ws, head_flops, e2e_s * 1e3, 1e12) if unit == "TFLOP/s"
+                   else job_rate(ws, head_wb, e2e_s * 1e3))
+        e2e = {"value": round(e2e_val, 3), "unit": unit,
+               "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hx),
+               "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in hy),
+               "api": "wq_gemm_w4a16_host (C ABI, host buffers) through its Python binding",
+               "note": f"{n_e2e} steps of the {head_cfg} calls, wall clock, each call copying X in from pinned "
+                       "host memory and Y back, the stream synchronised every step"}
+    t_end = clocks.mark()
+    clocks.stop()
+    clk = clocks.summary(t_timed0, t_end)
+    clk["timed_steps_samples"] = clocks.summary(t_timed0, t_timed1)["samples"]
 
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "tflops": round(tflops, 3),
+        "metric": METRIC, "value": round(value, 3), "unit": unit,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 6), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
-        "config": {"workload": WORKLOAD_NAMES[args.workload],
-                   "shapes": [f"M{p['s']['M']} K{p['s']['K']} N{p['s']['N']}" for p in probs],
-                   "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB "
-                         f"> 3x L2); activations resident",
+        "vs_baseline": None, "dtype": "bf16" if head_cfg == "c3" else "f16",
+        "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+        "config": {"workload": WORKLOAD_NAMES[workload], "headline": f"{head_cfg}: {WORKLOAD_NAMES[head_cfg]}",
+                   "value_is": (f"{unit} of the {head_cfg} calls over their device time inside the timed steps"),
+                   "config_ms_per_step": {c: round(v, 6) for c, v in cfg_ms.items()},
+                   "shapes": [label(p["s"]) for p in probs],
+                   "l2": ("every shape rotates over copies of its packed weights spanning > 2x L2 (c0: 64 "
+                          "copies of 36 KB, L2-resident: a launch-latency case); a step reads ~1 GB of "
+                          "distinct weights, activations and outputs, so no shape finds its weights in L2"),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "graph": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps, the weight copy rotating step by step",
-                   "launch": "programmatic dependent launch, weight prefetch enabled"},
+                   "launch": "eager launches, programmatic dependent launch, weight prefetch enabled; "
+                             "per-shape rows: CUDA graphs of consecutive calls"},
         "roofline": roofline,
+        "rooflines": rooflines,
+        "per_shape": rows,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
-        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "note": "every step: the step's activations copied from one pinned host buffer, the "
-                        "GEMM calls of the public API on the device copy (gemm_w4a16; W4A8: "
-                        "gemm_w4a8_fp16 quantizing inside), the outputs copied back to pinned host "
-                        "memory, synchronised"},
     }
+    if e2e:
+        line["e2e"] = e2e
     if rank == 0 and not args.no_cpu_baseline:
-        gbs, tfl, el, threads, sample = oracle_sample(shapes, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads,
-                                "kind": "oracle", "sample": sample, "seconds": round(el, 2)}
+        head_shapes = [(p["seed"], p["s"]) for p in head_probs]
+        cols = 64 if unit == "TFLOP/s" else 256
+        tfl, gbs, el, passes = oracle_rate(head_shapes, args.cpu_seconds, cols)
+        line["cpu_baseline"] = {
+            "value": round(tfl if unit == "TFLOP/s" else gbs, 9), "unit": unit, "cores": cpu_threads(),
+            "kind": "oracle", "seconds": round(el, 2),
+            "sample": (f"{passes} column window(s) of {cols} columns of each of "
+                       + ", ".join(label(s) for _, s in head_shapes) + "; all rows, full K, fp64 naive loops")}
     if ws > 1:
         torch.distributed.destroy_process_group()
     if rank == 0:
@@ -650,7 +826,8 @@ def run_moe(args, ws, rank, local):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clocks.stop()
+    clk = clocks.summary()
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
     xbytes = X.numel() * (1 if w4a8 else 2) + (X.shape[0] * 4 if w4a8 else 0)
     value = job_rate(ws, wb + xbytes + Y.numel() * 2, ms)
@@ -805,7 +982,8 @@ def run_swiglu(args, ws, rank, local):
     torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
-    clk = clocks.stop()
+    clocks.stop()
+    clk = clocks.summary()
     ms = max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
     calls = len(Xs)
     value = job_rate(ws, calls * wb + io_bytes, ms)
@@ -866,16 +1044,18 @@ def run_swiglu(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["wq", "reference"], default="wq")
-    ap.add_argument("--workload", choices=list(WORKLOAD_NAMES), default="c1")
+    ap.add_argument("--workload", choices=list(WORKLOAD_NAMES), default="sweep")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--windows", type=int, default=20, help="per-shape timing windows (median reported)")
+    ap.add_argument("--window-ms", type=float, default=50.0, help="minimum device time of one window")
     ap.add_argument("--shapes", type=str, default=None,
                     help="comma-separated indices into the workload's shape list (profiling)")
     ap.add_argument("--quick", action="store_true",
-                    help="timed region only: no per-shape timing, e2e or CPU baseline (profiling)")
+                    help="timed steps only: no per-shape timing, e2e or CPU baseline (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -884,7 +1064,7 @@ def main():
         return run_moe(args, ws, rank, local)
     if args.workload == "swiglu":
         return run_swiglu(args, ws, rank, local)
-    shapes = synth.shapes(args.workload)
+    shapes = workload_shapes(args.workload)
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]
     if args.quick:

@@ -323,10 +323,14 @@ int wq_get_option(int option, long long* value);
  *   array of device memory inside the library image (held by every GPU that
  *   loads the library until the process exits); problems that need more
  *   (wq_workspace_size > 16 MiB) return WQ_ERR_WORKSPACE without launching.
- *   Nothing is allocated or freed.  The first call on a device looks up the
- *   array's device address (cudaGetSymbolAddress); make that first call
- *   before capturing a stream.  All calls on a device share the array, so
- *   calls whose kernels may overlap on the GPU (different streams) race on it.
+ *   The arguments are checked first, as wq_gemm_w4a16 checks them, then the
+ *   size.  Nothing is allocated or freed.  The first call on a device looks
+ *   up the array's device address (cudaGetSymbolAddress), and so does the
+ *   first call after the device's context has been rebuilt (cudaDeviceReset);
+ *   make that first call before capturing a stream.  All calls on a device
+ *   share the array and it keeps the last call's contents (no call needs any
+ *   of it to start at zero), so calls whose kernels may overlap on the GPU
+ *   (different streams) race on it.
  */
 int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S,
                           const float* delta, void* Y, int y_dtype, int M, int N, int K,

@@ -78,3 +78,33 @@ def test_grouped_and_pair_reference_arms_print_one_line(workload):
     assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "GB/s"
     assert line["config"]["workload"] == bench.WORKLOAD_NAMES[workload]
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_sweep_reference_arm_reports_the_headline_metric():
+    """The default workload's oracle arm prints one line on rank 0, in the GPU arm's
+    unit (TFLOP/s of the c3 prefill shapes), with the contract's keys."""
+    import json
+
+    class A:
+        steps, warmup, workload = 1, 3, "sweep"
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        assert bench.run_reference(A, bench.workload_shapes("sweep"), 1, 0) == 0
+    line = json.loads(buf.getvalue().strip())
+    assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
+    assert line["config"]["shapes"] == ["c3 M4096 K5120 N17408", "c3 M4096 K17408 N5120"]
+    assert line["e2e"]["value"] == line["value"] and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_workload_shapes_and_dispatch_table():
+    """The sweep holds every configuration's shapes in order; the kernel table follows
+    the library's dispatch rule (M <= 8, 9..16, large M; W4A8 decode and large M)."""
+    sh = [s for _, s in bench.workload_shapes("sweep")]
+    assert [s["cfg"] for s in sh] == ["c0"] + ["c1"] * 6 + ["c2"] * 6 + ["c3"] * 2 + ["c4"] * 3
+    k = {bench.label(s): bench.kernels_for(s) for s in sh}
+    assert k["c1 M1 K4096 N4096"] == ["gemv_kernel"]
+    assert k["c1 M16 K4096 N11008"] == ["decode16_kernel"]
+    assert k["c3 M4096 K5120 N17408"] == ["corr_prep_kernel", "gemm_kernel"]
+    assert k["c4 M16 K5120 N17408"] == ["decode_prep_kernel", "decode_kernel"]
+    assert k["c4 M2048 K5120 N17408"] == ["i8_to_f16_kernel", "gemm_kernel"]
+    assert bench.headline_unit("sweep") == "TFLOP/s" and bench.headline_unit("c1") == "GB/s"

@@ -284,8 +284,12 @@ FULL = [(w, i) for w in ("c0", "c1", "c2", "c3", "c4") for i in range(len(synth.
 
 
 @pytest.mark.parametrize("workload,idx", FULL)
-def test_full_size_workloads_sampled(wq, workload, idx):
+def test_full_size_workloads_sampled(wq, workload, idx, record_property):
+    """Every configuration's shapes at full size, in the bench's launch configuration, on
+    sampled rows and column windows against the oracle; the largest measured error of
+    each shape is recorded (junit property rel_err_max, and printed with -s)."""
     seed, s = synth.shapes(workload)[idx]
+    errs = []
     d = synth.make_inputs(seed, **s)
     rows = _sample_rows(s["M"])
     gs = s["group_size"]
@@ -298,17 +302,25 @@ def test_full_size_workloads_sampled(wq, workload, idx):
         oXq, oxs = oracle.quantize_per_token(d["A"][rows])
         assert np.array_equal(Xq_h[rows], oXq) and np.array_equal(xs_h[rows], oxs)
         qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), gs)
+        A16 = d["A"][rows].astype(np.float64)  # the fp16 activations before quantization
         for c in _sample_cols(s["N"]):
             ref8 = oracle.gemm_w4a8(oXq, oxs, qf, sf, gs, cols=c)
+            # the fp16-activation reference over the same (folded) weights: scale 1 per token
+            ref16 = oracle.gemm_asym_identity(A16, qf, sf, None, gs, cols=c)
             got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
-            assert oracle.rel_fro(got, ref8) <= TOL_W4A8
+            errs.append(oracle.rel_fro(got, ref8))
+            assert errs[-1] <= TOL_W4A8
+            assert oracle.rel_fro(got, ref16) <= TOL_W4A8_VS_F16
     else:
         Y, _ = _w4a16(wq, d)
         for c in _sample_cols(s["N"]):
             ref = _ref_w4a16(d, rows=rows, cols=c)
             got = Y[rows][:, c[0]:c[1]].double().cpu().numpy()
             err = oracle.rel_fro(got, ref)
+            errs.append(err)
             assert err <= TOL_W4A16, (c, err)
+    record_property("rel_err_max", max(errs))
+    print(f"\n{workload}[{idx}] M{s['M']} K{s['K']} N{s['N']}: max sampled rel. error {max(errs):.3e}")
 
 
 @pytest.mark.parametrize("prefetch", [False, True])
@@ -346,6 +358,11 @@ def test_back_to_back_launches_see_their_inputs(wq, prefetch):
         torch.cuda.synchronize()
         for Y, R in zip(Ys, refs):
             assert torch.equal(Y, R)
+        sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+        for i, Y in enumerate(Ys):
+            A64 = (X * (i + 1)).double().cpu().numpy()  # the fp16 activations the GEMM read
+            ref = oracle.gemm_asym_plain(A64, d["q"], sb, zb, 128)
+            assert oracle.rel_fro(Y.double().cpu().numpy(), ref) <= TOL_W4A16, i
     finally:
         wq.set_weight_prefetch(False)
 
@@ -740,6 +757,28 @@ def test_every_entry_family_replays_in_a_cuda_graph(wq):
     torch.cuda.synchronize()
     for i, (o, e) in enumerate(zip(outs, eager)):
         assert torch.equal(o, e), i
+    # ... and the replayed results against the oracle at each family's bar
+    A64 = d["A"].astype(np.float64)
+    sb, zb = oracle.half_bits(d["scale"]), oracle.half_bits(d["zero"])
+    W = (d["q"], sb, zb)
+    _, A64p, (gate, up) = _pair_inputs(7501, 1, K, N // 2)
+    hb = oracle.half_bits
+    gate, up = (gate[0], hb(gate[1]), hb(gate[2])), (up[0], hb(up[1]), hb(up[2]))
+    Xp = X.double().cpu().numpy()
+    refs = [oracle.gemm_asym_plain(A64, *W, 128)]
+    for m in (5, 40):
+        oXq, oxs = oracle.quantize_per_token(d["A"][:m])
+        refs.append(oracle.gemm_w4a8_asym(oXq, oxs, *W, 128))
+    refs += [oracle.gemm_swiglu_pair(Xp[:m], gate, up, 128) for m in (4, 40)]
+    refs.append(oracle.gemm_asym_plain(A64[:7], *W, 128))  # both experts hold the same weights
+    oXq, oxs = oracle.quantize_per_token(d["A"][:7])
+    assert np.array_equal(Xq.cpu().numpy(), oXq) and np.array_equal(xs.cpu().numpy(), oxs)
+    refs.append(oracle.gemm_w4a8_asym(oXq, oxs, *W, 128))
+    tols = [TOL_W4A16, TOL_W4A8, TOL_W4A8, _swiglu_tol(Xp[:4], gate, up, 128),
+            _swiglu_tol(Xp[:40], gate, up, 128), TOL_W4A16, TOL_W4A8]
+    for i, (o, r, tol) in enumerate(zip(outs, refs, tols)):
+        err = oracle.rel_fro(o.double().cpu().numpy(), r)
+        assert err <= tol, (i, err, tol)
 
 
 def test_swiglu_pair_bench_size_sampled(wq):

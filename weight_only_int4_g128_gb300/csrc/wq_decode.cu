@@ -771,15 +771,14 @@ cudaError_t launch_decode(const CUtensorMap& tm_b, const CUtensorMap& tm_s, cons
   if (!status) return cudaErrorInvalidSymbol;
   if (p.splits < 1 || p.splits > dec::kMaxSplits || p.M < 1 || p.M > dec::kMT)
     return cudaErrorInvalidValue;
-  static unsigned long long attr_mask = 0;
+  static PerContextOnce attr_set;  // redone after a context rebuild
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_mask & bit)) {
+  if (attr_set.needed(dev)) {
     e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dec::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_mask |= bit;
+    attr_set.done(dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, p.splits, 1);

@@ -472,15 +472,14 @@ __global__ void __launch_bounds__(d16::kThreads, 2)
 template <int XK>
 static cudaError_t launch_decode16_xk(const CUtensorMap& tm_x, const CUtensorMap& tm_s, const CUtensorMap& tm_d,
                                       const GemmParams& p, unsigned* status, cudaStream_t st) {
-  static unsigned long long attr_mask = 0;
+  static PerContextOnce attr_set;  // redone after a context rebuild
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_mask & bit)) {
+  if (attr_set.needed(dev)) {
     e = cudaFuncSetAttribute(decode16_kernel<XK>, cudaFuncAttributeMaxDynamicSharedMemorySize, d16::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_mask |= bit;
+    attr_set.done(dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, p.splits, 1);

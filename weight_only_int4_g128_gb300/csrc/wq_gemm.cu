@@ -34,6 +34,8 @@
 //
 // Every wait is bounded; on expiry the CTA records a status bit, drains what
 // it issued, frees its TMEM and returns.
+#include <mutex>
+
 #include "wq_device.cuh"
 
 namespace wq {
@@ -466,16 +468,15 @@ template <int BT, int XK>
 static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
                              const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t st) {
   using C = Cfg<BT>;
-  static unsigned long long attr_mask = 0;  // one bit per device that has the attribute set
+  static PerContextOnce attr_set;  // redone after a context rebuild
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_mask & bit)) {
+  if (attr_set.needed(dev)) {
     e = cudaFuncSetAttribute(gemm_kernel<BT, XK>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_mask |= bit;
+    attr_set.done(dev);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
@@ -512,15 +513,21 @@ cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUten
                           : launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, p, stream);
 }
 
-// Device address of the status word (host side), looked up once per device.
+// Device address of the status word (host side), looked up once per device
+// and again whenever the device's context has been rebuilt (the old address
+// then belongs to a context that no longer exists).
 unsigned* status_word() {
+  static std::mutex mu;
+  static PerContextOnce looked_up;
   static unsigned* addr[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!addr[dev]) {
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev] || looked_up.needed(dev)) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_status) != cudaSuccess) return nullptr;
     addr[dev] = static_cast<unsigned*>(ptr);
+    looked_up.done(dev);
   }
   return addr[dev];
 }

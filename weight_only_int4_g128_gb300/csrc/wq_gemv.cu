@@ -603,15 +603,14 @@ bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delt
 
 template <int XK, int D, int MINB, bool PAIR, bool XS = false>
 static cudaError_t launch_gemv_t(const GemmParams& p, unsigned* status, cudaStream_t st) {
-  static unsigned long long attr_mask = 0;
+  static PerContextOnce attr_set;  // redone after a context rebuild
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(attr_mask & bit)) {
+  if (attr_set.needed(dev)) {
     e = cudaFuncSetAttribute(gemv_kernel<XK, D, MINB, PAIR, XS>, cudaFuncAttributeMaxDynamicSharedMemorySize, gv::kMaxSmem);
     if (e != cudaSuccess) return e;
-    attr_mask |= bit;
+    attr_set.done(dev);
   }
   const int gseg = (p.G == 1) ? 1 : p.kb_per_split;
   const gv::Layout L = gv::layout(p.M, p.kb_per_split, p.splits, gseg, p.delta != nullptr, D, PAIR);

@@ -60,6 +60,25 @@ struct GemmParams {
   int swiglu;
 };
 
+// Identifier of the calling thread's current CUDA context, unique for the life
+// of the process (the context a device gets after cudaDeviceReset has a new
+// one); 0 when no context is current yet or the driver cannot tell.
+unsigned long long current_context_id();
+
+// A per-device set-up step (a kernel attribute, a device symbol's address)
+// that has to be redone when the device's context is rebuilt, e.g. after
+// cudaDeviceReset.  Concurrent callers may both redo the step; that is harmless.
+struct PerContextOnce {
+  unsigned long long ctx[64] = {};
+  bool needed(int dev) const {
+    const unsigned long long id = current_context_id();
+    return dev < 0 || dev >= 64 || id == 0 || ctx[dev] != id;
+  }
+  void done(int dev) {
+    if (dev >= 0 && dev < 64) ctx[dev] = current_context_id();
+  }
+};
+
 // Record the message for wq_last_error() on this thread and return `code`.
 int set_last_error(int code, const char* fmt, ...);
 

@@ -27,11 +27,13 @@ constexpr size_t kScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
 static __device__ __align__(256) uint8_t g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[64] = {};  // device address of g_scratch, per device
+void* g_scratch_addr[64] = {};   // device address of g_scratch, per device
+wq::PerContextOnce g_looked_up;  // ... valid for the context it was looked up in
 
-// The array's name in host code is only a stand-in for the symbol; the
-// device address has to be looked up (once per device, with that device
-// current) before a kernel can be given it.
+// The array's name in host code is only a stand-in for the symbol; the device
+// address has to be looked up (once per device, with that device current, and
+// again if the device's context has been rebuilt, e.g. after cudaDeviceReset)
+// before a kernel can be given it.
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -39,13 +41,14 @@ int scratch_address(void** out) {
                                                   cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return wq::set_last_error(WQ_ERR_CUDA, "wq_gemm_w4a16_noalloc: device %d", dev);
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
+  if (!g_scratch_addr[dev] || g_looked_up.needed(dev)) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_scratch);
     if (e != cudaSuccess || !p)
       return wq::set_last_error(WQ_ERR_CUDA, "wq_gemm_w4a16_noalloc: cudaGetSymbolAddress: %s",
                                 cudaGetErrorString(e));
     g_scratch_addr[dev] = p;
+    g_looked_up.done(dev);
   }
   *out = g_scratch_addr[dev];
   return WQ_OK;
@@ -59,11 +62,18 @@ extern "C" int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t*
   const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
   // 0 for shapes the GEMM rejects; wq_gemm_w4a16 below reports those itself.
   const size_t need = (M > 0) ? wq_workspace_size(variant, M, N, K, group_size) : 0;
-  if (need > kScratchBytes)
+  if (need > kScratchBytes) {
+    // Too large for the array.  The arguments are still checked first, as the
+    // workspace entry checks them: without a workspace wq_gemm_w4a16 returns its
+    // argument errors, and otherwise WQ_ERR_WORKSPACE before it launches anything.
+    const int rc = wq_gemm_w4a16(X, x_dtype, Bpacked, S, delta, Y, y_dtype, M, N, K, group_size, nullptr, 0,
+                                 stream);
+    if (rc != WQ_ERR_WORKSPACE) return rc;
     return wq::set_last_error(WQ_ERR_WORKSPACE,
                               "wq_gemm_w4a16_noalloc: this problem needs %zu bytes of scratch; the built-in "
                               "scratch holds %zu (use wq_gemm_w4a16 with a workspace)",
                               need, kScratchBytes);
+  }
   void* scratch = nullptr;
   if (need > 0) {
     const int rc = scratch_address(&scratch);
