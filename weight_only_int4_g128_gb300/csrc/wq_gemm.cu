@@ -28,6 +28,9 @@
 // columns [d_hi | d_hi | d_lo] (delta split the same way).  Their bf16 MMAs add
 // a_hi*d_hi + a_lo*d_hi + a_hi*d_lo, which is a_sum*delta up to ~2^-16
 // relative.
+// Epilogue: with one K segment the dequant warps convert the accumulator into
+// a [BT tokens][128 columns] image over the idle activation ring and one TMA
+// tensor store writes it to Y (whole 256-byte row segments).
 // Split-K: gridDim.z segments of k-blocks form a thread-block cluster; the
 // partials are reduced through distributed shared memory in rank order
 // (deterministic) and written to Y.
@@ -73,10 +76,40 @@ struct Cfg {
   // split-K reduction buffer red[splits][128][rpr + 4] (rpr <= BT/splits + 3, splits <= 8)
   static_assert((BT + 64) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
                 "split-K reduction buffer reuses the stage ring");
+  static_assert(BT * kTileN * 4 <= kNSX * kXStageBytes, "the output tile is staged over the activation ring");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Epilogue image of one tile over shared memory: [BT tokens][128 columns] of
+// type YK (row-major, as the TMA store of Y reads it).  This thread owns column
+// `col` and writes tokens 16 c + j of its chunks c = h + 2 i, scaled by xs[token]
+// when xs is given (tokens past mlim, which the store clips, are left unscaled).
+template <int YK, int kCh>
+__device__ __forceinline__ void write_image(uint32_t img, int col, int h, const uint32_t (&r)[kCh][16],
+                                            const float* xs, int mlim) {
+  constexpr uint32_t es = (YK == kYF32) ? 4 : 2;
+  const uint32_t base = img + static_cast<uint32_t>(col) * es;
+#pragma unroll
+  for (int i = 0; i < kCh; ++i) {
+    const int c = h + 2 * i;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int ml = 16 * c + j;
+      float v = __uint_as_float(r[i][j]);
+      if (xs && ml < mlim) v *= __ldg(xs + ml);
+      const uint32_t a = base + static_cast<uint32_t>(ml) * (kTileN * es);
+      if constexpr (YK == kYF16) {
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(__half_as_ushort(__float2half_rn(v))) : "memory");
+      } else if constexpr (YK == kYBF16) {
+        asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(__bfloat16_as_ushort(__float2bfloat16_rn(v))) : "memory");
+      } else {
+        asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(v)) : "memory");
+      }
+    }
+  }
 }
 
 // All lanes wait; the warp proceeds only if every lane saw the phase complete,
@@ -89,7 +122,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, const W
 template <int BT, int XK>
 __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_aug,
-                const __grid_constant__ CUtensorMap tm_s, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_y,
+                const GemmParams p) {
   using C = Cfg<BT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -341,25 +375,36 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     warp_wait(done_bar, 0, wc);
     named_bar_sync(1, 32 * kDqWarps);
     tc_fence_after();
-    if (!*abort_flag && p.splits == 1) {  // uniform: no wait can set the flag past this point
+    // The tile's outputs are converted into a [BT tokens][128 columns] image over
+    // the (now idle) activation ring, then written by one TMA tensor store: full
+    // 256-byte row segments instead of 2-byte stores scattered over BT rows of Y.
+    // Tokens past M are outside the tensor map and are not written.
+    const bool store_tile = !*abort_flag && p.splits == 1;  // uniform: no wait can set the flag past here
+    if (store_tile) {
       const uint32_t dt = tmem + lane_base + C::kDCol;
       const int mlim = min(BT, p.M - m0);
-      for (int c = h; c < BT / 16; c += 2) {
-        if (16 * c >= mlim) break;
-        uint32_t r[16];
-        tmem_ld16(dt + 16 * c, r);
-        tmem_wait_ld();
+      // this warp's 16-column chunks c = h, h + 2, ...: every TMEM load is issued
+      // before the one wait, so the load latency is paid once per tile
+      constexpr int kCh = BT / 32;
+      uint32_t r[kCh][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int ml = 16 * c + j;
-          if (ml < mlim) {
-            const int m = m0 + ml;
-            float val = __uint_as_float(r[j]);
-            if (p.x_scale) val *= __ldg(p.x_scale + m);
-            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
-          }
-        }
+      for (int i = 0; i < kCh; ++i) tmem_ld16(dt + 16 * (h + 2 * i), r[i]);
+      tmem_wait_ld();
+      // the output type (and whether a per-token scale applies) is decided once,
+      // outside the element loop, and every element is one shared-memory store
+      const float* const xs = p.x_scale ? p.x_scale + m0 : nullptr;
+      switch (p.y_kind) {
+        case kYF16: write_image<kYF16, kCh>(sx, row, h, r, xs, mlim); break;
+        case kYBF16: write_image<kYBF16, kCh>(sx, row, h, r, xs, mlim); break;
+        default: write_image<kYF32, kCh>(sx, row, h, r, xs, mlim); break;
       }
+      fence_proxy_async_smem();  // the image's generic writes become visible to the TMA store
+    }
+    named_bar_sync(1, 32 * kDqWarps);
+    if (store_tile && warp == 2 && lane == 0) {
+      tma_store_2d(&tm_y, sx, n0, m0);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the image is read before the CTA's shared memory is released
     }
     tc_fence_before();
   }
@@ -465,8 +510,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
 }
 
 template <int BT, int XK>
-static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
-                             const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t st) {
+static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug, const CUtensorMap& tm_s,
+                             const CUtensorMap& tm_y, const GemmParams& p, cudaStream_t st) {
   using C = Cfg<BT>;
   static PerContextOnce attr_set;  // redone after a context rebuild
   int dev = 0;
@@ -492,25 +537,25 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_aug, tm_s, p);
+  return cudaLaunchKernelEx(&cfg, gemm_kernel<BT, XK>, tm_x, tm_aug, tm_s, tm_y, p);
 }
 
 template <int XK>
-static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
-                             const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t st) {
+static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap& tm_aug, const CUtensorMap& tm_s,
+                             const CUtensorMap& tm_y, const GemmParams& p, cudaStream_t st) {
   switch (bt) {
-    case 32: return launch_bt<32, XK>(tm_x, tm_aug, tm_s, p, st);
-    case 64: return launch_bt<64, XK>(tm_x, tm_aug, tm_s, p, st);
-    case 128: return launch_bt<128, XK>(tm_x, tm_aug, tm_s, p, st);
-    case 256: return launch_bt<256, XK>(tm_x, tm_aug, tm_s, p, st);
+    case 32: return launch_bt<32, XK>(tm_x, tm_aug, tm_s, tm_y, p, st);
+    case 64: return launch_bt<64, XK>(tm_x, tm_aug, tm_s, tm_y, p, st);
+    case 128: return launch_bt<128, XK>(tm_x, tm_aug, tm_s, tm_y, p, st);
+    case 256: return launch_bt<256, XK>(tm_x, tm_aug, tm_s, tm_y, p, st);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
-                        const CUtensorMap& tm_s, const GemmParams& p, cudaStream_t stream) {
-  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_aug, tm_s, p, stream)
-                          : launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, p, stream);
+                        const CUtensorMap& tm_s, const CUtensorMap& tm_y, const GemmParams& p, cudaStream_t stream) {
+  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_aug, tm_s, tm_y, p, stream)
+                          : launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, tm_y, p, stream);
 }
 
 // Device address of the status word (host side), looked up once per device
