@@ -62,6 +62,11 @@ struct Cfg {
   static constexpr int kNSA = kTwoPerSM ? 3 : (kNSX < 4 ? kNSX : 4);
   static constexpr int kDCol = kTwoPerSM ? 192 : 256;                // accumulator columns
   static constexpr int kTmemCols = kTwoPerSM ? 256 : 512;
+  // 128- and 256-token tiles (one CTA per SM) split the dequant warps into two
+  // groups that take alternate stages, each thread a whole 128-k row, and read
+  // their group scales straight from S; smaller tiles (two CTAs per SM) keep all
+  // eight warps on every stage (two per row) with the scale rows staged in chunks.
+  static constexpr bool kGroups = BT >= 128;
   static constexpr int kChunk = 8;  // groups per scale chunk (the index math below uses >> 3)
   static constexpr int kSChunkBytes = kChunk * kTileN * 2;            // 2 KB of fp16 scale rows
   static constexpr int kChunkSlots = 2;
@@ -178,11 +183,11 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     for (int s = 0; s < C::kNSX; ++s) {
       mbar_init(full_x(s), 1);
       mbar_init(full_w(s), 1);
-      mbar_init(empty_w(s), kDqWarps);  // one arrive per dequant warp
+      mbar_init(empty_w(s), C::kGroups ? kDqWarps / 2 : kDqWarps);  // one arrive per warp reading the stage
       mbar_init(mma_done(s), 1);
     }
     for (int a = 0; a < C::kNSA; ++a) {
-      mbar_init(full_a(a), kDqWarps);
+      mbar_init(full_a(a), C::kGroups ? kDqWarps / 2 : kDqWarps);
     }
     for (int c = 0; c < C::kChunkSlots; ++c) {
       mbar_init(full_c(c), 1);
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
         }
         const int kb = kb0 + (it2 - n_aug);
         const int o = chunk_of(kb);
-        if (o >= chunks_loaded) {
+        if (!C::kGroups && o >= chunks_loaded) {
           const int slot = o % C::kChunkSlots;
           if (!mbar_wait(empty_c(slot), ((o / C::kChunkSlots) & 1) ^ 1, wc)) return false;
           mbar_arrive_expect_tx(full_c(slot), C::kSChunkBytes);
@@ -290,9 +295,11 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     }
   } else {
     // ------------------------------------------------------------ dequant + epilogue
-    // Two warps per TMEM lane quarter: warp half h owns words [8h, 8h + 8) of
-    // each weight row (A-stage columns [32h, 32h + 32)) and, in the epilogue,
-    // the 16-column chunks c with c % 2 == h.
+    // Two warps per TMEM lane quarter, h = 0 or 1.  Tiles of 128 or 256 tokens:
+    // warp group h takes the stages it with it % 2 == h (see below); smaller tiles:
+    // warp half h owns words [8h, 8h + 8) of each weight row (A-stage columns
+    // [32h, 32h + 32)) of every stage.  In the epilogue warp h takes the
+    // 16-column chunks c with c % 2 == h.
     const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutMath, &g_status};
     const int q = warp & 3;               // TMEM lane quarter this warp may access
     const int h = (warp - 2) >> 2;        // 0 or 1
@@ -301,6 +308,93 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     const uint8_t* wring = gbase + (sw - base);
 
+    if constexpr (C::kGroups) {
+    // Two groups of four warps (one per TMEM lane quarter) take alternate stages:
+    // group h dequantizes the k-blocks it with it % 2 == h, each thread a whole
+    // 128-k weight row into the stage's 64 A columns, so every barrier round trip
+    // of a group is spread over two stages of MMA time.  The row's group scale
+    // is read from S into a register one of the group's stages ahead.
+    auto scale_of = [&](int st) -> __half {
+      if (st >= n_stages || st < n_aug) return __ushort_as_half(0);
+      const int kb = kb0 + (st - n_aug);
+      return __ldg(p.S + static_cast<size_t>(per_channel ? 0 : kb) * p.N + n);
+    };
+    __half sc_next = scale_of(h);
+    for (int it = h; it < n_stages; it += 2) {
+      const int s = it % C::kNSX;
+      const uint32_t ph = (it / C::kNSX) & 1;
+      const int a = it % C::kNSA;
+      const uint32_t a_tmem = tmem + lane_base + a * 64;
+      const __half sc = sc_next;
+      sc_next = scale_of(it + 2);
+      // A-stage a was last read by the MMAs of k-block it - kNSA.  Waiting for them
+      // first also makes the full_w wait below exact: a parity wait only tells the
+      // current phase from the one just before it, and the previous tile of slot s
+      // (k-block it - kNSX, possibly the other group's, whose copy may land after
+      // this group's own earlier tiles) has been consumed once MMA it - kNSA is
+      // done (MMAs complete in order and kNSA <= kNSX).
+      if (it >= C::kNSA) {
+        const int pk = it - C::kNSA;
+        if (!warp_wait(mma_done(pk % C::kNSX), (pk / C::kNSX) & 1, wc)) break;
+        tc_fence_after();
+      }
+      uint32_t v[64];
+      if (it < n_aug) {
+        // weight-side correction columns [d_hi | d_hi | d_lo | 0...] of this row,
+        // prepared per call in the workspace: 128 bf16 = 64 columns, 16 vector loads.
+        const uint4* src = reinterpret_cast<const uint4*>(p.delta_aug + static_cast<size_t>(n) * p.kaug + it * kKBlock);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint4 t = __ldg(src + i);
+          v[4 * i + 0] = t.x;
+          v[4 * i + 1] = t.y;
+          v[4 * i + 2] = t.z;
+          v[4 * i + 3] = t.w;
+        }
+        if (!warp_wait(full_w(s), ph, wc)) break;  // the producer's (empty) weight side of the stage
+        if (lane == 0) mbar_arrive(empty_w(s));
+      } else {
+        if (!warp_wait(full_w(s), ph, wc)) break;
+        const uint8_t* const slot = wring + s * C::kWStageBytes;
+        // the row's four 16-byte chunks (chunk c stored at c ^ ((row / 2) % 4))
+        uint4 wc4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          wc4[c] = *reinterpret_cast<const uint4*>(slot + row * 64 + 16 * (c ^ ((row >> 1) & 3)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_w(s));
+        if (XK == kXF16) {
+          const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const uint4& q4 = wc4[w >> 2];
+            const uint32_t word = (w & 3) == 0 ? q4.x : (w & 3) == 1 ? q4.y : (w & 3) == 2 ? q4.z : q4.w;
+            uint32_t o[4];
+            dq8_f16_scaled(word, s2, o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
+          }
+        } else {
+          const ScaleBf16 sb = split_scale_bf16(sc);
+#pragma unroll
+          for (int w = 0; w < 16; ++w) {
+            const uint4& q4 = wc4[w >> 2];
+            const uint32_t word = (w & 3) == 0 ? q4.x : (w & 3) == 1 ? q4.y : (w & 3) == 2 ? q4.z : q4.w;
+            uint32_t o[4];
+            dq8_bf16_scaled(word, sb, o);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
+          }
+        }
+      }
+      tmem_st32(a_tmem, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
+      tmem_st32(a_tmem + 32, *reinterpret_cast<const uint32_t(*)[32]>(&v[32]));
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_a(a));
+    }
+    } else {
     for (int it = 0; it < n_stages; ++it) {
       const int s = it % C::kNSX;
       const uint32_t ph = (it / C::kNSX) & 1;
@@ -369,6 +463,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(full_a(a));
+    }
     }
 
     // ---- epilogue (single K segment): accumulator -> Y
