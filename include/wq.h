@@ -351,6 +351,14 @@ int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t* Bpacked, c
  *            wq_host_workspace_size(...) bytes, 256-byte aligned: the device
  *            copies of X and Y, then the GEMM's own workspace.
  * All arguments are checked before anything is enqueued.
+ * With M >= 2048 the call pipelines token-row chunks (up to four, multiples of
+ * 256 rows): the copy of a chunk's X runs on one internal stream, its GEMM on
+ * `stream`, the copy of its Y on a second internal stream, ordered by events,
+ * so copies overlap the neighbouring chunks' GEMMs.  The two copy streams and
+ * their events are created once per device on the first such call (no memory
+ * is allocated); `stream` waits for the last copy before any later work, so
+ * Y_host is complete once `stream` is synchronized.  Concurrent calls from
+ * several host threads are serialized while they are enqueued.
  */
 int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked, const void* S,
                        const float* delta, void* Y_host, int y_dtype, int M, int N, int K,

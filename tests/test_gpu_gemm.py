@@ -396,6 +396,30 @@ def test_host_buffer_entry_matches_device_entry(wq, M, K, N, adt, sym, ydt):
     assert Y2.is_pinned() and torch.equal(Y2, Yd.cpu())
 
 
+@pytest.mark.parametrize("M,K,N,adt,ydt", [
+    (2500, 1024, 8192, "f16", torch.float16),    # two chunks of 1280 and 1220 rows
+    (4096, 512, 4096, "bf16", torch.float32),    # four chunks of 1024 rows
+])
+def test_host_buffer_entry_pipelined_chunks(wq, M, K, N, adt, ydt):
+    """gemm_w4a16_host with M >= 2048 runs row chunks in a pipeline (copies in and out on
+    internal streams overlapping the chunk GEMMs).  With one K segment per tile the chunk
+    boundaries (multiples of 256 rows) fall on token-tile boundaries, so the result equals
+    the device entry's bit for bit; sampled rows match the oracle; two calls in a row."""
+    d = synth.make_inputs(4200 + M, M, K, N, a_dtype=adt)
+    Yd, (Bp, S, dl) = _w4a16(wq, d, out_dtype=ydt)
+    hX = _x(d).cpu().pin_memory()
+    hY = torch.empty((M, N), dtype=ydt).pin_memory()
+    for _ in range(2):
+        hY.fill_(float("nan"))
+        wq.gemm_w4a16_host(hX, Bp, S, dl, 128, out=hY)
+        torch.cuda.synchronize()
+        assert torch.equal(hY, Yd.cpu())
+    rows = _sample_rows(M)
+    cols = (N // 2 - 64, N // 2 + 64)
+    ref = _ref_w4a16(d, rows=rows, cols=cols)
+    assert oracle.rel_fro(hY[rows][:, cols[0]:cols[1]].double().numpy(), ref) <= TOL_W4A16
+
+
 @pytest.mark.parametrize("M,K,N,gs,adt", [
     (3, 1408, 256, 128, "f16"),     # 11 k-blocks over 6 segments of 2: the last segment has one
     (2, 256, 20480, 128, "f16"),    # 160 column tiles: one segment, partials stored from registers

@@ -685,6 +685,45 @@ int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const voi
 
 static size_t y_elem_bytes(int y_dtype) { return y_dtype == WQ_DTYPE_F32 ? 4 : 2; }
 
+namespace {
+// The pipelined host-buffer GEMM: two copy streams and the events that order
+// them against the caller's stream, per device.  Created on the first large
+// call on a device (and again after its context has been rebuilt); no memory is
+// allocated.
+constexpr int kHostChunksMax = 4;
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t x_in[kHostChunksMax] = {}, y_ready[kHostChunksMax] = {};
+};
+std::mutex g_host_mu;  // held while a pipelined call is enqueued (the streams and events are shared)
+HostPipe g_host_pipe[64];
+wq::PerContextOnce g_host_pipe_made;
+
+int host_pipe(HostPipe** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(WQ_ERR_CUDA, "wq_gemm_w4a16_host: device %d", dev);
+  HostPipe& hp = g_host_pipe[dev];
+  if (g_host_pipe_made.needed(dev)) {
+    hp = HostPipe{};
+    e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+    for (int c = 0; c < kHostChunksMax && e == cudaSuccess; ++c) {
+      e = cudaEventCreateWithFlags(&hp.x_in[c], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.y_ready[c], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy streams");
+    g_host_pipe_made.done(dev);
+  }
+  *out = &hp;
+  return WQ_OK;
+}
+}  // namespace
+
 size_t wq_host_workspace_size(int variant, int M, int N, int K, int group_size, int y_dtype) {
   if (variant != WQ_VARIANT_W4A16 && variant != WQ_VARIANT_W4A16_SYM) return 0;
   if (y_kind_of(y_dtype) < 0 || M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
@@ -724,13 +763,64 @@ int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked,
   void* const Yd = ws + align256(x_bytes);
   uint8_t* const gws = ws + align256(x_bytes) + align256(y_bytes);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(Xd, X_host, x_bytes, cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of X to the device");
-  rc = gemm_core(Xd, x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16, Bpacked, S, delta, nullptr, Yd, yk, M, N, K,
-                 gs, variant, gws, workspace_bytes - (gws - ws), st, "wq_gemm_w4a16_host");
+  const int xk = x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16;
+  const size_t gws_bytes = workspace_bytes - (gws - ws);
+  const int chunks = (M >= 2048) ? (M / 1024 < kHostChunksMax ? M / 1024 : kHostChunksMax) : 1;
+  if (chunks == 1) {
+    cudaError_t e = cudaMemcpyAsync(Xd, X_host, x_bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of X to the device");
+    rc = gemm_core(Xd, xk, Bpacked, S, delta, nullptr, Yd, yk, M, N, K, gs, variant, gws, gws_bytes, st,
+                   "wq_gemm_w4a16_host");
+    if (rc) return rc;
+    e = cudaMemcpyAsync(Y_host, Yd, y_bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of Y to the host");
+    return WQ_OK;
+  }
+  // Large M: token-row chunks (a multiple of 256 rows) in a pipeline, so that the
+  // copy of chunk c + 1's activations and of chunk c - 1's outputs overlap chunk
+  // c's GEMM.  Copies in run on one internal stream, copies out on another, the
+  // GEMMs on the caller's stream; events order each chunk's three steps, and the
+  // caller's stream waits for the last copy out before anything enqueued after
+  // this call (so Y_host is complete once that stream is synchronized).
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe* hp = nullptr;
+  if ((rc = host_pipe(&hp))) return rc;
+  const int rows = ((M + chunks - 1) / chunks + 255) & ~255;
+  const size_t ysz = y_elem_bytes(y_dtype);
+  cudaError_t e = cudaEventRecord(hp->start, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->in, hp->start, 0);  // earlier work on st is done with Xd
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: stream fork");
+  int c = 0;
+  for (int r0 = 0; r0 < M && rc == WQ_OK; r0 += rows, ++c) {
+    const int mc = (M - r0 < rows) ? M - r0 : rows;
+    uint8_t* const xc = static_cast<uint8_t*>(Xd) + static_cast<size_t>(r0) * K * 2;
+    uint8_t* const yc = static_cast<uint8_t*>(Yd) + static_cast<size_t>(r0) * N * ysz;
+    e = cudaMemcpyAsync(xc, static_cast<const uint8_t*>(X_host) + static_cast<size_t>(r0) * K * 2,
+                        static_cast<size_t>(mc) * K * 2, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->x_in[c], hp->in);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hp->x_in[c], 0);
+    if (e != cudaSuccess) {
+      rc = cuda_fail(e, "wq_gemm_w4a16_host: copy of X to the device");
+      break;
+    }
+    rc = gemm_core(xc, xk, Bpacked, S, delta, nullptr, yc, yk, mc, N, K, gs, variant, gws, gws_bytes, st,
+                   "wq_gemm_w4a16_host");
+    if (rc) break;
+    e = cudaEventRecord(hp->y_ready[c], st);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->out, hp->y_ready[c], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(static_cast<uint8_t*>(Y_host) + static_cast<size_t>(r0) * N * ysz, yc,
+                          static_cast<size_t>(mc) * N * ysz, cudaMemcpyDeviceToHost, hp->out);
+    if (e != cudaSuccess) rc = cuda_fail(e, "wq_gemm_w4a16_host: copy of Y to the host");
+  }
+  // join the copy streams back into the caller's stream, also after an error
+  cudaError_t ej = cudaEventRecord(hp->done, hp->out);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, hp->done, 0);
+  if (ej == cudaSuccess) ej = cudaEventRecord(hp->start, hp->in);
+  if (ej == cudaSuccess) ej = cudaStreamWaitEvent(st, hp->start, 0);
   if (rc) return rc;
-  e = cudaMemcpyAsync(Y_host, Yd, y_bytes, cudaMemcpyDeviceToHost, st);
-  if (e != cudaSuccess) return cuda_fail(e, "wq_gemm_w4a16_host: copy of Y to the host");
+  if (ej != cudaSuccess) return cuda_fail(ej, "wq_gemm_w4a16_host: stream join");
   return WQ_OK;
 }
 
