@@ -541,11 +541,17 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
       const bool aborted = *abort_flag != 0;
       const uint32_t dt = tmem + (static_cast<uint32_t>(q * 32) << 16) + C::kDCol;
       const uint32_t red_row = smem_u32(red) + static_cast<uint32_t>((seg * kTileN + row) * rpr_pad * 4);
-      for (int c = h; c < BT / 16; c += 2) {
+      // this warp's 16-column chunks c = h, h + 2, ...: every TMEM load is issued
+      // before the one wait, then the partials are pushed to their owners
+      constexpr int kCh = BT / 32;
+      uint32_t r[kCh][16];
+#pragma unroll
+      for (int i = 0; i < kCh; ++i) tmem_ld16(dt + 16 * (h + 2 * i), r[i]);
+      tmem_wait_ld();
+#pragma unroll
+      for (int i = 0; i < kCh; ++i) {
+        const int c = h + 2 * i;
         if (16 * c >= mlim) break;
-        uint32_t r[16];
-        tmem_ld16(dt + 16 * c, r);
-        tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 16; j += 4) {
           const int ml = 16 * c + j;  // 4 consecutive rows, same owner (rpr % 4 == 0)
@@ -557,8 +563,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
               const float nanv = __int_as_float(0x7fc00000);
               st_dsmem_v4(addr, nanv, nanv, nanv, nanv);
             } else {
-              st_dsmem_v4(addr, __uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                          __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+              st_dsmem_v4(addr, __uint_as_float(r[i][j]), __uint_as_float(r[i][j + 1]),
+                          __uint_as_float(r[i][j + 2]), __uint_as_float(r[i][j + 3]));
             }
           }
         }

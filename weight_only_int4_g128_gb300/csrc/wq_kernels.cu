@@ -245,46 +245,67 @@ struct CorrPrep {
   int n_sum_blocks;  // blocks of the group-sum part
   int g_tiles;       // 32-wide group tiles of the delta part
 };
+constexpr int kSumItems = 4;  // (token, group pair) items per warp in the 128-group layout
 
+// Group sums of the activations, written as the activation-side correction
+// columns [a_hi | a_lo | a_hi | 0 ...] of each token row.
+//   group 128: a warp takes kSumItems (token, group pair) items; for an item the
+//   lanes read the pair's 512 contiguous bytes (16 bytes each, lanes 0..15 the
+//   first group, 16..31 the second) and each half-warp adds its group up.
+//   group K (one group per column): a warp per (token, group), lanes striding
+//   the row.
 template <int XK>
 __device__ __forceinline__ void corr_group_sums(const CorrPrep& c, int bid) {
   const uint16_t* Xh = reinterpret_cast<const uint16_t*>(c.X);
   const int G = c.G;
   const int pad = c.kaug - 3 * G;
-  if (c.group_size <= 1024) {
-    // one thread per (m, g); the thread of g == 0 also zeroes the row's padding
-    const long long idx = bid * 256LL + threadIdx.x;
-    if (idx >= static_cast<long long>(c.M) * G) return;
-    const int m = static_cast<int>(idx / G);
-    const int g = static_cast<int>(idx - static_cast<long long>(m) * G);
-    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * c.K +
-                                                     static_cast<size_t>(g) * c.group_size);
-    float acc = 0.0f;
-    const int nv = c.group_size / 8;
-#pragma unroll 16
-    for (int i = 0; i < nv; ++i) acc += sum8<XK>(__ldg(gp + i));
-    __nv_bfloat16* arow = c.aug + static_cast<size_t>(m) * c.kaug;
-    write_aug(arow, G, g, acc);
-    if (g == 0)
-      for (int j = 0; j < pad; ++j) arow[3 * G + j] = __float2bfloat16_rn(0.0f);
+  const int lane = threadIdx.x & 31;
+  const long long warp = (static_cast<long long>(bid) * 256 + threadIdx.x) >> 5;
+  if (c.group_size == kKBlock) {
+    const int npairs = (G + 1) / 2;
+    const long long items = static_cast<long long>(c.M) * npairs;
+    const int half = lane >> 4;
+    uint4 v[kSumItems];
+    int m[kSumItems], g[kSumItems];
+#pragma unroll
+    for (int u = 0; u < kSumItems; ++u) {
+      const long long q = warp * kSumItems + u;
+      m[u] = -1;
+      v[u] = make_uint4(0u, 0u, 0u, 0u);
+      if (q < items) {
+        m[u] = static_cast<int>(q / npairs);
+        g[u] = 2 * static_cast<int>(q - static_cast<long long>(m[u]) * npairs) + half;
+        if (g[u] < G)
+          v[u] = __ldg(reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m[u]) * c.K +
+                                                      static_cast<size_t>(g[u]) * kKBlock) + (lane & 15));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kSumItems; ++u) {
+      if (m[u] < 0) break;  // uniform over the warp
+      float acc = sum8<XK>(v[u]);
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      __nv_bfloat16* arow = c.aug + static_cast<size_t>(m[u]) * c.kaug;
+      if ((lane & 15) == 0 && g[u] < G) write_aug(arow, G, g[u], acc);
+      if (g[u] == 0 && half == 0)  // the item holding group 0 zeroes the row's padding
+        for (int j = lane; j < pad; j += 16) arow[3 * G + j] = __float2bfloat16_rn(0.0f);
+    }
   } else {
-    // one warp per (m, g) for long groups (per-channel)
-    const int warp = (bid * 256 + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (warp >= c.M * G) return;
-    const int m = warp / G;
-    const int g = warp - m * G;
-    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(m) * c.K +
-                                                     static_cast<size_t>(g) * c.group_size);
+    if (warp >= static_cast<long long>(c.M) * G) return;
+    const int mm = static_cast<int>(warp / G);
+    const int gg = static_cast<int>(warp - static_cast<long long>(mm) * G);
+    const uint4* gp = reinterpret_cast<const uint4*>(Xh + static_cast<size_t>(mm) * c.K +
+                                                     static_cast<size_t>(gg) * c.group_size);
     float acc = 0.0f;
     const int nv = c.group_size / 8;
 #pragma unroll 8
     for (int i = lane; i < nv; i += 32) acc += sum8<XK>(__ldg(gp + i));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    __nv_bfloat16* arow = c.aug + static_cast<size_t>(m) * c.kaug;
-    if (lane == 0) write_aug(arow, G, g, acc);
-    if (g == 0)
+    __nv_bfloat16* arow = c.aug + static_cast<size_t>(mm) * c.kaug;
+    if (lane == 0) write_aug(arow, G, gg, acc);
+    if (gg == 0)
       for (int j = lane; j < pad; j += 32) arow[3 * G + j] = __float2bfloat16_rn(0.0f);
   }
 }
@@ -431,9 +452,10 @@ cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int 
   c.group_size = group_size;
   c.G = G;
   c.kaug = kaug;
-  const long long sum_threads = (group_size <= 1024) ? static_cast<long long>(M) * G
-                                                     : static_cast<long long>(M) * G * 32;
-  c.n_sum_blocks = static_cast<int>((sum_threads + 255) / 256);
+  const long long sum_warps = (group_size == kKBlock)
+                                  ? (static_cast<long long>(M) * ((G + 1) / 2) + kSumItems - 1) / kSumItems
+                                  : static_cast<long long>(M) * G;
+  c.n_sum_blocks = static_cast<int>((sum_warps + 7) / 8);
   c.g_tiles = (G + 31) / 32;
   const long long blocks = c.n_sum_blocks + static_cast<long long>(c.g_tiles) * (N / 32);
   cudaLaunchConfig_t cfg = {};
