@@ -151,7 +151,12 @@ int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, 
  *            initialization is needed.  Calls that may run concurrently must
  *            use different workspaces.
  * Accumulation is fp32.  The weights are dequantized as RN((q-8)*scale) in
- * the activation type; the correction is added in the same accumulator.
+ * fp16 for M > 16 (in the activation type's exact offset form with the scale
+ * applied in fp32 per 128-k block for M <= 16); the correction is added in
+ * the same accumulator.  bf16 activations with M > 16 are first copied into
+ * the workspace as fp16 after a per-token power-of-two scale (exact: fp16
+ * holds every bf16 significand in range), which the GEMM undoes exactly at its
+ * store, so large-M bf16 calls keep fp16's 11-bit weights.
  */
 int wq_gemm_w4a16(const void* X, int x_dtype, const uint32_t* Bpacked, const void* S,
                   const float* delta, void* Y, int y_dtype, int M, int N, int K, int group_size,
@@ -322,7 +327,11 @@ int wq_get_option(int option, long long* value);
  *   Arguments and result as wq_gemm_w4a16.  The scratch comes from a 16 MiB
  *   array of device memory inside the library image (held by every GPU that
  *   loads the library until the process exits); problems that need more
- *   (wq_workspace_size > 16 MiB) return WQ_ERR_WORKSPACE without launching.
+ *   return WQ_ERR_WORKSPACE without launching.  The need is that of this
+ *   call's activation type: about (M + N) * K/128 * 4 bytes of correction
+ *   columns for M > 16 with delta, plus M * K * 2 bytes of scaled fp16
+ *   activations when they are bf16 (so bf16 problems above about 8M
+ *   activation elements are refused).
  *   The arguments are checked first, as wq_gemm_w4a16 checks them, then the
  *   size.  Nothing is allocated or freed.  The first call on a device looks
  *   up the array's device address (cudaGetSymbolAddress), and so does the
@@ -368,7 +377,9 @@ int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked,
  * variant WQ_VARIANT_W4A16 or WQ_VARIANT_W4A16_SYM. */
 size_t wq_host_workspace_size(int variant, int M, int N, int K, int group_size, int y_dtype);
 
-/* Bytes of workspace the GEMM needs for this problem (0 if none). */
+/* Bytes of workspace the GEMM needs for this problem (0 if none): the most any
+ * activation type needs (bf16 activations with M > 16 need M * K * 2 + M * 4
+ * bytes more than fp16 ones, for their scaled fp16 copy). */
 size_t wq_workspace_size(int variant, int M, int N, int K, int group_size);
 
 /* 1 if `device` is an sm_103 GPU this library can run on, else 0. */

@@ -57,10 +57,14 @@ def test_version_and_workspace_queries(lib):
     b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 1, 4096, 4096, 128)
     c = lib.wq_workspace_size(wq.VARIANT_W4A8, 16, 4096, 4096, 128)
     assert a == b == 0 and c == 56 * 4096
-    # large M: the asymmetric variant needs the correction columns, [M + N][kaug] bf16
+    # large M: the asymmetric variant needs the correction columns, [M + N][kaug] bf16;
+    # both variants need room for bf16 activations' scaled fp16 copy [M][K] and its
+    # per-token factors [M] fp32 (the query takes no activation type, so it returns
+    # the most any type needs)
     a = lib.wq_workspace_size(wq.VARIANT_W4A16, 512, 4096, 4096, 128)
     b = lib.wq_workspace_size(wq.VARIANT_W4A16_SYM, 512, 4096, 4096, 128)
-    assert a >= (512 + 4096) * 128 * 2 and b == 0
+    assert b == 512 * 4096 * 2 + 512 * 4
+    assert a == (512 + 4096) * 128 * 2 + b
     assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4000, 128) == 0  # K % 128
     assert lib.wq_workspace_size(wq.VARIANT_W4A16, 16, 4096, 4096, 64) == 0   # group size
     assert lib.wq_workspace_size(9, 16, 4096, 4096, 128) == 0

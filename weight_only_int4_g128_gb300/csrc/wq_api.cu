@@ -172,7 +172,7 @@ struct Plan {
   int splits;
   int kb_per_split;
   int kaug;       // large-M correction length (0 without correction or for the decode kernel)
-  size_t off_aug, off_daug, off_x16;  // byte offsets into the workspace (large M)
+  size_t off_aug, off_daug, off_x16, off_xs;  // byte offsets into the workspace (large M)
   size_t off_x8;                      // byte offset into the workspace (decode)
   size_t bytes;
 };
@@ -181,7 +181,9 @@ constexpr int kMaxClusterSplits = 8;  // K segments of one tile form a portable 
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-Plan make_plan(int variant, int M, int N, int K, int gs) {
+// x_kind: the activations' type, or -1 for the most any activation type needs
+// (the public size query, which takes no type).
+Plan make_plan(int variant, int M, int N, int K, int gs, int x_kind) {
   Plan p{};
   const int G = K / gs;
   const int kb = K / 128;
@@ -209,8 +211,12 @@ Plan make_plan(int variant, int M, int N, int K, int gs) {
   if (p.kaug) off = align256(off + static_cast<size_t>(M) * p.kaug * 2);
   p.off_daug = off;
   if (p.kaug) off = align256(off + static_cast<size_t>(N) * p.kaug * 2);
+  // large M: W4A8's int8 rows as fp16, or bf16 rows as per-token scaled fp16 (+ the factors)
+  const bool conv = !p.gemv && !int8x && x_kind != wq::kXF16;
   p.off_x16 = off;
-  if (int8x && !p.gemv) off = align256(off + static_cast<size_t>(M) * K * 2);
+  if ((int8x && !p.gemv) || conv) off = align256(off + static_cast<size_t>(M) * K * 2);
+  p.off_xs = off;
+  if (conv) off = align256(off + static_cast<size_t>(M) * 4);
   // decode W4A8: e4m3 activation components + per-block sums/factors row, padded: [56][K]
   // bytes (the W4A16 decode kernel reads the activations directly)
   p.off_x8 = off;
@@ -252,7 +258,7 @@ int launch_gemv_call(const void* X, int x_kind, const uint32_t* Bpacked, const v
 int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S, const float* delta,
               const float* x_scale, void* Y, int y_kind, int M, int N, int K, int gs, int variant,
               void* ws, size_t ws_bytes, cudaStream_t st, const char* name, bool quant_in = false) {
-  const Plan plan = make_plan(variant, M, N, K, gs);
+  const Plan plan = make_plan(variant, M, N, K, gs, x_kind);
   if (plan.bytes > 0 && (!ws || ws_bytes < plan.bytes))
     return fail(WQ_ERR_WORKSPACE, "%s: workspace of %zu bytes given, %zu needed", name, ws_bytes, plan.bytes);
   if (ws && !aligned16(ws)) return fail(WQ_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", name);
@@ -369,15 +375,27 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   }
   __nv_bfloat16* aug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_aug);
   __nv_bfloat16* daug = reinterpret_cast<__nv_bfloat16*>(wsb + plan.off_daug);
-  if (plan.kaug) {
-    // group sums of the activations the GEMM reads (for W4A8 the int8 rows as fp16, exact)
-    e = wq::launch_corr_prep(xg, x_kind, delta, M, K, N, gs, G, plan.kaug, aug, daug, st);
+  // bf16 rows: the GEMM runs on fp16 operands, reading a per-token scaled fp16
+  // copy of X that the pre-pass writes, and undoes the scale in its epilogue
+  const bool conv = !int8x && x_kind == wq::kXBF16;
+  __half* x16c = conv ? reinterpret_cast<__half*>(wsb + plan.off_x16) : nullptr;
+  float* xsc = conv ? reinterpret_cast<float*>(wsb + plan.off_xs) : nullptr;
+  if (plan.kaug || conv) {
+    // group sums of the activations the GEMM reads (for W4A8 the int8 rows as fp16,
+    // exact; for bf16 rows the scaled fp16 copy written here)
+    e = wq::launch_corr_prep(xg, x_kind, delta, M, K, N, gs, G, plan.kaug, aug, daug, x16c, xsc, st);
     if (e != cudaSuccess) return cuda_fail(e, "correction pre-pass");
+  }
+  int gk = x_kind;  // the GEMM's operand type
+  if (conv) {
+    xg = x16c;
+    gk = wq::kXF16;
+    x_scale = xsc;
   }
 
   CUtensorMap tm_x, tm_aug, tm_s, tm_d;
   const CUtensorMapDataType xdt =
-      x_kind == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      gk == wq::kXBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   int rc = make_map_x3d(&tm_x, xdt, xg, M, K, plan.bt);
   if (rc) return rc;
   if (plan.kaug) {
@@ -423,7 +441,7 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   rc = make_map(&tm_y, ydt, y_kind == wq::kYF32 ? 4 : 2, Y, M, N, plan.bt, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
-  e = wq::launch_gemm(plan.bt, x_kind, tm_x, tm_aug, tm_s, tm_y, p, st);
+  e = wq::launch_gemm(plan.bt, gk, tm_x, tm_aug, tm_s, tm_y, p, st);
   return after_launch(e, name, st);
 }
 
@@ -461,6 +479,15 @@ unsigned long long current_context_id() {
   if (get_current(&c) != CUDA_SUCCESS || !c) return 0;
   unsigned long long id = 0;
   return get_id(c, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+size_t gemm_workspace_bytes(int variant, int x_dtype, int M, int N, int K, int group_size) {
+  if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % 128) return 0;
+  const int gs = (group_size == -1) ? K : group_size;
+  if (gs != 128 && gs != K) return 0;
+  if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8_ASYM) return 0;
+  return make_plan(variant, M, N, K, gs, x_dtype == WQ_DTYPE_F16 ? kXF16 : x_dtype == WQ_DTYPE_BF16 ? kXBF16 : -1)
+      .bytes;
 }
 
 int set_last_error(int code, const char* fmt, ...) {
@@ -518,13 +545,13 @@ struct SwigluPlan {
   size_t off_prod, bytes;
 };
 
-SwigluPlan make_swiglu_plan(int M, int N, int K, int gs, bool has_delta) {
+SwigluPlan make_swiglu_plan(int M, int N, int K, int gs, bool has_delta, int x_kind) {
   SwigluPlan sp{};
   const int Nc = 2 * N;
   sp.fused = wq::gemv_plan(M, Nc, K, gs, has_delta, &sp.splits, &sp.kbps, true) != 0;
   if (sp.fused) return sp;
   const int variant = has_delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
-  sp.off_prod = align256(make_plan(variant, M, Nc, K, gs).bytes);
+  sp.off_prod = align256(make_plan(variant, M, Nc, K, gs, x_kind).bytes);
   sp.bytes = sp.off_prod + static_cast<size_t>(M) * Nc * 4;
   return sp;
 }
@@ -534,9 +561,9 @@ size_t wq_workspace_size(int variant, int M, int N, int K, int group_size) {
   if (M <= 0 || N <= 0 || K <= 0 || K % 128 || N % (pair ? 64 : 128)) return 0;
   int gs = (group_size == -1) ? K : group_size;
   if (gs != 128 && gs != K) return 0;
-  if (pair) return make_swiglu_plan(M, N, K, gs, variant == WQ_VARIANT_W4A16_SWIGLU).bytes;
+  if (pair) return make_swiglu_plan(M, N, K, gs, variant == WQ_VARIANT_W4A16_SWIGLU, -1).bytes;
   if (variant < WQ_VARIANT_W4A16 || variant > WQ_VARIANT_W4A8_ASYM) return 0;
-  return make_plan(variant, M, N, K, gs).bytes;
+  return make_plan(variant, M, N, K, gs, -1).bytes;
 }
 
 int wq_pack_w4a16_pair(const uint8_t* q_gate, const void* scale_gate, const void* zero_gate, const uint8_t* q_up,
@@ -575,7 +602,8 @@ int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, co
   if (!X || !Bpacked || !S || !Y) return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: null pointer");
   if (!aligned16(X) || !aligned16(Bpacked) || !aligned16(Y) || !aligned16(S) || (delta && !aligned16(delta)))
     return fail(WQ_ERR_INVALID_ARG, "wq_gemm_w4a16_swiglu: X, Bpacked, S, delta and Y must be 16-byte aligned");
-  const SwigluPlan sp = make_swiglu_plan(M, N, K, gs, delta != nullptr);
+  const SwigluPlan sp =
+      make_swiglu_plan(M, N, K, gs, delta != nullptr, x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16);
   if (sp.bytes > 0 && (!workspace || workspace_bytes < sp.bytes))
     return fail(WQ_ERR_WORKSPACE, "wq_gemm_w4a16_swiglu: workspace of %zu bytes given, %zu needed", workspace_bytes,
                 sp.bytes);
@@ -730,7 +758,7 @@ size_t wq_host_workspace_size(int variant, int M, int N, int K, int group_size, 
   const int gs = (group_size == -1) ? K : group_size;
   if (gs != 128 && gs != K) return 0;
   return align256(static_cast<size_t>(M) * K * 2) + align256(static_cast<size_t>(M) * N * y_elem_bytes(y_dtype)) +
-         make_plan(variant, M, N, K, gs).bytes;
+         make_plan(variant, M, N, K, gs, -1).bytes;
 }
 
 int wq_gemm_w4a16_host(const void* X_host, int x_dtype, const uint32_t* Bpacked, const void* S, const float* delta,
@@ -910,7 +938,7 @@ int wq_gemm_w4a16_grouped(const void* X, int x_dtype, const uint32_t* Bpacked, c
   for (int e = 0; e < experts; ++e) {
     const int me = expert_offsets[e + 1] - expert_offsets[e];
     if (me > 0) {
-      const size_t b = make_plan(variant, me, N, K, gs).bytes;
+      const size_t b = make_plan(variant, me, N, K, gs, xk).bytes;
       need = b > need ? b : need;
     }
   }
@@ -998,7 +1026,7 @@ int wq_gemm_w4a8_grouped(const int8_t* Xq, const float* x_scale, const uint32_t*
   for (int e = 0; e < experts; ++e) {
     const int me = expert_offsets[e + 1] - expert_offsets[e];
     if (me > 0) {
-      const size_t b = make_plan(variant, me, N, K, gs).bytes;
+      const size_t b = make_plan(variant, me, N, K, gs, -1).bytes;
       need = b > need ? b : need;
     }
   }

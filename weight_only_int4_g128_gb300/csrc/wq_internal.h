@@ -64,6 +64,9 @@ struct GemmParams {
 // of the process (the context a device gets after cudaDeviceReset has a new
 // one); 0 when no context is current yet or the driver cannot tell.
 unsigned long long current_context_id();
+// Workspace bytes of one GEMM call with activations of x_dtype (WQ_DTYPE_*):
+// wq_workspace_size() returns the most over the activation types.
+size_t gemm_workspace_bytes(int variant, int x_dtype, int M, int N, int K, int group_size);
 
 // A per-device set-up step (a kernel attribute, a device symbol's address)
 // that has to be redone when the device's context is rebuilt, e.g. after
@@ -107,8 +110,11 @@ cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUten
 size_t gemm_smem_bytes(int bt);
 
 // Pre-pass kernels (wq_kernels.cu).
+// Correction columns (kaug > 0) and, for bf16 X (x_kind == kXBF16), the per-token
+// scaled fp16 copy x16 [M][K] with its factors xs [M] that the GEMM reads instead.
 cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int M, int K, int N, int group_size,
-                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, cudaStream_t stream);
+                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, __half* x16, float* xs,
+                             cudaStream_t stream);
 cudaError_t launch_i8_to_f16(const int8_t* Xq, __half* X16, long long count, cudaStream_t stream);
 cudaError_t launch_pack_pair(const uint8_t* q_gate, const __half* scale_gate, const __half* zero_gate,
                              const uint8_t* q_up, const __half* scale_up, const __half* zero_up, uint32_t* Bpacked,

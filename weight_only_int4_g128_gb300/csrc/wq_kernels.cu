@@ -239,11 +239,13 @@ __device__ __forceinline__ void write_aug(__nv_bfloat16* arow, int G, int g, flo
 struct CorrPrep {
   const void* X;
   const float* delta;
-  __nv_bfloat16* aug;
+  __nv_bfloat16* aug;        // null without a correction (symmetric weights)
   __nv_bfloat16* delta_aug;
+  __half* x16;               // bf16 activations: the scaled fp16 copy the GEMM reads
+  float* xs;                 // ... and the per-token factor 2^-e that undoes the scale
   int M, K, N, group_size, G, kaug;
-  int n_sum_blocks;  // blocks of the group-sum part
-  int g_tiles;       // 32-wide group tiles of the delta part
+  int n_sum_blocks;  // blocks of the group-sum part (bf16: one per two token rows)
+  int g_tiles;       // 32-wide group tiles of the delta part (0 without a correction)
 };
 constexpr int kSumItems = 4;  // (token, group pair) items per warp in the 128-group layout
 
@@ -310,6 +312,104 @@ __device__ __forceinline__ void corr_group_sums(const CorrPrep& c, int bid) {
   }
 }
 
+// bf16 activations.  The large-M GEMM multiplies fp16 operands: its weights
+// RN((q - 8) * s) then carry 11 significant bits instead of bf16's 8.  Each token
+// row is scaled by a power of two 2^e that brings its largest magnitude into
+// [2^14, 2^15) and converted to fp16, which holds every bf16 significand, so the
+// copy is exact (values below 2^-14 after scaling, more than 2^28 under the row's
+// largest, lose low bits as fp16 subnormals); xs[m] = 2^-e undoes the scale in the
+// GEMM's epilogue, also exactly.  The group sums are taken over the fp16 values the
+// GEMM reads.  Each half of a 256-thread block takes one row: pass 1 finds the
+// row's largest magnitude, pass 2 reads the row again (from L1 or L2), converts,
+// stores and sums, a half-warp per group of 128.  Few registers, so many rows are
+// in flight per SM.
+constexpr int kRowThreads = 128;  // threads per row: two rows per block
+
+__device__ __forceinline__ float absmax_bf16x8(const uint4 v) {
+  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a = fmaxf(a, fabsf(__uint_as_float(u[i] << 16)));
+    a = fmaxf(a, fabsf(__uint_as_float(u[i] & 0xFFFF0000u)));
+  }
+  return a;
+}
+
+__device__ __forceinline__ void corr_rows_bf16(const CorrPrep& c, int bid) {
+  __shared__ float red[2][4];
+  __shared__ float red_sum[2][4];
+  const int half = threadIdx.x >> 7;
+  const int t = threadIdx.x & (kRowThreads - 1);
+  const int lane = threadIdx.x & 31;
+  const int w = t >> 5;
+  const int m = 2 * bid + half;
+  const bool valid = m < c.M;  // M odd: the last block's second half has no row
+  const int nch = c.K / 8;
+  const uint4* row = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(c.X) +
+                                                    static_cast<size_t>(valid ? m : 0) * c.K);
+  float amax = 0.0f;
+  if (valid) {
+#pragma unroll 4
+    for (int ch = t; ch < nch; ch += kRowThreads) amax = fmaxf(amax, absmax_bf16x8(__ldg(row + ch)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (lane == 0) red[half][w] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(red[half][0], red[half][1]), fmaxf(red[half][2], red[half][3]));
+  if (!valid) return;  // no block-wide barrier follows
+  // amax in [2^(E-127), 2^(E-126)): e = 141 - E puts it in [2^14, 2^15); zero rows
+  // keep e = 0; the cap keeps 2^e a normal fp32 for rows of bf16 subnormals
+  const int E = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int e = (amax == 0.0f) ? 0 : min(141 - E, 126);
+  const float up = __uint_as_float(static_cast<uint32_t>(127 + e) << 23);
+  if (t == 0) c.xs[m] = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+
+  uint4* out = reinterpret_cast<uint4*>(c.x16 + static_cast<size_t>(m) * c.K);
+  const bool g128 = c.group_size == kKBlock;
+  __nv_bfloat16* arow = c.aug ? c.aug + static_cast<size_t>(m) * c.kaug : nullptr;
+  float chan = 0.0f;  // one group per row (per-channel scales): this thread's part
+  // Every lane runs the same trip count (the half-warp reductions need all 32);
+  // nch is a multiple of 16, so a half-warp is all in range or all out.
+#pragma unroll 2
+  for (int b0 = 0; b0 < nch; b0 += kRowThreads) {
+    const int ch = b0 + t;
+    const bool ok = ch < nch;
+    const uint4 v = ok ? __ldg(row + ch) : make_uint4(0u, 0u, 0u, 0u);
+    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = __floats2half2_rn(__uint_as_float(u[i] << 16) * up, __uint_as_float(u[i] & 0xFFFF0000u) * up);
+      o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      s += __low2float(h);
+      s += __high2float(h);
+    }
+    if (ok) out[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+    if (g128) {
+#pragma unroll
+      for (int x = 8; x > 0; x >>= 1) s += __shfl_xor_sync(0xffffffffu, s, x);
+      if (ok && arow && (lane & 15) == 0) write_aug(arow, c.G, ch >> 4, s);
+    } else {
+      chan += s;
+    }
+  }
+  if (arow) {
+    if (!g128) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) chan += __shfl_xor_sync(0xffffffffu, chan, o);
+      if (lane == 0) red_sum[half][w] = chan;
+      // the four warps of this row only (named barrier 1 or 2, 128 threads)
+      if (half == 0) asm volatile("bar.sync 1, 128;" ::: "memory");
+      else asm volatile("bar.sync 2, 128;" ::: "memory");
+      if (t == 0) write_aug(arow, c.G, 0, (red_sum[half][0] + red_sum[half][1]) + (red_sum[half][2] + red_sum[half][3]));
+    }
+    for (int j = 3 * c.G + t; j < c.kaug; j += kRowThreads) arow[j] = __float2bfloat16_rn(0.0f);
+  }
+}
+
 __device__ __forceinline__ void corr_delta_columns(const CorrPrep& c, int tile) {
   __shared__ uint16_t hi_t[32][33];
   __shared__ uint16_t lo_t[32][33];
@@ -355,8 +455,12 @@ template <int XK>
 __global__ void __launch_bounds__(256) corr_prep_kernel(const CorrPrep c) {
   griddep_launch_dependents();
   griddep_wait();
-  if (static_cast<int>(blockIdx.x) < c.n_sum_blocks) corr_group_sums<XK>(c, blockIdx.x);
-  else corr_delta_columns(c, blockIdx.x - c.n_sum_blocks);
+  if (static_cast<int>(blockIdx.x) < c.n_sum_blocks) {
+    if constexpr (XK == kXBF16) corr_rows_bf16(c, blockIdx.x);
+    else corr_group_sums<XK>(c, blockIdx.x);
+  } else {
+    corr_delta_columns(c, blockIdx.x - c.n_sum_blocks);
+  }
 }
 
 __global__ void i8_to_f16_kernel(const int8_t* __restrict__ Xq, __half* __restrict__ X16,
@@ -440,12 +544,15 @@ static cudaLaunchAttribute pdl_attr_k() {
 }
 
 cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int M, int K, int N, int group_size,
-                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, cudaStream_t st) {
+                             int G, int kaug, __nv_bfloat16* aug, __nv_bfloat16* delta_aug, __half* x16, float* xs,
+                             cudaStream_t st) {
   CorrPrep c{};
   c.X = X;
-  c.delta = delta;
-  c.aug = aug;
-  c.delta_aug = delta_aug;
+  c.delta = kaug ? delta : nullptr;
+  c.aug = kaug ? aug : nullptr;
+  c.delta_aug = kaug ? delta_aug : nullptr;
+  c.x16 = x16;
+  c.xs = xs;
   c.M = M;
   c.K = K;
   c.N = N;
@@ -455,8 +562,8 @@ cudaError_t launch_corr_prep(const void* X, int x_kind, const float* delta, int 
   const long long sum_warps = (group_size == kKBlock)
                                   ? (static_cast<long long>(M) * ((G + 1) / 2) + kSumItems - 1) / kSumItems
                                   : static_cast<long long>(M) * G;
-  c.n_sum_blocks = static_cast<int>((sum_warps + 7) / 8);
-  c.g_tiles = (G + 31) / 32;
+  c.n_sum_blocks = (x_kind == kXBF16) ? (M + 1) / 2 : static_cast<int>((sum_warps + 7) / 8);
+  c.g_tiles = kaug ? (G + 31) / 32 : 0;
   const long long blocks = c.n_sum_blocks + static_cast<long long>(c.g_tiles) * (N / 32);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);

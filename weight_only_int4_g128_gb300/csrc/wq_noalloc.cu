@@ -7,7 +7,8 @@
 // into a CUDA graph (cudaMalloc is not a capturable operation), or
 // latency-critical loops where a cudaMalloc may synchronize the device.  This
 // entry point needs no workspace argument: the scratch the GEMM may need (the
-// correction columns of the large-M path) lives in one fixed-size array of
+// correction columns of the large-M path and, for bf16 activations, the
+// per-token scaled fp16 copy of X that path reads) lives in one fixed-size array of
 // device memory that is part of the library image, so every GPU that loads the
 // library holds it until the process exits.  Nothing here allocates.
 #include <cuda_runtime.h>
@@ -61,7 +62,7 @@ extern "C" int wq_gemm_w4a16_noalloc(const void* X, int x_dtype, const uint32_t*
                                      int group_size, void* stream) {
   const int variant = delta ? WQ_VARIANT_W4A16 : WQ_VARIANT_W4A16_SYM;
   // 0 for shapes the GEMM rejects; wq_gemm_w4a16 below reports those itself.
-  const size_t need = (M > 0) ? wq_workspace_size(variant, M, N, K, group_size) : 0;
+  const size_t need = (M > 0) ? wq::gemm_workspace_bytes(variant, x_dtype, M, N, K, group_size) : 0;
   if (need > kScratchBytes) {
     // Too large for the array.  The arguments are still checked first, as the
     // workspace entry checks them: without a workspace wq_gemm_w4a16 returns its
