@@ -81,7 +81,10 @@ struct Cfg {
   // split-K reduction buffer red[splits][128][rpr + 4] (rpr <= BT/splits + 3, splits <= 8)
   static_assert((BT + 64) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
                 "split-K reduction buffer reuses the stage ring");
-  static_assert(BT * kTileN * 4 <= kNSX * kXStageBytes, "the output tile is staged over the activation ring");
+  // the output tile's image (fp32 at most) and the tile's per-token factors are
+  // staged over the activation ring
+  static constexpr int kXsOffset = BT * kTileN * 4;
+  static_assert(kXsOffset + BT * 4 <= kNSX * kXStageBytes, "the output tile is staged over the activation ring");
 };
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -90,21 +93,30 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 
 // Epilogue image of one tile over shared memory: [BT tokens][128 columns] of
 // type YK (row-major, as the TMA store of Y reads it).  This thread owns column
-// `col` and writes tokens 16 c + j of its chunks c = h + 2 i, scaled by xs[token]
-// when xs is given (tokens past mlim, which the store clips, are left unscaled).
-template <int YK, int kCh>
+// `col` and writes tokens 16 c + j of its chunks c = h + 2 i; with XS each value is
+// first multiplied by its token's factor, read per chunk from the factors staged
+// in shared memory at xs_s (1.0 for tokens past M, which the store clips).
+template <int YK, int kCh, bool XS>
 __device__ __forceinline__ void write_image(uint32_t img, int col, int h, const uint32_t (&r)[kCh][16],
-                                            const float* xs, int mlim) {
+                                            uint32_t xs_s) {
   constexpr uint32_t es = (YK == kYF32) ? 4 : 2;
   const uint32_t base = img + static_cast<uint32_t>(col) * es;
 #pragma unroll
   for (int i = 0; i < kCh; ++i) {
     const int c = h + 2 * i;
+    float sc[16];
+    if constexpr (XS) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(sc[4 * q]), "=f"(sc[4 * q + 1]), "=f"(sc[4 * q + 2]), "=f"(sc[4 * q + 3])
+                     : "r"(xs_s + static_cast<uint32_t>(64 * c + 16 * q)));
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       const int ml = 16 * c + j;
       float v = __uint_as_float(r[i][j]);
-      if (xs && ml < mlim) v *= __ldg(xs + ml);
+      if constexpr (XS) v *= sc[j];
       const uint32_t a = base + static_cast<uint32_t>(ml) * (kTileN * es);
       if constexpr (YK == kYF16) {
         asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(__half_as_ushort(__float2half_rn(v))) : "memory");
@@ -468,6 +480,14 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
 
     // ---- epilogue (single K segment): accumulator -> Y
     warp_wait(done_bar, 0, wc);
+    // Every MMA has completed, so the activation ring is idle: the tile's per-token
+    // factors go next to where the image will be (1.0 past M: those rows are clipped).
+    const uint32_t xs_s = sx + C::kXsOffset;
+    if (p.x_scale && p.splits == 1 && !*abort_flag) {
+      const int mlim = min(BT, p.M - m0);
+      float* const xs_g = reinterpret_cast<float*>(gbase + C::kXsOffset);
+      for (int i = threadIdx.x - 64; i < BT; i += 32 * kDqWarps) xs_g[i] = (i < mlim) ? __ldg(p.x_scale + m0 + i) : 1.0f;
+    }
     named_bar_sync(1, 32 * kDqWarps);
     tc_fence_after();
     // The tile's outputs are converted into a [BT tokens][128 columns] image over
@@ -477,7 +497,6 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     const bool store_tile = !*abort_flag && p.splits == 1;  // uniform: no wait can set the flag past here
     if (store_tile) {
       const uint32_t dt = tmem + lane_base + C::kDCol;
-      const int mlim = min(BT, p.M - m0);
       // this warp's 16-column chunks c = h, h + 2, ...: every TMEM load is issued
       // before the one wait, so the load latency is paid once per tile
       constexpr int kCh = BT / 32;
@@ -485,13 +504,22 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
 #pragma unroll
       for (int i = 0; i < kCh; ++i) tmem_ld16(dt + 16 * (h + 2 * i), r[i]);
       tmem_wait_ld();
-      // the output type (and whether a per-token scale applies) is decided once,
+      // the output type and whether a per-token factor applies are decided once,
       // outside the element loop, and every element is one shared-memory store
-      const float* const xs = p.x_scale ? p.x_scale + m0 : nullptr;
+      const bool xs_on = p.x_scale != nullptr;
       switch (p.y_kind) {
-        case kYF16: write_image<kYF16, kCh>(sx, row, h, r, xs, mlim); break;
-        case kYBF16: write_image<kYBF16, kCh>(sx, row, h, r, xs, mlim); break;
-        default: write_image<kYF32, kCh>(sx, row, h, r, xs, mlim); break;
+        case kYF16:
+          if (xs_on) write_image<kYF16, kCh, true>(sx, row, h, r, xs_s);
+          else write_image<kYF16, kCh, false>(sx, row, h, r, xs_s);
+          break;
+        case kYBF16:
+          if (xs_on) write_image<kYBF16, kCh, true>(sx, row, h, r, xs_s);
+          else write_image<kYBF16, kCh, false>(sx, row, h, r, xs_s);
+          break;
+        default:
+          if (xs_on) write_image<kYF32, kCh, true>(sx, row, h, r, xs_s);
+          else write_image<kYF32, kCh, false>(sx, row, h, r, xs_s);
+          break;
       }
       fence_proxy_async_smem();  // the image's generic writes become visible to the TMA store
     }
