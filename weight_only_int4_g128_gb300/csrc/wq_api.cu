@@ -434,12 +434,12 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
   p.y_kind = y_kind;
   p.timeout_ns = timeout_ns();
   p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
-  // Y for the epilogue's tile store: [M][N], boxes of {128 columns, bt tokens}
+  // Y for the epilogue's tile stores: [M][N], boxes of {128 columns, 16 tokens}
   CUtensorMap tm_y;
   const CUtensorMapDataType ydt = y_kind == wq::kYF32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                   : y_kind == wq::kYBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-  rc = make_map(&tm_y, ydt, y_kind == wq::kYF32 ? 4 : 2, Y, M, N, plan.bt, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
+  rc = make_map(&tm_y, ydt, y_kind == wq::kYF32 ? 4 : 2, Y, M, N, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
   e = wq::launch_gemm(plan.bt, gk, tm_x, tm_aug, tm_s, tm_y, p, st);
   return after_launch(e, name, st);

@@ -78,8 +78,19 @@ struct Cfg {
   static_assert(!kTwoPerSM || kSmemBytes + 1024 <= 116 * 1024, "two CTAs per SM");
   static_assert(kNSA * 64 <= kDCol, "TMEM budget");
   static_assert(kNSA <= kNSX, "mma_done is indexed by stage");
-  // split-K reduction buffer red[splits][128][rpr + 4] (rpr <= BT/splits + 3, splits <= 8)
-  static_assert((BT + 64) * kTileN * 4 <= kNSX * (kXStageBytes + kWStageBytes),
+  // split-K: the reduction buffer red[splits][128][rpr + 4] fp32 (rows of the tile
+  // per rank rounded up to 16) and the owner's output image [rpr][128] (fp32 at
+  // most) after it, over the idle activation and weight rings
+  static constexpr int split_rpr(int splits) { return ((BT + splits - 1) / splits + 15) & ~15; }
+  static constexpr int split_bytes(int splits) {
+    return splits * kTileN * (split_rpr(splits) + 4) * 4 + split_rpr(splits) * kTileN * 4;
+  }
+  static constexpr int split_bytes_max() {
+    int m = 0;
+    for (int k = 2; k <= 8; ++k) m = split_bytes(k) > m ? split_bytes(k) : m;
+    return m;
+  }
+  static_assert(split_bytes_max() <= kNSX * (kXStageBytes + kWStageBytes),
                 "split-K reduction buffer reuses the stage ring");
   // the output tile's image (fp32 at most) and the tile's per-token factors are
   // staged over the activation ring
@@ -525,7 +536,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     }
     named_bar_sync(1, 32 * kDqWarps);
     if (store_tile && warp == 2 && lane == 0) {
-      tma_store_2d(&tm_y, sx, n0, m0);
+      const uint32_t box = 16u * kTileN * ((p.y_kind == kYF32) ? 4u : 2u);
+      for (int b = 0; 16 * b < BT && m0 + 16 * b < p.M; ++b) tma_store_2d(&tm_y, sx + b * box, n0, m0 + 16 * b);
       bulk_commit_group();
       bulk_wait_group_read0();  // the image is read before the CTA's shared memory is released
     }
@@ -548,13 +560,13 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
 
   // ---- split-K over a thread-block cluster (the K segments of one output tile).
   // Rows (tokens) [r*rpr, (r+1)*rpr) of the tile belong to rank r (rpr a multiple
-  // of 4).  Every CTA pushes its fp32 partial of those rows into rank r's shared
-  // memory with 16-byte remote stores, laid out red[src][row][rpr_pad] (rows are
-  // the 128 weight rows of the tile); the owner sums the partials in rank order
-  // (deterministic) and writes Y.
+  // of 16).  Every CTA pushes its fp32 partial of those rows into rank r's shared
+  // memory with 16-byte stores (remote for the other ranks), laid out
+  // red[src][row][rpr_pad] (rows are the 128 weight rows of the tile); the owner
+  // sums the partials in rank order (deterministic) and stores its rows of Y.
   if (p.splits > 1) {
     const int splits = p.splits;
-    const int rpr = ((BT + splits - 1) / splits + 3) & ~3;
+    const int rpr = C::split_rpr(splits);  // a multiple of 16: whole 16-row store boxes
     const int rpr_pad = rpr + 4;  // breaks shared-memory bank conflicts between rows
     const int mlim = min(BT, p.M - m0);
     const bool math = warp >= 2;
@@ -586,23 +598,34 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
           if (ml < mlim) {
             const int owner = ml / rpr;
             const int local = ml - owner * rpr;
-            const uint32_t addr = mapa_shared(red_row + static_cast<uint32_t>(local * 4), owner);
-            if (aborted) {
-              const float nanv = __int_as_float(0x7fc00000);
-              st_dsmem_v4(addr, nanv, nanv, nanv, nanv);
-            } else {
-              st_dsmem_v4(addr, __uint_as_float(r[i][j]), __uint_as_float(r[i][j + 1]),
-                          __uint_as_float(r[i][j + 2]), __uint_as_float(r[i][j + 3]));
-            }
+            const uint32_t la = red_row + static_cast<uint32_t>(local * 4);
+            const float nanv = __int_as_float(0x7fc00000);
+            const float v0 = aborted ? nanv : __uint_as_float(r[i][j]);
+            const float v1 = aborted ? nanv : __uint_as_float(r[i][j + 1]);
+            const float v2 = aborted ? nanv : __uint_as_float(r[i][j + 2]);
+            const float v3 = aborted ? nanv : __uint_as_float(r[i][j + 3]);
+            // rows this CTA owns stay in its own shared memory (a plain store);
+            // the others go to their owner over the cluster
+            if (owner == seg)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(la), "f"(v0), "f"(v1), "f"(v2), "f"(v3)
+                           : "memory");
+            else
+              st_dsmem_v4(mapa_shared(la, owner), v0, v1, v2, v3);
           }
         }
       }
       tc_fence_before();
     }
     cluster_sync_all();  // all pushes landed
-    if (math) {
-      const int lo = seg * rpr;
-      const int hi = min(mlim, lo + rpr);
+    // The owner sums its rows' partials in rank order (deterministic) into an image
+    // [rpr tokens][128 columns] of Y's type after the reduction buffer, which TMA
+    // stores of 16-token boxes write to Y (rows past M are clipped by the map).
+    const int lo = seg * rpr;
+    const int hi = min(mlim, lo + rpr);
+    const uint32_t img = smem_u32(red) + static_cast<uint32_t>(splits * kTileN * rpr_pad * 4);
+    if (math && !*abort_flag) {
+      const uint32_t ecol = static_cast<uint32_t>(row) * ((p.y_kind == kYF32) ? 4u : 2u);
+      const uint32_t pitch = (p.y_kind == kYF32) ? kTileN * 4u : kTileN * 2u;
       for (int l4 = 4 * h; lo + l4 < hi; l4 += 8) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int src = 0; src < splits; ++src) {
@@ -612,18 +635,32 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
           acc.z += v.z;
           acc.w += v.w;
         }
-        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        if (p.x_scale) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) a4[e] *= (lo + l4 + e < hi) ? __ldg(p.x_scale + m0 + lo + l4 + e) : 1.0f;
+        }
+        const uint32_t a0 = img + static_cast<uint32_t>(l4) * pitch + ecol;
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int ml = lo + l4 + e;
-          if (ml < hi) {
-            const int m = m0 + ml;
-            float val = a4[e];
-            if (p.x_scale) val *= __ldg(p.x_scale + m);
-            store_y_any(p.Y, p.y_kind, static_cast<size_t>(m) * p.N + n, val);
-          }
+          const uint32_t a = a0 + static_cast<uint32_t>(e) * pitch;
+          if (p.y_kind == kYF16)
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(__half_as_ushort(__float2half_rn(a4[e]))) : "memory");
+          else if (p.y_kind == kYBF16)
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(__bfloat16_as_ushort(__float2bfloat16_rn(a4[e])))
+                         : "memory");
+          else
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(a), "r"(__float_as_uint(a4[e])) : "memory");
         }
       }
+      fence_proxy_async_smem();  // the image's generic writes become visible to the TMA stores
+    }
+    __syncthreads();
+    if (warp == 2 && lane == 0 && !*abort_flag && hi > lo) {
+      const uint32_t box = 16u * kTileN * ((p.y_kind == kYF32) ? 4u : 2u);
+      for (int b = 0; lo + 16 * b < hi; ++b) tma_store_2d(&tm_y, img + b * box, n0, m0 + lo + 16 * b);
+      bulk_commit_group();
+      bulk_wait_group_read0();  // the image is read before the CTA's shared memory is released
     }
   }
 

@@ -104,7 +104,7 @@ int gemv_plan(int M, int N, int K, int group_size, bool has_delta, int* splits, 
 bool gemv_plan_fits(int M, int kbps, int splits, bool per_channel, bool has_delta, bool pair = false);
 int decode_b_rows();  // rows of the activation-component tensor (3 x 16 components + sums/factors)
 unsigned* status_word();
-// tm_y: Y [M][N] with boxes of {128 columns, bt tokens} (the one-segment epilogue's TMA store).
+// tm_y: Y [M][N] with boxes of {128 columns, 16 tokens} (the epilogue's TMA stores).
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
                         const CUtensorMap& tm_s, const CUtensorMap& tm_y, const GemmParams& p, cudaStream_t stream);
 size_t gemm_smem_bytes(int bt);
