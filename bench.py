@@ -113,13 +113,36 @@ def kernels_for(s):
     9..16 tokens the activation pre-pass and the e4m3 decode kernel, beyond that the
     int8 -> fp16 pre-pass and the large-M kernel."""
     M = s["M"]
+    gemm = ["gemm_kernel"] * (2 if M > 16 and large_m_tail(M, s["N"], s["K"]) else 1)
     if s["mode"] == "w4a8":
-        return ["decode_prep_kernel", "decode_kernel"] if M <= 16 else ["i8_to_f16_kernel", "gemm_kernel"]
+        return ["decode_prep_kernel", "decode_kernel"] if M <= 16 else ["i8_to_f16_kernel"] + gemm
     if M <= 8:
         return ["gemv_kernel"]
     if M <= 16:
         return ["decode16_kernel"]
-    return ["corr_prep_kernel", "gemm_kernel"]
+    return ["corr_prep_kernel"] + gemm
+
+
+def large_m_tail(M, N, K, sms=152, max_splits=8) -> bool:
+    """Whether a large-M call runs its last, partial wave of tiles as a second launch
+    split along K (the library's plan: token tiles of 32/64/128/256, two CTAs per SM
+    up to 64 tokens, as many K segments as fill one wave; with one segment per tile
+    of at least 96 k-blocks, a last wave at most half full goes to the second launch)."""
+    bt = 32 if M <= 32 else 64 if M <= 64 else 128 if M <= 128 else 256
+    slots = 2 * sms if bt <= 64 else sms
+    tiles = (N // 128) * (-(-M // bt))
+    kb = K // 128
+    splits = min(max(1, slots // tiles), max_splits, kb)
+    kbps = -(-kb // splits)
+    splits = -(-kb // kbps)
+    if splits != 1 or tiles <= slots or kb < 96:
+        return False
+    rest = tiles % slots
+    if rest == 0 or 2 * rest > slots:
+        return False
+    ts = min(slots // rest, max_splits, kb)
+    kbps = -(-kb // ts)
+    return -(-kb // kbps) > 1
 
 
 def kernel_launches(s) -> int:

@@ -104,7 +104,14 @@ def test_workload_shapes_and_dispatch_table():
     k = {bench.label(s): bench.kernels_for(s) for s in sh}
     assert k["c1 M1 K4096 N4096"] == ["gemv_kernel"]
     assert k["c1 M16 K4096 N11008"] == ["decode16_kernel"]
+    # c3 K17408: 640 tiles of 256 tokens leave the last wave of 152 one-CTA slots 32
+    # tiles of 136 k-blocks: those go to a second, K-split launch; with K = 5120 (40
+    # k-blocks) the split does not pay and the last wave stays partial
     assert k["c3 M4096 K5120 N17408"] == ["corr_prep_kernel", "gemm_kernel"]
+    assert k["c3 M4096 K17408 N5120"] == ["corr_prep_kernel", "gemm_kernel", "gemm_kernel"]
     assert k["c4 M16 K5120 N17408"] == ["decode_prep_kernel", "decode_kernel"]
     assert k["c4 M2048 K5120 N17408"] == ["i8_to_f16_kernel", "gemm_kernel"]
+    # one partial wave (136 tiles), or a last wave more than half full: one launch
+    assert k["c4 M256 K5120 N17408"] == ["i8_to_f16_kernel", "gemm_kernel"]
+    assert not bench.large_m_tail(4096, 8192, 8192)  # 1024 tiles: last wave 112 of 152
     assert bench.headline_unit("sweep") == "TFLOP/s" and bench.headline_unit("c1") == "GB/s"

@@ -154,6 +154,21 @@ def test_large_m_precision(wq, M, K, N, gs, adt):
     assert err <= TOL_LARGE_M, err
 
 
+@pytest.mark.parametrize("M,K,N,gs,adt,odt", [(300, 12288, 10240, 128, "f16", torch.float16),
+                                              (280, 13312, 10240, -1, "bf16", torch.float32)])
+def test_large_m_last_wave_split_along_k(wq, M, K, N, gs, adt, odt):
+    """2 x 80 = 160 tiles of 256 tokens and 96 or more k-blocks: the last wave of 152
+    one-CTA slots holds 8 tiles, which run as a second launch split along K (a cluster
+    per tile).  Those tiles (rows 256.., the last 8 column tiles) and tiles of the first
+    launch are checked against the oracle."""
+    d = synth.make_inputs(1700 + M, M, K, N, group_size=gs, a_dtype=adt)
+    Y, _ = _w4a16(wq, d, odt)
+    got = Y.double().cpu().numpy()
+    for c in [(N - 1024, N), (0, 256)]:
+        err = oracle.rel_fro(got[:, c[0]:c[1]], _ref_w4a16(d, cols=c))
+        assert err <= TOL_LARGE_M, (c, err)
+
+
 def test_bf16_rows_of_any_magnitude(wq):
     """bf16 rows far outside fp16's range (1e30, 1e-30), near its limits (1e4 -> values
     above 65504, 1e-6 -> fp16 subnormals) and all-zero rows: each token row is scaled by
@@ -451,12 +466,19 @@ def test_host_buffer_entry_matches_device_entry(wq, M, K, N, adt, sym, ydt):
 ])
 def test_host_buffer_entry_pipelined_chunks(wq, M, K, N, adt, ydt):
     """gemm_w4a16_host with M >= 2048 runs row chunks in a pipeline (copies in and out on
-    internal streams overlapping the chunk GEMMs).  With one K segment per tile the chunk
-    boundaries (multiples of 256 rows) fall on token-tile boundaries, so the result equals
-    the device entry's bit for bit; sampled rows match the oracle; two calls in a row."""
+    internal streams overlapping the chunk GEMMs): min(4, M / 1024) chunks of rows rounded
+    up to 256.  The result equals the device entry called on the same row chunks bit for
+    bit (the whole-M device call may tile its last wave differently, so it is compared
+    within the large-M bar); sampled rows match the oracle; two calls in a row."""
     d = synth.make_inputs(4200 + M, M, K, N, a_dtype=adt)
-    Yd, (Bp, S, dl) = _w4a16(wq, d, out_dtype=ydt)
-    hX = _x(d).cpu().pin_memory()
+    Yfull, (Bp, S, dl) = _w4a16(wq, d, out_dtype=ydt)
+    X = _x(d)
+    chunks = min(4, M // 1024)
+    rows_c = ((M + chunks - 1) // chunks + 255) // 256 * 256
+    Yd = torch.cat([wq.gemm_w4a16(X[r0:r0 + rows_c], Bp, S, dl, 128, ydt) for r0 in range(0, M, rows_c)])
+    torch.cuda.synchronize()
+    assert oracle.rel_fro(Yd.double().cpu().numpy(), Yfull.double().cpu().numpy()) <= TOL_LARGE_M
+    hX = X.cpu().pin_memory()
     hY = torch.empty((M, N), dtype=ydt).pin_memory()
     for _ in range(2):
         hY.fill_(float("nan"))

@@ -172,6 +172,9 @@ struct Plan {
   int splits;
   int kb_per_split;
   int kaug;       // large-M correction length (0 without correction or for the decode kernel)
+  // large M, one K segment per tile: the last, partial wave of tiles as a second
+  // launch split along K (0 tiles: none)
+  int tail_tiles, tail_splits, tail_kbps;
   size_t off_aug, off_daug, off_x16, off_xs;  // byte offsets into the workspace (large M)
   size_t off_x8;                      // byte offset into the workspace (decode)
   size_t bytes;
@@ -203,6 +206,30 @@ Plan make_plan(int variant, int M, int N, int K, int gs, int x_kind) {
   if (splits > kb) splits = kb;
   p.kb_per_split = (kb + splits - 1) / splits;
   p.splits = (kb + p.kb_per_split - 1) / p.kb_per_split;
+  // Equal tiles leave the last wave partly empty: with T tiles over S CTA slots the
+  // call takes ceil(T / S) tile times.  When the last wave holds at most half the
+  // slots, its tiles go to a second launch, split along K so that they fill it
+  // (a cluster per tile, as above), and take a fraction of a tile time.
+  // Measured on this part, a K-split tile pays ~10 us more than a whole one (the
+  // cluster reduction), and a partial last wave otherwise lets the next call's
+  // pre-pass start on the idle SMs: the tail launch pays off only for long K
+  // segments (c3's K = 17408: -3.6 %; K = 5120: +2 to +6 %), so it is used from
+  // 96 k-blocks on.
+  if (!p.gemv && p.splits == 1 && tiles > slots && kb >= 96) {
+    const int rest = tiles % slots;
+    if (rest > 0 && 2 * rest <= slots) {
+      int ts = slots / rest;
+      if (ts > kMaxClusterSplits) ts = kMaxClusterSplits;
+      if (ts > kb) ts = kb;
+      const int kbps = (kb + ts - 1) / ts;
+      ts = (kb + kbps - 1) / kbps;
+      if (ts > 1) {
+        p.tail_tiles = rest;
+        p.tail_splits = ts;
+        p.tail_kbps = kbps;
+      }
+    }
+  }
   const bool corr = variant == WQ_VARIANT_W4A16 || variant == WQ_VARIANT_W4A8_ASYM;
   const bool int8x = variant == WQ_VARIANT_W4A8 || variant == WQ_VARIANT_W4A8_ASYM;
   p.kaug = (!p.gemv && corr) ? ((3 * G + 127) / 128) * 128 : 0;
@@ -441,7 +468,20 @@ int gemm_core(const void* X, int x_kind, const uint32_t* Bpacked, const void* S,
                                                          : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   rc = make_map(&tm_y, ydt, y_kind == wq::kYF32 ? 4 : 2, Y, M, N, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (rc) return rc;
+  const int tiles = (N / 128) * ((M + plan.bt - 1) / plan.bt);
+  p.tile_base = 0;
+  p.tile_count = tiles - plan.tail_tiles;
+  p.tail = plan.tail_tiles > 0 ? 2 : 0;
   e = wq::launch_gemm(plan.bt, gk, tm_x, tm_aug, tm_s, tm_y, p, st);
+  if (e == cudaSuccess && plan.tail_tiles > 0) {
+    // the last, partial wave: its own launch, each tile split along K
+    p.tile_base = p.tile_count;
+    p.tile_count = plan.tail_tiles;
+    p.tail = 1;
+    p.splits = plan.tail_splits;
+    p.kb_per_split = plan.tail_kbps;
+    e = wq::launch_gemm(plan.bt, gk, tm_x, tm_aug, tm_s, tm_y, p, st);
+  }
   return after_launch(e, name, st);
 }
 

@@ -188,8 +188,11 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTileN;
-  const int m0 = blockIdx.y * BT;
+  const int tile = p.tile_base + static_cast<int>(blockIdx.x);  // column tile fastest
+  const int ntiles = p.N / kTileN;
+  const int n_tile = tile % ntiles;
+  const int n0 = n_tile * kTileN;
+  const int m0 = (tile / ntiles) * BT;
   const int seg = blockIdx.z;
   const int kb0 = seg * p.kb_per_split;
   const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
@@ -234,12 +237,22 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // Programmatic dependent launch: the next grid in the stream may be scheduled
-  // now (a grid of this library waits for this one to complete before it touches
-  // memory this one uses); nothing here reads or writes memory a preceding grid
-  // may write (X, the correction columns of the pre-pass, Y) before the wait.
-  griddep_launch_dependents();
-  griddep_wait();
+  // Programmatic dependent launch.  Nothing here reads or writes memory a preceding
+  // grid may write (X, the correction columns of the pre-pass, Y) before the wait.
+  // The next grid in the stream may be scheduled at once (it waits for this one to
+  // complete before it touches memory this one uses), except after a main launch
+  // with a tail (tail == 2): only once every CTA of it is past its wait, so that the
+  // tail launch starts after the pre-pass completed.  The tail launch (tail == 1)
+  // does not wait for the main launch (they write disjoint tiles and read what the
+  // pre-pass wrote); it waits before exiting, so its completion implies the main
+  // launch's.
+  if (p.tail == 2) {
+    griddep_wait();
+    griddep_launch_dependents();
+  } else {
+    griddep_launch_dependents();
+    if (p.tail == 0) griddep_wait();
+  }
 
   int issued = 0;         // stages whose activation tile the producer lane has issued
   int w_issued = 0;       // stages whose weight side the producer lane has issued
@@ -269,7 +282,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
         }
         mbar_arrive_expect_tx(full_w(s2), C::kWStageBytes);
         // packed weight tile: one contiguous 8 KB block of the blocked layout
-        bulk_load(sw + s2 * C::kWStageBytes, p.B + (static_cast<size_t>(blockIdx.x) * p.kb_total + kb) * 2048,
+        bulk_load(sw + s2 * C::kWStageBytes, p.B + (static_cast<size_t>(n_tile) * p.kb_total + kb) * 2048,
                   C::kWStageBytes, full_w(s2));
         return true;
       };
@@ -673,6 +686,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (p.tail == 1) griddep_wait();
 }
 
 template <int BT, int XK>
@@ -690,7 +704,9 @@ static cudaError_t launch_bt(const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
     attr_set.done(dev);
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.N / kTileN, (p.M + BT - 1) / BT, p.splits);
+  const int tiles = (p.N / kTileN) * ((p.M + BT - 1) / BT);
+  const int count = (p.tail == 1) ? tiles - p.tile_base : (p.tile_count > 0 ? p.tile_count : tiles);
+  cfg.gridDim = dim3(count, 1, p.splits);
   cfg.blockDim = dim3(kGemmThreads, 1, 1);
   cfg.dynamicSmemBytes = C::kSmemBytes;
   cfg.stream = st;

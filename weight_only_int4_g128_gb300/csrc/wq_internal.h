@@ -47,6 +47,15 @@ struct GemmParams {
   int y_kind;
   unsigned long long timeout_ns;
   int weight_prefetch;   // issue weight copies before waiting on the preceding grid
+  // Large-M kernel: this launch covers tiles [tile_base, tile_base + gridDim.x) of
+  // the (column tile fastest) tile order.  tail = 1: the launch finishes the last,
+  // partial wave of tiles of the launch just before it on the stream (same call,
+  // split along K): it starts without waiting for that launch, which (tail = 2) let
+  // it start only after the call's pre-pass had completed, and waits for it before
+  // exiting.
+  int tile_base;
+  int tile_count;  // tiles of a main launch (0: all of them); a tail launch takes the rest
+  int tail;
   // Grouped (mixture-of-experts) launch of the weight-streaming decode kernel:
   // blockIdx.z = expert e, whose token rows are goff[e] .. goff[e+1] of X and Y
   // and whose weights sit b_stride words / sd_stride elements after expert 0's.
