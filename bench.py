@@ -653,7 +653,8 @@ def run_gpu(args, shapes, ws, rank, local):
     tr = load_traffic(hk, head_probs[0]["s"])
     roofline.update({
         "kernel": f"wq::{hk}",
-        "launches_per_step": n_launch,
+        "calls_per_step": n_launch,
+        "launches_per_step": sum(kernel_launches(p["s"]) for p in head_probs),
         "time": (f"device time of the {head_cfg} calls inside the {args.steps} timed steps "
                  f"(CUDA events on the launching stream), {1e3 * cfg_ms[head_cfg] / n_launch:.1f} us per call"
                  + (" including its pre-pass launch" if len(kernels_for(head_probs[0]['s'])) > 1 else "")),
