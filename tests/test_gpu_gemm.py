@@ -169,6 +169,25 @@ def test_large_m_last_wave_split_along_k(wq, M, K, N, gs, adt, odt):
         assert err <= TOL_LARGE_M, (c, err)
 
 
+@pytest.mark.parametrize("M,K,N,gs,adt,odt,sym", [
+    (600, 1024, 16384, 128, "f16", torch.float16, False),   # 384 tiles, 9 stages per tile (odd)
+    (520, 1152, 16384, 128, "bf16", torch.float16, False),  # 9 k-blocks + a correction stage: 10 (even)
+    (700, 1024, 12288, -1, "f16", torch.float16, True),     # symmetric, one group per column: 8 stages
+])
+def test_large_m_several_waves(wq, M, K, N, gs, adt, odt, sym):
+    """More than one wave of 256-token tiles (288 or 384 tiles over 152 one-CTA slots),
+    odd and even stage counts per tile, the last token tile ragged: column windows at
+    the start, middle and end against the oracle, and a repeat call bit-equal."""
+    d = synth.make_inputs(1800 + M, M, K, N, group_size=gs, a_dtype=adt)
+    Y, _ = _w4a16(wq, d, odt, sym=sym)
+    got = Y.double().cpu().numpy()
+    for c in [(0, 384), (N // 2 - 128, N // 2 + 128), (N - 384, N)]:
+        err = oracle.rel_fro(got[:, c[0]:c[1]], _ref_w4a16(d, sym=sym, cols=c))
+        assert err <= TOL_LARGE_M, (c, err)
+    Y2, _ = _w4a16(wq, d, odt, sym=sym)
+    assert torch.equal(Y, Y2)
+
+
 def test_bf16_rows_of_any_magnitude(wq):
     """bf16 rows far outside fp16's range (1e30, 1e-30), near its limits (1e4 -> values
     above 65504, 1e-6 -> fp16 subnormals) and all-zero rows: each token row is scaled by
