@@ -194,8 +194,10 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
   const int n0 = n_tile * kTileN;
   const int m0 = (tile / ntiles) * BT;
   const int seg = blockIdx.z;
-  const int kb0 = seg * p.kb_per_split;
-  const int kb1 = min(p.kb_total, kb0 + p.kb_per_split);
+  // segment 0 carries the correction stages, so it may take fewer k-blocks
+  const int kb_first = p.kb_first > 0 ? p.kb_first : p.kb_per_split;
+  const int kb0 = (seg == 0) ? 0 : kb_first + (seg - 1) * p.kb_per_split;
+  const int kb1 = min(p.kb_total, (seg == 0) ? kb_first : kb0 + p.kb_per_split);
   const int n_aug = (seg == 0) ? p.aug_stages : 0;
   const int n_stages = n_aug + max(0, kb1 - kb0);
   // group size is 128 (group = k-block) or K (one group per column)

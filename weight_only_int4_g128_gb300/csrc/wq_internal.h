@@ -34,6 +34,8 @@ struct GemmParams {
   int G;                 // number of groups
   int kb_total;          // K / 128
   int kb_per_split;      // k-blocks per split segment
+  int kb_first;          // large-M kernel: k-blocks of segment 0, which also runs the
+                         // correction stages (0: kb_per_split like the others)
   int splits;            // number of K segments (one thread-block cluster per tile)
   int aug_stages;        // correction stages (Kaug / 128), 0 when there is no correction
   int kaug;              // padded correction length (multiple of 128)
