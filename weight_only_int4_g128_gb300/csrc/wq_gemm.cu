@@ -263,6 +263,9 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const WaitCtx wc{abort_flag, p.timeout_ns, kDevTimeoutProducer, &g_status};
+      // A weight tile is read again by every token tile's CTA, waves apart; Y is
+      // written once: weights stay in L2 ahead of the output's lines.
+      const uint64_t pol_w = l2_evict_last();
       // Weight side of stage it2: the packed tile (+ a scale chunk when its k-block
       // starts one); a correction stage has no weight tile and only completes the
       // phase.  Every wait comes before the first copy of the stage.
@@ -284,8 +287,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
         }
         mbar_arrive_expect_tx(full_w(s2), C::kWStageBytes);
         // packed weight tile: one contiguous 8 KB block of the blocked layout
-        bulk_load(sw + s2 * C::kWStageBytes, p.B + (static_cast<size_t>(n_tile) * p.kb_total + kb) * 2048,
-                  C::kWStageBytes, full_w(s2));
+        bulk_load_hint(sw + s2 * C::kWStageBytes, p.B + (static_cast<size_t>(n_tile) * p.kb_total + kb) * 2048,
+                       C::kWStageBytes, full_w(s2), pol_w);
         return true;
       };
       bool ok = n_stages == 0 || issue_w(0);
@@ -552,7 +555,9 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     named_bar_sync(1, 32 * kDqWarps);
     if (store_tile && warp == 2 && lane == 0) {
       const uint32_t box = 16u * kTileN * ((p.y_kind == kYF32) ? 4u : 2u);
-      for (int b = 0; 16 * b < BT && m0 + 16 * b < p.M; ++b) tma_store_2d(&tm_y, sx + b * box, n0, m0 + 16 * b);
+      const uint64_t pol_y = l2_evict_first();
+      for (int b = 0; 16 * b < BT && m0 + 16 * b < p.M; ++b)
+        tma_store_2d_hint(&tm_y, sx + b * box, n0, m0 + 16 * b, pol_y);
       bulk_commit_group();
       bulk_wait_group_read0();  // the image is read before the CTA's shared memory is released
     }
@@ -673,7 +678,8 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     __syncthreads();
     if (warp == 2 && lane == 0 && !*abort_flag && hi > lo) {
       const uint32_t box = 16u * kTileN * ((p.y_kind == kYF32) ? 4u : 2u);
-      for (int b = 0; lo + 16 * b < hi; ++b) tma_store_2d(&tm_y, img + b * box, n0, m0 + lo + 16 * b);
+      const uint64_t pol_y = l2_evict_first();
+      for (int b = 0; lo + 16 * b < hi; ++b) tma_store_2d_hint(&tm_y, img + b * box, n0, m0 + lo + 16 * b, pol_y);
       bulk_commit_group();
       bulk_wait_group_read0();  // the image is read before the CTA's shared memory is released
     }
