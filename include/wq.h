@@ -130,9 +130,11 @@ int wq_pack_w4a16_pair(const uint8_t* q_gate, const void* scale_gate, const void
 int wq_unpack_w4(const uint32_t* Bpacked, uint8_t* q, int K, int N, void* stream);
 
 /*
- * Dequantized symmetric weights, the values the GEMM feeds to the tensor
- * cores: W[k][n] = RN((q - 8) * S[g][n]) rounded once to w_dtype
- * (WQ_DTYPE_F16 or WQ_DTYPE_BF16).  W is [K][N] device, output.
+ * Dequantized symmetric weights: W[k][n] = RN((q - 8) * S[g][n]) rounded once to
+ * w_dtype (WQ_DTYPE_F16 or WQ_DTYPE_BF16).  With WQ_DTYPE_F16 these are the
+ * values the large-M GEMM feeds to the tensor cores, for fp16 and bf16
+ * activations alike; WQ_DTYPE_BF16 gives the same product rounded to bf16.
+ * W is [K][N] device, output.
  */
 int wq_dequant_w4(const uint32_t* Bpacked, const void* S, void* W, int w_dtype, int K, int N,
                   int group_size, void* stream);

@@ -6,9 +6,10 @@
 //   W_sym[k][n] = (q[k][n] - 8) * scale[g][n],  a_sum[m][g] = sum_{k in g} X[m][k]
 // The second term is the zero-point correction; it is accumulated into the
 // same TMEM accumulator as extra "K" steps (see below), so there is no
-// second pass over Y.  For W4A8 (HyperQwen article, "hidden mine") the int8
-// activations arrive converted to fp16, delta is absent and the accumulator
-// is multiplied by the per-token scale in the epilogue.
+// second pass over Y.  The operands are fp16: bf16 activations arrive as a
+// per-token power-of-two scaled fp16 copy (exact) and W4A8's int8 activations
+// (HyperQwen article, "hidden mine") as fp16 (exact); the accumulator is
+// multiplied by the per-token factor (2^-e, or x_scale) in the epilogue.
 //
 // Tiling (swap-AB): one CTA owns 128 output columns n (the MMA's M = 128,
 // i.e. 128 TMEM lanes, one weight row per lane) and BT tokens (the MMA's N).
@@ -17,11 +18,13 @@
 //               contiguous 8 KB block, bulk copy) and the scale row.
 //   warp 1      allocates TMEM; lane 0 issues tcgen05.mma (A from TMEM,
 //               B = activations from shared memory) and tcgen05.commit.
-//   warps 2..9  dequant: two warps per TMEM lane quarter, each thread owns one
-//               weight row and one 64-k half of the k-block, turns its codes
-//               into scaled fp16/bf16 values in registers and stores them into
-//               a TMEM A-stage with tcgen05.st (the weights never pass through
-//               shared memory once dequantized); then the epilogue.
+//   warps 2..9  dequant: each thread owns one weight row (a TMEM lane), turns
+//               its codes into scaled fp16 values in registers and stores them
+//               into a TMEM A-stage with tcgen05.st (the weights never pass
+//               through shared memory once dequantized).  128- and 256-token
+//               tiles: two groups of four warps take alternate stages, a thread
+//               the whole 128-k row; smaller tiles: all eight warps every stage,
+//               a thread one 64-k half.  Then the epilogue.
 // Correction as K-augmentation: a_sum (fp32, computed once by a pre-pass) is
 // split into bf16 hi/lo and laid out as extra activation columns
 // [a_hi | a_lo | a_hi]; the dequant warps write the matching weight-side
@@ -153,6 +156,7 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
                 const __grid_constant__ CUtensorMap tm_s, const __grid_constant__ CUtensorMap tm_y,
                 const GemmParams p) {
   using C = Cfg<BT>;
+  static_assert(XK == kXF16, "fp16 operands (bf16 and int8 activations arrive as fp16)");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -404,28 +408,15 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
           wc4[c] = *reinterpret_cast<const uint4*>(slot + row * 64 + 16 * (c ^ ((row >> 1) & 3)));
         __syncwarp();
         if (lane == 0) mbar_arrive(empty_w(s));
-        if (XK == kXF16) {
-          const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
+        const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
 #pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const uint4& q4 = wc4[w >> 2];
-            const uint32_t word = (w & 3) == 0 ? q4.x : (w & 3) == 1 ? q4.y : (w & 3) == 2 ? q4.z : q4.w;
-            uint32_t o[4];
-            dq8_f16_scaled(word, s2, o);
+        for (int w = 0; w < 16; ++w) {
+          const uint4& q4 = wc4[w >> 2];
+          const uint32_t word = (w & 3) == 0 ? q4.x : (w & 3) == 1 ? q4.y : (w & 3) == 2 ? q4.z : q4.w;
+          uint32_t o[4];
+          dq8_f16_scaled(word, s2, o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
-          }
-        } else {
-          const ScaleBf16 sb = split_scale_bf16(sc);
-#pragma unroll
-          for (int w = 0; w < 16; ++w) {
-            const uint4& q4 = wc4[w >> 2];
-            const uint32_t word = (w & 3) == 0 ? q4.x : (w & 3) == 1 ? q4.y : (w & 3) == 2 ? q4.z : q4.w;
-            uint32_t o[4];
-            dq8_bf16_scaled(word, sb, o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
-          }
+          for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
         }
       }
       tmem_st32(a_tmem, *reinterpret_cast<const uint32_t(*)[32]>(&v[0]));
@@ -474,24 +465,13 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
           if (kb + 1 == kb1 || chunk_of(kb + 1) != o) mbar_arrive(empty_c(slot));  // chunk done
         }
         const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        if (XK == kXF16) {
-          const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
+        const uint32_t s2 = static_cast<uint32_t>(__half_as_ushort(sc)) * 0x00010001u;
 #pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            uint32_t o[4];
-            dq8_f16_scaled(words[w], s2, o);
+        for (int w = 0; w < 8; ++w) {
+          uint32_t o[4];
+          dq8_f16_scaled(words[w], s2, o);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
-          }
-        } else {
-          const ScaleBf16 sb = split_scale_bf16(sc);
-#pragma unroll
-          for (int w = 0; w < 8; ++w) {
-            uint32_t o[4];
-            dq8_bf16_scaled(words[w], sb, o);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
-          }
+          for (int e = 0; e < 4; ++e) v[4 * w + e] = o[e];
         }
       }
       if (it >= C::kNSA) {  // A-stage a was last read by the MMAs of k-block it - kNSA
@@ -742,10 +722,12 @@ static cudaError_t launch_xk(int bt, const CUtensorMap& tm_x, const CUtensorMap&
   }
 }
 
+// fp16 operands only: bf16 activations reach this kernel as their per-token scaled
+// fp16 copy (the correction pre-pass), int8 ones as exact fp16.
 cudaError_t launch_gemm(int bt, int x_kind, const CUtensorMap& tm_x, const CUtensorMap& tm_aug,
                         const CUtensorMap& tm_s, const CUtensorMap& tm_y, const GemmParams& p, cudaStream_t stream) {
-  return x_kind == kXBF16 ? launch_xk<kXBF16>(bt, tm_x, tm_aug, tm_s, tm_y, p, stream)
-                          : launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, tm_y, p, stream);
+  if (x_kind != kXF16) return cudaErrorInvalidValue;
+  return launch_xk<kXF16>(bt, tm_x, tm_aug, tm_s, tm_y, p, stream);
 }
 
 // Device address of the status word (host side), looked up once per device

@@ -131,8 +131,9 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ Bpacked, uint8_t* __r
     q[static_cast<size_t>(8 * w + j) * N + n] = (word >> code_shift(j)) & 0xFu;
 }
 
-// W[k][n] = RN((v - 8) * s) in fp16 or bf16: the same dequant routines the
-// GEMM uses, exposed so the dequantized weights can be checked bit for bit.
+// W[k][n] = RN((v - 8) * s) in fp16 or bf16.  The fp16 routine is the one the
+// large-M GEMM uses (for every activation type), exposed so its dequantized
+// weights can be checked bit for bit; bf16 gives the same product rounded to bf16.
 __global__ void dequant_kernel(const uint32_t* __restrict__ Bpacked, const __half* __restrict__ S,
                                void* __restrict__ W, int w_kind, int K, int N, int group_size) {
   const long long idx = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x;
