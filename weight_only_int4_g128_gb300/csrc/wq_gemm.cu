@@ -573,7 +573,6 @@ __global__ void __launch_bounds__(kGemmThreads, (BT <= 64) ? 2 : 1)
     const int q = warp & 3;
     const int h = math ? (warp - 2) >> 2 : 0;
     const int row = q * 32 + lane;
-    const int n = n0 + row;
     float* const red = reinterpret_cast<float*>(gbase);  // over the (now idle) stage ring
     cluster_sync_all();  // every CTA of the cluster is past its mainloop: rings are free
     if (math) {
