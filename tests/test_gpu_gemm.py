@@ -298,6 +298,23 @@ def test_w4a8_parity(wq, M, K, N):
     assert oracle.rel_fro(y, ref16) <= TOL_W4A8_VS_F16
 
 
+def test_w4a8_last_wave_split_along_k(wq):
+    """W4A8 over 2 x 80 = 160 tiles of 256 tokens with 96 k-blocks: the last wave runs
+    as a K-split second launch whose owners apply the per-token scale at their store;
+    the tail tiles and first-launch tiles against the int8 oracle."""
+    M, K, N = 300, 12288, 10240
+    d = synth.make_inputs(1950, M, K, N, mode="w4a8")
+    Xq, xs = oracle.quantize_per_token(d["A"])
+    Bp, S = wq.pack_w4a8(_cuda(d["q"]), _cuda(d["scale"]), 128)
+    Y = wq.gemm_w4a8(_cuda(Xq), _cuda(xs), Bp, S, 128, torch.float32)
+    torch.cuda.synchronize()
+    qf, sf = oracle.fold(d["q"], oracle.half_bits(d["scale"]), 128)
+    y = Y.double().cpu().numpy()
+    for c in [(N - 1024, N), (0, 256)]:
+        ref8 = oracle.gemm_w4a8(Xq, xs, qf, sf, 128, cols=c)
+        assert oracle.rel_fro(y[:, c[0]:c[1]], ref8) <= TOL_W4A8, c
+
+
 @pytest.mark.parametrize("M,K", [(1, 4096), (5, 1024), (8, 2048), (12, 1024), (40, 1024), (300, 2048)])
 def test_w4a8_integer_problems_exact(wq, M, K):
     """Unit scales and unit per-token scales make Y = Xq @ (q - 8), an integer below 2^24:
