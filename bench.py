@@ -16,7 +16,7 @@ CUDA-graph replays.  `roofline` is the prefill kernel against the dense bf16
 tensor peak; `rooflines` holds each regime's kernel against its own bound.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wq|reference]
-                    [--workload sweep|c0|c1|c2|c3|c4|moe|moe8|swiglu]
+                    [--workload sweep|c0|c1|c2|c3|c4|moe|moe8|swiglu|mlp]
 
 --impl reference times the CPU oracle (plain C, fp64, naive loops) on a bounded
 sample of the same workload.  Under torchrun each rank runs an independent
@@ -59,6 +59,8 @@ WORKLOAD_NAMES = {
     "moe": "W4A16 asym grouped (mixture of experts): 16 tokens top-1 over 8 experts, K256 N7168 g128 fp16",
     "moe8": "W4A8 zero-point grouped (mixture of experts): 16 int8 per-token rows top-1 over 8 experts, K256 N7168 g128",
     "swiglu": "W4A16 asym fused SwiGLU gate/up pair, decode M{1,4} K4096 N11008 (x2 projections) g128 fp16",
+    "mlp": "W4A16 asym decode MLP block M{1,4}: gate/up pair K4096 N11008 (x2, SwiGLU) then down K11008 N4096, "
+           "g128 fp16, one persistent chain launch per block",
 }
 # The unit of a single-configuration workload's `value`: TFLOP/s where the tensor cores
 # bound most of its shapes, weight GB/s where the weight stream does.
@@ -1065,6 +1067,197 @@ def run_swiglu(args, ws, rank, local):
     return 0
 
 
+def mlp_weight_bytes(d) -> int:
+    """Weight bytes of one decode MLP block: codes, scales and delta of gate, up and down."""
+    total = 0
+    for w in (d["gate"], d["up"], d["down"]):
+        K, N = w["q"].shape
+        G = w["scale"].shape[0]
+        total += K * N // 2 + G * N * 6
+    return total
+
+
+def mlp_oracle(d, budget_s, cols: int = 256):
+    """The oracle on column windows: the pair on `cols` of its columns and the down
+    projection on `cols` of its outputs (its input a seeded stand-in for the pair's
+    output), every token count, until budget_s."""
+    import oracle
+    gs = synth.MLP["group_size"]
+    win = lambda w: (np.ascontiguousarray(w["q"][:, :cols]), oracle.half_bits(w["scale"][:, :cols]),
+                     oracle.half_bits(w["zero"][:, :cols]))
+    gate, up, down = win(d["gate"]), win(d["up"]), win(d["down"])
+    F = d["down"]["q"].shape[0]
+    H = [synth.make_activations(synth.MLP["seed"] + 20 + i, A.shape[0], F).astype(np.float64)
+         for i, A in enumerate(d["A"])]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        for A, h in zip(d["A"], H):
+            oracle.gemm_swiglu_pair(A.astype(np.float64), gate, up, gs)
+            oracle.gemm_asym_plain(h, down[0], down[1], down[2], gs)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    wb = 0
+    for w in (d["gate"], d["up"], d["down"]):
+        K = w["q"].shape[0]
+        wb += K * cols // 2 + w["scale"].shape[0] * cols * 6
+    wb *= n * len(d["A"])
+    return wb / el / 1e9, el, threads, (f"{n} pass(es) of both token counts on {cols} columns of each projection, "
+                                        "fp64 naive loops")
+
+
+def run_mlp(args, ws, rank, local):
+    """The decode MLP block as one chain launch per token count, against the same block as
+    two single-GEMM calls (fused SwiGLU pair, then down) timed the same way."""
+    d = synth.mlp_inputs()
+    name = WORKLOAD_NAMES["mlp"]
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        gbs, el, threads, sample = mlp_oracle(d, max(2.0, min(20.0, 4.0 * args.steps)))
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": None,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+            "config": {"workload": name, "sampled": True},
+            "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return 0
+    import torch
+    import weight_only_int4_g128_gb300 as wq
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws > 1:
+        torch.distributed.init_process_group("nccl", device_id=dev)
+    wq.load_library(build_if_missing=True)
+    if not wq.device_supported(local):
+        raise RuntimeError("not an sm_103 device")
+    wq.set_weight_prefetch(True)
+    cu = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    gs = synth.MLP["group_size"]
+    g, u, dn = d["gate"], d["up"], d["down"]
+    pair0 = wq.pack_w4a16_pair(cu(g["q"]), cu(g["scale"]), cu(g["zero"]), cu(u["q"]), cu(u["scale"]),
+                               cu(u["zero"]), gs)
+    down0 = wq.pack_w4a16(cu(dn["q"]), cu(dn["scale"]), cu(dn["zero"]), gs)
+    wb = mlp_weight_bytes(d)
+    set_bytes = sum(t.numel() * t.element_size() for t in pair0 + down0)
+    reps = max(1, int(np.ceil(3 * L2_BYTES / set_bytes)) + 1)
+    W = [(pair0, down0)] + [(tuple(t.clone() for t in pair0), tuple(t.clone() for t in down0))
+                            for _ in range(reps - 1)]
+    Xs = [cu(A) for A in d["A"]]
+    F, N = g["q"].shape[1], dn["q"].shape[1]
+    Hs = [torch.empty((X.shape[0], F), dtype=torch.float16, device=dev) for X in Xs]
+    Ys = [torch.empty((X.shape[0], N), dtype=torch.float16, device=dev) for X in Xs]
+    wsp = torch.zeros(16 << 20, dtype=torch.uint8, device=dev)  # chain workspace, zeroed once
+    io_bytes = sum(X.numel() * 2 + Y.numel() * 2 for X, Y in zip(Xs, Ys))
+
+    def chain(X, H, Y, r):
+        (Bp, Sp, Dp), (Bd, Sd, Dd) = W[r]
+        wq.gemm_w4a16_chain(X, [{"B": Bp, "S": Sp, "delta": Dp, "pair": True, "out": H},
+                                {"B": Bd, "S": Sd, "delta": Dd, "src": 0, "out": Y}], workspace=wsp)
+
+    def two_calls(X, H, Y, r):
+        (Bp, Sp, Dp), (Bd, Sd, Dd) = W[r]
+        wq.gemm_w4a16_swiglu(X, Bp, Sp, Dp, gs, out=H)
+        wq.gemm_w4a16(H, Bd, Sd, Dd, gs, out=Y)
+
+    def timed(fn):
+        def step(r):
+            for X, H, Y in zip(Xs, Hs, Ys):
+                fn(X, H, Y, r)
+        for r in range(reps):
+            step(r)
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream(device=dev)
+        graphs, graphs1 = build_step_graphs(torch, stream, reps, step, STEPS_PER_GRAPH)
+        with torch.cuda.stream(stream):
+            replay_steps(graphs, graphs1, args.warmup, STEPS_PER_GRAPH)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            replay_steps(graphs, graphs1, args.steps, STEPS_PER_GRAPH)
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps, stream
+
+    ms_two, _ = timed(two_calls)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    ms, stream = timed(chain)
+    clocks.stop()
+    clk = clocks.summary()
+    if ws > 1:
+        torch.distributed.barrier()
+    calls = len(Xs)
+    value = job_rate(ws, calls * wb + io_bytes, ms)
+    peaks, src = load_peaks()
+    achieved = calls * wb / (ms * 1e-3) / 1e9
+    # end to end: the step's activations copied in from one pinned host buffer, the chain
+    # calls on views of the device copy, the block outputs copied back; synchronised each step
+    hx = torch.from_numpy(np.concatenate([np.ascontiguousarray(A).reshape(-1) for A in d["A"]])).pin_memory()
+    hy = torch.empty(sum(Y.numel() for Y in Ys), dtype=torch.float16).pin_memory()
+    dx, dy = torch.empty_like(hx, device=dev), torch.empty_like(hy, device=dev)
+    xv, yv, ox, oy = [], [], 0, 0
+    for X, Y in zip(Xs, Ys):
+        xv.append(dx[ox:ox + X.numel()].view(X.shape))
+        yv.append(dy[oy:oy + Y.numel()].view(Y.shape))
+        ox += X.numel()
+        oy += Y.numel()
+    n_e2e = max(20, min(500, args.steps // 20))
+    with torch.cuda.stream(stream):
+        for i in range(3 + n_e2e):
+            if i == 3:
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+            dx.copy_(hx, non_blocking=True)
+            for j in range(calls):
+                chain(xv[j], Hs[j], yv[j], i % reps)
+            hy.copy_(dy, non_blocking=True)
+            stream.synchronize()
+    e2e_s = (time.perf_counter() - t0) / n_e2e
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded PCG64, recipe in synth/__init__.py)",
+        "config": {"workload": name, "blocks_per_step": calls, "us_per_block": round(1e3 * ms / calls, 3),
+                   "us_per_block_two_calls": round(1e3 * ms_two / calls, 3),
+                   "two_calls": "wq_gemm_w4a16_swiglu then wq_gemm_w4a16 (down), timed the same way",
+                   "l2": f"weights rotate over {reps} copies ({reps * set_bytes / 2**20:.0f} MiB > 3x L2)",
+                   "graph": f"CUDA graphs of {STEPS_PER_GRAPH} consecutive steps, the weight copy rotating step by step",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+                     "frac_two_calls": round(calls * wb / (ms_two * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                     "kernel": "wq::chain_kernel (persistent, cooperative); weight bytes of gate, up and down",
+                     "peak_source": src},
+        "gpu_launches": args.steps * calls,
+        "clocks": clk,
+        "e2e": {"value": round(ws * calls * wb / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": hx.numel() * 2, "d2h_bytes_per_step": hy.numel() * 2},
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        gbs, el, threads, sample = mlp_oracle(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(gbs, 6), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": sample, "seconds": round(el, 2)}
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -1088,6 +1281,8 @@ def main():
         return run_moe(args, ws, rank, local)
     if args.workload == "swiglu":
         return run_swiglu(args, ws, rank, local)
+    if args.workload == "mlp":
+        return run_mlp(args, ws, rank, local)
     shapes = workload_shapes(args.workload)
     if args.shapes:
         shapes = [shapes[int(i)] for i in args.shapes.split(",")]

@@ -202,6 +202,75 @@ int wq_gemm_w4a16_swiglu(const void* X, int x_dtype, const uint32_t* Bpacked, co
                          size_t workspace_bytes, void* stream);
 
 /*
+ * Persistent decode chain: a list of W4A16 GEMMs over the same M <= 8 token
+ * rows, run by ONE cooperative launch, in which a GEMM may take an earlier
+ * GEMM's output as its activations (a decode layer's MLP: the gate/up pair with
+ * SwiGLU, then the down projection).  Each GEMM computes what wq_gemm_w4a16
+ * (pair == 0) or wq_gemm_w4a16_swiglu (pair == 1) computes ("Marlin INT4 on
+ * Ada -- how it works", section "The core mismatch": Y = X @ W_sym +
+ * A_group_sum @ delta, fp32 accumulation, Y rounded once to y_dtype); the
+ * launch-latency floor of small-batch decode (section "Gaps and follow-ups" of
+ * the same page) is paid once per list instead of once per GEMM.  The k-blocks
+ * of every GEMM are shared evenly by all CTAs (stream-K ranges); a tile shared
+ * by several CTAs is summed in a fixed order, so repeated calls give bitwise
+ * identical results.  A GEMM that reads an earlier output starts each part of
+ * its work once the producer tiles it reads are stored; its weights stream in
+ * before that.
+ *   gemms[i].X       [M][K] device activations of x_dtype (F16 or BF16); NULL
+ *                    or gemms[src].Y when src >= 0.
+ *   gemms[i].src     -1, or the index (< i) of the GEMM whose Y is this X: that
+ *                    GEMM's output width N must equal this K and its y_dtype must
+ *                    be x_dtype.
+ *   Bpacked, S, delta  from wq_pack_w4a16 (pair 0) or wq_pack_w4a16_pair
+ *                    (pair 1); delta NULL: symmetric weights.
+ *   Y, y_dtype       [M][N] device output (F16, BF16 or F32).  Outputs must not
+ *                    overlap one another or any input.
+ *   N, K, group_size N the output width (pair: each projection's width, a
+ *                    multiple of 64; otherwise a multiple of 128); K a multiple
+ *                    of 128; group_size 128 or K (-1).
+ *   n                1..8 GEMMs with at most 65536 output tiles of 128 columns
+ *                    in all (pair: 2N columns).  M: 1..8 token rows (0: no-op;
+ *                    larger M goes to the single-GEMM entries,
+ *                    WQ_ERR_UNSUPPORTED_SHAPE here).
+ *   workspace        wq_chain_workspace_size(gemms, n, M, x_dtype) bytes of
+ *                    device memory, 256-byte aligned, ZEROED once before its
+ *                    first use and then passed unchanged to later calls: each
+ *                    call leaves its counters and control words as the next
+ *                    call needs them, and any chain may reuse a workspace large
+ *                    enough for it.  Calls that share a workspace must not run
+ *                    at the same time (different streams).  After a call that
+ *                    reports WQ_ERR_TIMEOUT (status bit 5: a GEMM's wait for its
+ *                    producer's tiles expired), zero the workspace again.
+ * The launch needs every CTA resident at once (two per SM); a device that is
+ * shared with other work still runs it, later.  WQ_ERR_CUDA if the launch is
+ * refused.  The weight-prefetch option (wq_set_option) applies as for the
+ * decode GEMMs.  Measured on a GB300 for a decode MLP block (hidden 4096,
+ * intermediate 11008, 4 tokens) it takes 41 us, against 27 us for
+ * wq_gemm_w4a16_swiglu followed by wq_gemm_w4a16: use it where one launch per
+ * list matters more than the time.
+ */
+typedef struct wq_chain_gemm {
+  const void* X;
+  int src;
+  const uint32_t* Bpacked;
+  const void* S;
+  const float* delta;
+  void* Y;
+  int y_dtype;
+  int N;
+  int K;
+  int group_size;
+  int pair;
+} wq_chain_gemm;
+
+/* Bytes of workspace wq_gemm_w4a16_chain needs on the current device (0 for an
+ * invalid list, M == 0 or an unsupported device). */
+size_t wq_chain_workspace_size(const wq_chain_gemm* gemms, int n, int M, int x_dtype);
+
+int wq_gemm_w4a16_chain(const wq_chain_gemm* gemms, int n, int M, int x_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * Grouped (mixture-of-experts) W4A16 GEMM: the token rows of X are sorted by
  * expert, and expert e multiplies rows expert_offsets[e] .. expert_offsets[e+1]
  * by its own weights (the grouped GEMM of the SGLang W4A8 MoE article, section
@@ -396,7 +465,8 @@ const char* wq_version(void);
 /*
  * Synchronizes `stream`, then reads the device status word of the current
  * device into *status (bit 0..3: a bounded wait in the GEMM expired, bit 4:
- * the wait probe expired) and clears it if `reset` is nonzero.  Returns
+ * the wait probe expired, bit 5: a chain GEMM's wait for its producer expired)
+ * and clears it if `reset` is nonzero.  Returns
  * WQ_ERR_TIMEOUT if any bit was set, else WQ_OK.
  */
 int wq_device_status(unsigned int* status, int reset, void* stream);

@@ -135,3 +135,19 @@ def swiglu_inputs(seed: int = SWIGLU["seed"], tokens=SWIGLU["tokens"], K: int = 
     up = make_inputs(seed + 11, 1, K, N, group_size=group_size, weights_only=True)
     return {"A": A, "gate": gate, "up": up}
 
+
+
+# Decode MLP block of the c1 model dimensions (hidden 4096, intermediate 11008): the
+# gate/up pair on the token rows, then the down projection of its SwiGLU output.
+MLP = dict(tokens=(1, 4), K=4096, F=11008, N=4096, group_size=GROUP, seed=5200)
+
+
+def mlp_inputs(seed: int = MLP["seed"], tokens=MLP["tokens"], K: int = MLP["K"], F: int = MLP["F"],
+               N: int = MLP["N"], group_size: int = MLP["group_size"]):
+    """Activations [m, K] fp16 for each token count, gate and up weights [K, F] and the down
+    weight [F, N] (make_inputs recipe, asymmetric, group 128)."""
+    A = [make_activations(seed + 1 + i, m, K) for i, m in enumerate(tokens)]
+    gate = make_inputs(seed + 10, 1, K, F, group_size=group_size, weights_only=True)
+    up = make_inputs(seed + 11, 1, K, F, group_size=group_size, weights_only=True)
+    down = make_inputs(seed + 12, 1, F, N, group_size=group_size, weights_only=True)
+    return {"A": A, "gate": gate, "up": up, "down": down}

@@ -248,3 +248,51 @@ def test_no_device_means_an_error_not_a_fallback(lib):
     rc = lib.wq_pack_w4a16(fake, fake, fake, fake, fake, fake, 256, 256, 128, None)
     assert rc in (4, 5)  # WQ_ERR_ARCH or WQ_ERR_CUDA, never success
     assert lib.wq_device_supported(0) == 0
+
+
+def _chain(*gemms):
+    arr = (wq.ChainGemm * len(gemms))()
+    for i, g in enumerate(gemms):
+        arr[i] = g
+    return arr
+
+
+def test_chain_entry_checks(lib):
+    """wq_gemm_w4a16_chain rejects bad lists before touching the device: the list size,
+    M beyond 8 rows, the activation type, forward or mismatched producers, shapes, null
+    and misaligned pointers, a workspace that is not 256-byte aligned."""
+    f = lib.wq_gemm_w4a16_chain
+    x, b, s, y = 0x10000, 0x20000, 0x30000, 0x40000
+
+    def g(X=x, src=-1, B=b, S=s, delta=None, Y=y, yd=0, N=256, K=512, gs=128, pair=0):
+        return wq.ChainGemm(X, src, B, S, delta, Y, yd, N, K, gs, pair)
+
+    one = _chain(g())
+    assert f(one, 0, 4, 0, None, 0, None) == 1                                   # empty list
+    assert f(one, 9, 4, 0, None, 0, None) == 1                                   # more than 8 GEMMs
+    assert f(one, 1, 9, 0, None, 0, None) == 2                                   # M > 8
+    assert f(one, 1, 4, 2, None, 0, None) == 1                                   # x dtype
+    assert f(one, 1, 0, 0, None, 0, None) == 0                                   # M == 0: no-op
+    assert f(_chain(g(src=0)), 1, 4, 0, None, 0, None) == 1                      # src not earlier
+    assert f(_chain(g(), g(X=None, src=0, K=384)), 2, 4, 0, None, 0, None) == 2  # K != producer N
+    assert f(_chain(g(yd=2), g(X=None, src=0, K=256)), 2, 4, 0, None, 0, None) == 1  # producer y dtype
+    assert f(_chain(g(), g(X=x, src=0, K=256)), 2, 4, 0, None, 0, None) == 1     # X not the producer's Y
+    assert f(_chain(g(N=96, pair=1)), 1, 4, 0, None, 0, None) == 2              # pair N % 64
+    assert f(_chain(g(pair=2)), 1, 4, 0, None, 0, None) == 1                    # pair flag
+    assert f(_chain(g(K=500)), 1, 4, 0, None, 0, None) == 2                     # K % 128
+    assert f(_chain(g(gs=64)), 1, 4, 0, None, 0, None) == 2                     # group size
+    assert f(_chain(g(B=None)), 1, 4, 0, None, 0, None) == 1                    # null weights
+    assert f(_chain(g(X=x + 2)), 1, 4, 0, None, 0, None) == 1                   # misaligned X
+    assert f(_chain(g(yd=5)), 1, 4, 0, None, 0, None) == 1                      # y dtype
+    assert f(one, 1, 4, 0, ctypes.c_void_p(0x10080), 1 << 20, None) == 1         # workspace alignment
+    ws = lib.wq_chain_workspace_size
+    assert ws(one, 0, 4, 0) == 0 and ws(one, 1, 9, 0) == 0 and ws(one, 1, 0, 0) == 0
+
+
+def test_chain_without_a_device_is_an_error(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    arr = _chain(wq.ChainGemm(0x10000, -1, 0x20000, 0x30000, None, 0x40000, 0, 256, 512, 128, 0))
+    assert lib.wq_gemm_w4a16_chain(arr, 1, 4, 0, ctypes.c_void_p(0x100000), 1 << 20, None) in (4, 5)
+    assert lib.wq_chain_workspace_size(arr, 1, 4, 0) == 0

@@ -28,7 +28,7 @@ __all__ = [
     "EXPORTS", "DTYPE_F16", "DTYPE_BF16", "DTYPE_F32",
     "VARIANT_W4A16", "VARIANT_W4A16_SYM", "VARIANT_W4A8", "VARIANT_W4A8_ASYM", "VARIANT_W4A16_SWIGLU",
     "VARIANT_W4A16_SWIGLU_SYM", "set_weight_prefetch",
-    "OPTION_WEIGHT_PREFETCH",
+    "OPTION_WEIGHT_PREFETCH", "gemm_w4a16_chain", "chain_workspace", "ChainGemm",
 ]
 
 DTYPE_F16, DTYPE_BF16, DTYPE_F32 = 0, 1, 2
@@ -38,6 +38,14 @@ ERRORS = {1: "WQ_ERR_INVALID_ARG", 2: "WQ_ERR_UNSUPPORTED_SHAPE", 3: "WQ_ERR_WOR
           4: "WQ_ERR_ARCH", 5: "WQ_ERR_CUDA", 6: "WQ_ERR_TIMEOUT"}
 
 _P, _I, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+
+
+class ChainGemm(ctypes.Structure):
+    """wq_chain_gemm of include/wq.h: one GEMM of a persistent decode chain."""
+    _fields_ = [("X", _P), ("src", _I), ("Bpacked", _P), ("S", _P), ("delta", _P), ("Y", _P),
+                ("y_dtype", _I), ("N", _I), ("K", _I), ("group_size", _I), ("pair", _I)]
+
+
 # name -> (restype, argtypes); one entry per function declared in include/wq.h
 EXPORTS = {
     "wq_pack_w4a16": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _P]),
@@ -64,6 +72,8 @@ EXPORTS = {
     "wq_get_option": (_I, [_I, ctypes.POINTER(ctypes.c_longlong)]),
     "wq_gemm_w4a16_host": (_I, [_P, _I, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _SZ, _P]),
     "wq_host_workspace_size": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "wq_chain_workspace_size": (_SZ, [ctypes.POINTER(ChainGemm), _I, _I, _I]),
+    "wq_gemm_w4a16_chain": (_I, [ctypes.POINTER(ChainGemm), _I, _I, _I, _P, _SZ, _P]),
 }
 OPTION_WEIGHT_PREFETCH = 1
 
@@ -320,6 +330,62 @@ def gemm_w4a16_swiglu(X, Bpacked, S, delta, group_size: int = 128, out_dtype=Non
                 M, N, K, group_size), (), workspace, variant, M, N, K, group_size, X.device,
                _raw_stream(X.device.index))
     return Y
+
+
+_chain_ws = {}
+
+
+def chain_workspace(device=None, nbytes: int = 0):
+    """The zero-initialised chain workspace of a device's current stream, grown (as a new
+    zeroed buffer) when a chain needs more.  Chain calls keep its control words consistent,
+    so it is never cleared between calls."""
+    torch = _torch()
+    device = torch.device(device if device is not None else "cuda")
+    if device.index is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    key = (device.index, _raw_stream(device.index))
+    buf = _chain_ws.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = _chain_ws[key] = torch.zeros(max(nbytes, 4096), dtype=torch.uint8, device=device)
+    return buf
+
+
+def gemm_w4a16_chain(X, steps, workspace=None):
+    """One persistent launch over a list of decode GEMMs (X [M,K] fp16/bf16, M <= 8).
+
+    steps[i] is a dict: "B", "S", "delta" (None: symmetric) from pack_w4a16, or from
+    pack_w4a16_pair with "pair": True (output silu(gate) * up); optional "group_size" (128),
+    "src" (index of an earlier step whose output is this step's input; default: X, or "x"
+    for another input tensor), "out_dtype" (fp16) or "out".  A step read by a later one must
+    have the activation dtype.  Returns the list of outputs."""
+    torch = _torch()
+    M = X.shape[0]
+    n = len(steps)
+    arr = (ChainGemm * max(n, 1))()
+    outs = []
+    for i, st in enumerate(steps):
+        B, S, dl = st["B"], st["S"], st.get("delta")
+        src = st.get("src")
+        x = None if src is not None else st.get("x", X)
+        K = outs[src].shape[1] if src is not None else x.shape[1]
+        pair = bool(st.get("pair", False))
+        N = B.numel() * 8 // K // (2 if pair else 1)
+        _require_cuda(x, B, S, dl, st.get("out"))
+        Y = st.get("out")
+        if Y is None:
+            Y = torch.empty((M, N), dtype=st.get("out_dtype", torch.float16), device=X.device)
+        outs.append(Y)
+        arr[i] = ChainGemm(x.data_ptr() if x is not None else None, -1 if src is None else src, B.data_ptr(),
+                           S.data_ptr(), dl.data_ptr() if dl is not None else None, Y.data_ptr(),
+                           _dtype_code(Y.dtype), N, K, st.get("group_size", 128), 1 if pair else 0)
+    lib = _lib or load_library()
+    xd = _dtype_code(X.dtype)
+    if workspace is None:
+        need = int(lib.wq_chain_workspace_size(arr, n, M, xd))
+        workspace = chain_workspace(X.device, need)
+    _check(lib.wq_gemm_w4a16_chain(arr, n, M, xd, workspace.data_ptr(), workspace.numel(),
+                                   _raw_stream(X.device.index)), "wq_gemm_w4a16_chain")
+    return outs
 
 
 def gemm_w4a16_host(X, Bpacked, S, delta, group_size: int = 128, out_dtype=None, out=None,

@@ -12,6 +12,7 @@
 
 #include "wq.h"
 #include "wq_internal.h"
+#include "wq_chain.h"
 
 namespace {
 
@@ -1172,3 +1173,109 @@ int wq_debug_wait_probe(unsigned long long limit_ns, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- persistent decode chain
+namespace {
+
+// Checks a chain's arguments (pointers only when check_ptrs) and fills the
+// host-given fields of p; nothing here touches the device.
+int chain_args(const wq_chain_gemm* gemms, int n, int M, int x_dtype, wq::ChainParams* p, bool check_ptrs,
+               const char* name) {
+  if (!gemms || n < 1 || n > wq::kChainMaxGemms)
+    return fail(WQ_ERR_INVALID_ARG, "%s: n=%d (a list of 1..%d GEMMs)", name, n, wq::kChainMaxGemms);
+  if (M < 0 || M > wq::kChainMaxM)
+    return fail(WQ_ERR_UNSUPPORTED_SHAPE, "%s: M=%d (at most %d token rows)", name, M, wq::kChainMaxM);
+  if (x_dtype != WQ_DTYPE_F16 && x_dtype != WQ_DTYPE_BF16)
+    return fail(WQ_ERR_INVALID_ARG, "%s: x_dtype must be F16 or BF16", name);
+  memset(p, 0, sizeof(*p));
+  p->n = n;
+  p->M = M;
+  for (int i = 0; i < n; ++i) {
+    const wq_chain_gemm& s = gemms[i];
+    if (s.pair != 0 && s.pair != 1) return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: pair must be 0 or 1", name, i);
+    if (s.pair && (s.N <= 0 || s.N % 64))
+      return fail(WQ_ERR_UNSUPPORTED_SHAPE, "%s: GEMM %d: N=%d (a multiple of 64 for a pair)", name, i, s.N);
+    const int ncols = s.pair ? 2 * s.N : s.N;
+    int rc = check_kn(s.K, ncols);
+    if (rc) return rc;
+    int gs;
+    if ((rc = norm_group(s.K, s.group_size, &gs))) return rc;
+    const int yk = y_kind_of(s.y_dtype);
+    if (yk < 0) return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: bad y_dtype %d", name, i, s.y_dtype);
+    if (static_cast<long long>(ncols / 128) * (s.K / 128) >= (1ll << 31))
+      return fail(WQ_ERR_UNSUPPORTED_SHAPE, "%s: GEMM %d: too many k-blocks", name, i);
+    if (s.src < -1 || s.src >= i)
+      return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: src=%d (-1 or an earlier GEMM)", name, i, s.src);
+    const void* X = s.X;
+    if (s.src >= 0) {
+      const wq_chain_gemm& q = gemms[s.src];
+      if (q.N != s.K)
+        return fail(WQ_ERR_UNSUPPORTED_SHAPE, "%s: GEMM %d: K=%d differs from the output width %d of GEMM %d", name,
+                    i, s.K, q.N, s.src);
+      if (q.y_dtype != x_dtype)
+        return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d reads GEMM %d's Y, whose y_dtype is not x_dtype", name, i,
+                    s.src);
+      if (s.X && s.X != q.Y)
+        return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: X must be NULL or GEMM %d's Y", name, i, s.src);
+      X = q.Y;
+    }
+    if (check_ptrs) {
+      if (!X || !s.Bpacked || !s.S || !s.Y) return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: null pointer", name, i);
+      if (!aligned16(X) || !aligned16(s.Bpacked) || !aligned16(s.S) || !aligned16(s.Y) ||
+          (s.delta && !aligned16(s.delta)))
+        return fail(WQ_ERR_INVALID_ARG, "%s: GEMM %d: X, Bpacked, S, delta and Y must be 16-byte aligned", name, i);
+    }
+    wq::ChainGemm& G = p->g[i];
+    G.X = X;
+    G.B = s.Bpacked;
+    G.S = static_cast<const __half*>(s.S);
+    G.delta = s.delta;
+    G.Y = s.Y;
+    G.y_kind = yk;
+    G.N = ncols;
+    G.K = s.K;
+    G.per_channel = gs == s.K ? 1 : 0;
+    G.pair = s.pair;
+    G.src = s.src;
+  }
+  return WQ_OK;
+}
+
+int x_kind_of(int x_dtype) { return x_dtype == WQ_DTYPE_BF16 ? wq::kXBF16 : wq::kXF16; }
+
+}  // namespace
+
+size_t wq_chain_workspace_size(const wq_chain_gemm* gemms, int n, int M, int x_dtype) {
+  wq::ChainParams p;
+  if (chain_args(gemms, n, M, x_dtype, &p, false, "wq_chain_workspace_size") || M == 0) return 0;
+  if (check_device()) return 0;
+  wq::ChainGeom geo;
+  if (wq::chain_geometry(x_kind_of(x_dtype), M, &geo) != cudaSuccess) return 0;
+  return wq::chain_plan(p, geo);
+}
+
+int wq_gemm_w4a16_chain(const wq_chain_gemm* gemms, int n, int M, int x_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  static const char* name = "wq_gemm_w4a16_chain";
+  wq::ChainParams p;
+  int rc = chain_args(gemms, n, M, x_dtype, &p, true, name);
+  if (rc) return rc;
+  if (M == 0) return WQ_OK;
+  if (workspace && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return fail(WQ_ERR_INVALID_ARG, "%s: workspace must be 256-byte aligned", name);
+  if ((rc = check_device())) return rc;
+  wq::ChainGeom geo;
+  cudaError_t e = wq::chain_geometry(x_kind_of(x_dtype), M, &geo);
+  if (e != cudaSuccess) return cuda_fail(e, name);
+  const size_t need = wq::chain_plan(p, geo);
+  if (need == 0)
+    return fail(WQ_ERR_UNSUPPORTED_SHAPE, "%s: more than %d output tiles of 128 columns in one chain", name,
+                wq::kChainMaxTiles);
+  if (!workspace || workspace_bytes < need)
+    return fail(WQ_ERR_WORKSPACE, "%s: workspace of %zu bytes given, %zu needed", name, workspace_bytes, need);
+  wq::chain_bind_workspace(p, workspace);
+  p.timeout_ns = timeout_ns();
+  p.weight_prefetch = g_weight_prefetch.load(std::memory_order_relaxed);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return after_launch(wq::launch_chain(x_kind_of(x_dtype), p, geo, st), name, st);
+}
