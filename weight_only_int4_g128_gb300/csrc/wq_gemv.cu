@@ -51,7 +51,7 @@
 // (fragment k 2t+8, 2t+9); the activation fragment takes x at the same physical
 // k: 32t + 16h + 2p (+ 8).  One chunk of codes per row and one 64-byte run of
 // the activation row per lane cover a whole k-block with no shuffles.
-#include "wq_device.cuh"
+#include "wq_warp.cuh"
 
 namespace wq {
 
@@ -116,81 +116,10 @@ __host__ __device__ inline Layout layout(int M, int kbps, int splits, int gseg, 
 }
 }  // namespace gv
 
-// 16-byte asynchronous copy global -> shared (L1 bypassed), with an L2 policy.
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint64_t policy) {
-  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "l"(policy)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-// Wait until at most N of this thread's most recent copy groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr)
-               : "memory");
-  return v;
-}
+// The per-lane copies, offset-code operands, MMA, block sums and activation
+// swizzle of this path are in wq_warp.cuh.
+using namespace warp;
 
-// D = A * B + C, m16n8k16, fp32 accumulate; A 16 x 16 (row), B 16 x 8 (col).
-template <int XK>
-__device__ __forceinline__ void mma16816(float (&d)[4], const float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-  if (XK == kXBF16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%10, %11, %12, %13};"
-        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-  }
-}
-
-
-// Sums of one 16-byte chunk (k = 8c .. 8c+7) of an activation row, split by
-// the position of k in its code word: k % 8 in {0, 1, 4, 5} (the low nibble of
-// each code byte) into lo, {2, 3, 6, 7} (the high nibble) into hi.
-template <int XK>
-__device__ __forceinline__ void sum_chunk(const uint4& v, float& lo, float& hi) {
-  const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-  float s[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (XK == kXF16) {
-      s[i] = __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] & 0xFFFFu))) +
-             __half2float(__ushort_as_half(static_cast<uint16_t>(u[i] >> 16)));
-    } else {
-      s[i] = __uint_as_float(u[i] << 16) + __uint_as_float(u[i] & 0xFFFF0000u);
-    }
-  }
-  lo = s[0] + s[2];
-  hi = s[1] + s[3];
-}
-
-// Code pairs as MMA operands with an offset instead of (v - 8), one LOP3 each:
-// fp16 gives 1024 + v (nibble at bits 0..3 of each half) or 1024 + 16 v (bits
-// 4..7); bf16 gives 128 + v (its 7-bit mantissa cannot hold a nibble at bits
-// 4..7, so those pairs are shifted first).  All are exact.
-__device__ __forceinline__ uint32_t off_lo_f16(uint32_t w) { return lop_and_or(w, 0x000F000Fu, 0x64006400u); }
-__device__ __forceinline__ uint32_t off_hi_f16(uint32_t w) { return lop_and_or(w, 0x00F000F0u, 0x64006400u); }
-__device__ __forceinline__ uint32_t off_bf16(uint32_t w) { return lop_and_or(w, 0x000F000Fu, 0x43004300u); }
-
-// Swizzle of the activation tile: logical 16-byte chunk c of token row m is
-// stored at chunk c ^ (bit 3 of c | (m & 1) << 1).  The eight lanes of a
-// quarter warp (two token rows x four lanes t, chunks 4t + q) then hit eight
-// distinct bank groups.
-__device__ __forceinline__ int xswz(int c, int m) { return c ^ (((c >> 3) & 1) | ((m & 1) << 1)); }
-
-// MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
-// wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
-// per column tile and expert) then fit in one wave.
 // Eight int8 activations (one 8-byte load) as the 16-byte chunk of their fp16
 // values, element e in half e of the chunk (|x| <= 128: exact).
 __device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
@@ -206,6 +135,9 @@ __device__ __forceinline__ uint4 i8x8_to_f16x8(uint2 w) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// MINB: CTAs per SM the registers are budgeted for -- 2 for a plain GEMM (one
+// wave of two CTAs per SM), 3 for a grouped launch, whose many short CTAs (one
+// per column tile and expert) then fit in one wave.
 template <int XK, int D, int MINB, bool PAIR, bool XS>
 __global__ void __launch_bounds__(gv::kThreads, MINB) gemv_kernel(const GemmParams p, unsigned* status) {
   using namespace gv;

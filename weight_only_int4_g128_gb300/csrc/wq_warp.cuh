@@ -1,7 +1,8 @@
 // wq_warp.cuh -- helpers of the warp-level MMA decode path (M <= 8 tokens as
 // the N = 8 side of mma.sync.m16n8k16): per-lane asynchronous copies, the
 // offset-code MMA operands and the activation block sums.  Used by the
-// persistent chain kernel (wq_chain.cu).
+// weight-streaming decode kernel (wq_gemv.cu) and the persistent chain kernel
+// (wq_chain.cu).
 //
 // Offset codes (section "The core mismatch": W_sym = (q - 8) * scale).  One
 // LOP3 turns a word of code pairs into MMA operands that carry an exact
