@@ -252,3 +252,19 @@ def test_one_workspace_serves_different_chains(wq):
         for a, b in zip(two, ref_mlp):
             assert torch.equal(a, b)
     assert wq.device_status(reset=True) == 0
+
+
+def test_chain_limits_on_the_device(wq):
+    """With a device present: a chain of more than 65536 output tiles and a workspace
+    smaller than the query are refused before anything is launched (the placeholder
+    pointers below are never dereferenced)."""
+    import ctypes
+    lib = wq.load_library()
+    arr = (wq.ChainGemm * 1)()
+    arr[0] = wq.ChainGemm(0x10000, -1, 0x20000, 0x30000, None, 0x40000, 0, 128 * 65537, 128, 128, 0)
+    assert lib.wq_chain_workspace_size(arr, 1, 4, 0) == 0
+    assert lib.wq_gemm_w4a16_chain(arr, 1, 4, 0, ctypes.c_void_p(0x100000), 1 << 30, None) == 2
+    arr[0] = wq.ChainGemm(0x10000, -1, 0x20000, 0x30000, None, 0x40000, 0, 256, 512, 128, 0)
+    need = lib.wq_chain_workspace_size(arr, 1, 4, 0)
+    assert need > 0
+    assert lib.wq_gemm_w4a16_chain(arr, 1, 4, 0, ctypes.c_void_p(0x100000), need - 256, None) == 3
