@@ -85,8 +85,7 @@ constexpr int kThreads = kComputeThreads + 32;  // + the fixup warp
 constexpr int kMT = 8;                     // token slots = MMA N
 constexpr int kD = 6;                      // ring depth: k-blocks in flight per warp
 constexpr int kPre = 3;                    // of them requested before the first activation window
-constexpr int kLaneOff = 1024;             // in a ring slot: each lane's own scales and deltas (16 B)
-constexpr int kSlot = 1536;                // codes (2 row halves x 32 lanes x 16 B) + 32 x 16 B
+constexpr int kSlot = 1024;                // codes of one k-block of one warp: 2 row halves x 32 lanes x 16 B
 constexpr int kRing = kComputeWarps * kD * kSlot;
 constexpr int kMaxSmem = 113 * 1024;       // two CTAs per SM
 constexpr int kMaxWindow = 128;            // k-blocks of a window (the done-word polls use 2 per k-block)
@@ -96,8 +95,11 @@ constexpr int kUint4PerBlock = kTileN * kWordsPerKBlock / 4;  // 16-byte chunks 
 __host__ __device__ inline int align128(int x) { return (x + 127) & ~127; }
 __host__ __device__ inline int xs_bytes(int M, int lmax) { return align128((M * lmax + 1) * kKBlock * 2); }
 __host__ __device__ inline int asum_bytes(int lmax) { return align128(lmax * 2 * kMT * 4); }
+// scale rows [lmax][128] fp16 and delta rows [lmax][128] fp32 of the window's k-blocks
+__host__ __device__ inline int ssc_bytes(int lmax) { return align128(lmax * kTileN * 2); }
+__host__ __device__ inline int sdl_bytes(int lmax) { return align128(lmax * kTileN * 4); }
 __host__ __device__ inline int smem_bytes(int M, int lmax) {
-  return 128 + kRing + xs_bytes(M, lmax) + asum_bytes(lmax) + 128;
+  return 128 + kRing + xs_bytes(M, lmax) + asum_bytes(lmax) + ssc_bytes(lmax) + sdl_bytes(lmax) + 128;
 }
 }  // namespace chn
 
@@ -163,16 +165,20 @@ __device__ __forceinline__ bool cursor_next(const ChainParams& p, int c, Cursor&
   return false;
 }
 
-// Stages the activation rows of k-blocks k0, k0 + 1, ... (lx of them, cyclic in
-// K) into the window and forms their block sums: asum[s][0][m] = sum x,
-// asum[s][1][m] = the offset term of the codes (see wq_warp.cuh).
+// Stages a window: the activation rows of k-blocks k0, k0 + 1, ... (lx of them,
+// cyclic in K) with their block sums (asum[s][0][m] = sum x, asum[s][1][m] = the
+// offset term of the codes, see wq_warp.cuh), and the scale and delta rows of the
+// window's L positions (tile t0, k-block k0 onwards, wrapping to the next tile):
+// ssc[j][128] fp16, sdl[j][128] fp32.  All loads of a batch are in flight together.
 template <int XK>
-__device__ __noinline__ void chain_stage(const ChainGemm& G, int M, int k0, int lx, uint8_t* xs, int xstride,
-                                            float* asum) {
+__device__ __forceinline__ void chain_stage(const ChainGemm& G, int M, int t0, int k0, int lx, int L, uint8_t* xs,
+                                         int xstride, float* asum, __half* ssc, float* sdl) {
   using namespace chn;
   const uint8_t* const X = static_cast<const uint8_t*>(G.X);
   const int per_tok = lx * 16;  // 16-byte chunks per token row of the window
-  const int total = M * per_tok;
+  const int xtotal = M * per_tok;  // a multiple of 16: a 16-lane group is all X or all scale rows
+  const int per_pos = G.delta != nullptr ? 48 : 16;  // 16-byte chunks of one position's scale + delta rows
+  const int total = xtotal + L * per_pos;
   constexpr int kU = 8;
   for (int b = 0; b < total; b += kComputeThreads * kU) {
     uint4 v[kU];
@@ -180,12 +186,20 @@ __device__ __noinline__ void chain_stage(const ChainGemm& G, int M, int k0, int 
     for (int u = 0; u < kU; ++u) {
       const int idx = b + u * kComputeThreads + threadIdx.x;
       v[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (idx < total) {
+      if (idx < xtotal) {
         const int m = idx / per_tok;
         const int rem = idx - m * per_tok;
         int kk = k0 + (rem >> 4);
         if (kk >= G.kb) kk -= G.kb;
         v[u] = warp::ldg_cg128(X + (static_cast<size_t>(m) * G.K + kk * kKBlock) * 2 + (rem & 15) * 16);
+      } else if (idx < total) {
+        const int j = (idx - xtotal) / per_pos;
+        const int ch = (idx - xtotal) - j * per_pos;
+        const int q = k0 + j;
+        const int tile = t0 + q / G.kb;
+        const int kk = q - (q / G.kb) * G.kb;
+        const size_t row = static_cast<size_t>(G.per_channel ? 0 : kk) * G.N + static_cast<size_t>(tile) * kTileN;
+        v[u] = ch < 16 ? warp::ldg_cg128(G.S + row + 8 * ch) : warp::ldg_cg128(G.delta + row + 4 * (ch - 16));
       }
     }
 #pragma unroll
@@ -195,11 +209,16 @@ __device__ __noinline__ void chain_stage(const ChainGemm& G, int M, int k0, int 
       const int idx = idx0 + threadIdx.x;
       float lo = 0.0f, hi = 0.0f;
       int m = 0, rem = 0;
-      if (idx < total) {
+      if (idx < xtotal) {
         m = idx / per_tok;
         rem = idx - m * per_tok;
         *reinterpret_cast<uint4*>(xs + m * xstride + 16 * warp::xswz(rem, m)) = v[u];
         warp::sum_chunk<XK>(v[u], lo, hi);
+      } else if (idx < total) {
+        const int j = (idx - xtotal) / per_pos;
+        const int ch = (idx - xtotal) - j * per_pos;
+        if (ch < 16) *reinterpret_cast<uint4*>(ssc + j * kTileN + 8 * ch) = v[u];
+        else *reinterpret_cast<uint4*>(sdl + j * kTileN + 4 * (ch - 16)) = v[u];
       }
       // the 16 chunks of one (token, k-block) are 16 consecutive lanes
 #pragma unroll
@@ -207,7 +226,7 @@ __device__ __noinline__ void chain_stage(const ChainGemm& G, int M, int k0, int 
         lo += __shfl_xor_sync(0xffffffffu, lo, sh);
         hi += __shfl_xor_sync(0xffffffffu, hi, sh);
       }
-      if (idx < total && (rem & 15) == 0) {
+      if (idx < xtotal && (rem & 15) == 0) {
         const int s = rem >> 4;
         asum[s * 2 * kMT + m] = lo + hi;
         asum[s * 2 * kMT + kMT + m] = (XK == kXF16) ? fmaf(1032.0f, lo, 72.0f * hi) : 136.0f * (lo + hi);
@@ -368,7 +387,9 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
   const int xstride = lmax * kKBlock * 2;  // bytes per token row of the window
   uint8_t* const xs = sm + kRing;
   float* const asum = reinterpret_cast<float*>(sm + kRing + xs_bytes(M, lmax));
-  const int misc_off = kRing + xs_bytes(M, lmax) + asum_bytes(lmax);
+  __half* const ssc = reinterpret_cast<__half*>(sm + kRing + xs_bytes(M, lmax) + asum_bytes(lmax));
+  float* const sdl = reinterpret_cast<float*>(sm + kRing + xs_bytes(M, lmax) + asum_bytes(lmax) + ssc_bytes(lmax));
+  const int misc_off = kRing + xs_bytes(M, lmax) + asum_bytes(lmax) + ssc_bytes(lmax) + sdl_bytes(lmax);
   // The last 128 bytes: the compute -> fixup hand-off barriers full[2] and empty[2]
   // (slot b of flush i is i % 2), the CTA's abort flag, and misc words: misc[1] the
   // last-sharer flag of the compute warps' own reduction, misc[2] the last GEMM in
@@ -424,16 +445,6 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
       const uint4* src = reinterpret_cast<const uint4*>(G.B) + static_cast<size_t>(iu.f) * kUint4PerBlock;
       cp_async16(dst + lane * 16, src + offA, pol);
       cp_async16(dst + 512 + lane * 16, src + offB, pol);
-      // this lane's own scales (the aligned 4 bytes holding row rA's, row rB's) and
-      // deltas, so no lane reads another's copies
-      const size_t col = static_cast<size_t>(G.per_channel ? 0 : iu.k) * G.N + iu.tile * kTileN + rA;
-      const uint32_t own = dst + kLaneOff + lane * 16;
-      cp_async4(own, G.S + (col & ~static_cast<size_t>(1)), pol);
-      cp_async4(own + 4, G.S + ((col + 8) & ~static_cast<size_t>(1)), pol);
-      if (G.delta != nullptr) {
-        cp_async4(own + 8, G.delta + col, pol);
-        cp_async4(own + 12, G.delta + col + 8, pol);
-      }
       cursor_next(p, c, iu);
     }
     cp_async_commit();  // one group per slot, empty past the list
@@ -603,13 +614,17 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
 
     // ---- the compute warps: the CTA's k-blocks, GEMM after GEMM
     Cursor cu = cursor_seek(p, c, 0);
-    int slot = 0, prem = 0, xslot = 0, lx = 1, nfl = 0;
+    int slot = 0, prem = 0, xslot = 0, lx = 1, nfl = 0, wpos = 0;
     bool primed = false;
     float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const int sw = (t >> 1) | ((g & 1) << 1);  // xswz for this lane's chunks 4t + q: flips the low bits of q
     // token slot g: its row of the window, or the zero k-block (not advanced) past M
-    const uint8_t* const xrow = xs + (g < M ? g * xstride : M * xstride) + 64 * t;
+    // (shared-space addresses: 32-bit, which keeps the loop within its registers)
+    const uint32_t xrow = smem_u32(xs) + static_cast<uint32_t>((g < M ? g * xstride : M * xstride) + 64 * t);
+    const uint32_t asum_s = smem_u32(asum) + 8u * t;        // + 64 xslot: (sum, offset) of tokens 2t, 2t+1
+    const uint32_t ssc_s = smem_u32(ssc) + 2u * rA;          // + 256 wpos: the scale of row rA (rB: + 16)
+    const uint32_t sdl_s = smem_u32(sdl) + 4u * rA;          // + 512 wpos: the delta of row rA (rB: + 32)
     const int xstep = g < M ? kKBlock * 2 : 0;
     while (cu.l < p.n) {
       const ChainGemm& G = p.g[cu.l];
@@ -618,7 +633,7 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
         lx = min(L, G.kb);
         if (G.src >= 0) wait_window(G, cu.k, lx);
         compute_sync();  // every warp is done with the previous window
-        chain_stage<XK>(G, M, cu.k, lx, xs, xstride, asum);
+        chain_stage<XK>(G, M, cu.tile, cu.k, lx, L, xs, xstride, asum, ssc, sdl);
         compute_sync();
         if (!primed) {
 #pragma unroll 1
@@ -627,6 +642,7 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
         }
         prem = L;
         xslot = 0;
+        wpos = 0;
       }
       // The k-blocks up to the end of the window or of the tile, whichever is first.
       const int run = min(prem, min(G.kb - cu.k, cu.end - cu.f));
@@ -637,24 +653,23 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
         const uint32_t sl = ring_w + static_cast<uint32_t>(slot * kSlot);
         const uint4 a = lds128(sl + lane * 16);
         const uint4 cc = lds128(sl + 512 + lane * 16);
-        const uint4 sd = lds128(sl + kLaneOff + lane * 16);
         // The slot has been read into registers: refill it with the k-block kD further on.
-        asm volatile("" ::"r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(cc.x), "r"(cc.y), "r"(cc.z), "r"(cc.w),
-                     "r"(sd.x), "r"(sd.y), "r"(sd.z), "r"(sd.w)
+        asm volatile("" ::"r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(cc.x), "r"(cc.y), "r"(cc.z), "r"(cc.w)
                      : "memory");
         issue(slot);
-        const int hs = (g & 1) ? 16 : 0;  // the half of the aligned pair that is this lane's row
-        const float sA = __half2float(__ushort_as_half(static_cast<uint16_t>(sd.x >> hs)));
-        const float sB = __half2float(__ushort_as_half(static_cast<uint16_t>(sd.y >> hs)));
-        const float dA = has_delta ? __uint_as_float(sd.z) : 0.0f;
-        const float dB = has_delta ? __uint_as_float(sd.w) : 0.0f;
         slot = (slot + 1 == kD) ? 0 : slot + 1;
+        // the scale and delta rows of this position of the window
+        const float sA = __half2float(__ushort_as_half(lds_u16(ssc_s + 256u * wpos)));
+        const float sB = __half2float(__ushort_as_half(lds_u16(ssc_s + 256u * wpos + 16u)));
+        const float dA = has_delta ? lds_f32(sdl_s + 512u * wpos) : 0.0f;
+        const float dB = has_delta ? lds_f32(sdl_s + 512u * wpos + 32u) : 0.0f;
+        ++wpos;
 
         uint32_t xr[16];
-        const uint8_t* const row = xrow + xslot * xstep;
+        const uint32_t row = xrow + static_cast<uint32_t>(xslot * xstep);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 v = *reinterpret_cast<const uint4*>(row + 16 * (q ^ sw));
+          const uint4 v = lds128(row + 16u * (q ^ sw));
           xr[4 * q] = v.x;
           xr[4 * q + 1] = v.y;
           xr[4 * q + 2] = v.z;
@@ -684,7 +699,7 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
           if (first) mma16816<XK>(acc[ch], zero4, f[0], f[1], f[2], f[3], xr[8 * h + pp], xr[8 * h + 4 + pp]);
           else mma16816<XK>(acc[ch], acc[ch], f[0], f[1], f[2], f[3], xr[8 * h + pp], xr[8 * h + 4 + pp]);
         }
-        const float2 ofs = *reinterpret_cast<const float2*>(asum + xslot * 2 * kMT + kMT + 2 * t);
+        const float2 ofs = lds_f2(asum_s + 64u * xslot + 32u);
         float d[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -692,7 +707,7 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
           d[e] = (XK == kXBF16 ? acc[0][e] + acc[1][e] : fmaf(acc[1][e], 0.0625f, acc[0][e])) - o;
         }
         if (has_delta) {
-          const float2 as = *reinterpret_cast<const float2*>(asum + xslot * 2 * kMT + 2 * t);
+          const float2 as = lds_f2(asum_s + 64u * xslot);
           tot[0] = fmaf(dA, as.x, fmaf(sA, d[0], tot[0]));
           tot[1] = fmaf(dA, as.y, fmaf(sA, d[1], tot[1]));
           tot[2] = fmaf(dB, as.x, fmaf(sB, d[2], tot[2]));

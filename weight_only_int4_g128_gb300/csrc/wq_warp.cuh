@@ -44,6 +44,21 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint16_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 lds_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
 // 16-byte global load cached in L2 only: data written during the same launch
 // by other CTAs (after they released it) is never served from a stale L1 line.
 __device__ __forceinline__ uint4 ldg_cg128(const void* p) {
