@@ -540,17 +540,17 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
       compute_sync();
       if (misc[1] == 0u) return false;
       __threadfence();
-      // the sum in slot order from 0.0f (as the fixup warp forms it), 2 slots per batch
+      // the sum in slot order from 0.0f (as the fixup warp forms it), 8 slots per batch
       float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      for (int j0 = 0; j0 < nc; j0 += 2) {
-        float v[2][4];
+      for (int j0 = 0; j0 < nc; j0 += 8) {
+        float v[8][4];
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 8; ++b) {
           const int jj = j0 + b;
           if (jj < nc && jj != j) get_partial(part + jj * kPartFloats, v[b], M, rA, rB, t);
         }
 #pragma unroll
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 8; ++b) {
           const int jj = j0 + b;
           if (jj < nc)
 #pragma unroll
@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
 
     // ---- the compute warps: the CTA's k-blocks, GEMM after GEMM
     Cursor cu = cursor_seek(p, c, 0);
-    int slot = 0, prem = 0, xslot = 0, lx = 1, nfl = 0, wpos = 0;
+    int slot = 0, prem = 0, xslot = 0, lx = 1, nfl = 0, wpos = 0, final_tile = -1;
     bool primed = false;
     float tot[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -725,7 +725,8 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
       cu.k += run;
       if (cu.k == G.kb || cu.f == cu.end) {  // the CTA's part of this tile is done
         if (cu.f == cu.end && cu.l == static_cast<int>(misc[2])) {
-          if (reduce_final(G, cu.tile, tot)) store_final(G, cu.tile, tot);
+          final_tile = cu.tile;  // reduced after the loop, where few registers are live
+          break;
         } else {
           // hand the partial to the fixup warp: its slot in the workspace, then the barrier
           const int bi = nfl & 1;
@@ -753,6 +754,10 @@ __global__ void __launch_bounds__(chn::kThreads, 2)
       }
     }
     cp_async_wait<0>();  // nothing of this thread is in flight (the trailing groups are empty)
+    if (final_tile >= 0) {
+      const ChainGemm& G = p.g[misc[2]];
+      if (reduce_final(G, final_tile, tot)) store_final(G, final_tile, tot);
+    }
   }
 
   // The last CTA to finish advances the generation for the next call.
