@@ -38,14 +38,15 @@
 // compute warps never drains at a tile boundary.  The CTA's final tile, when
 // nothing is in flight any more, is reduced by the compute warps themselves.
 //
-// Weights: each lane streams its two 16-byte code chunks per k-block, plus its
-// own two scales and two deltas (4-byte copies), into a per-warp ring kD k-blocks
-// deep, in the CTA's own order across GEMM boundaries, so the next GEMM's first
-// k-blocks arrive while the current one finishes.  Activations: each range is
-// processed in windows of up to lmax k-blocks; a window's activation rows (a
-// cyclic run of K: consecutive positions of a range are consecutive k, wrapping
-// to the next tile) are staged once in shared memory with their block sums.
-//
+// Weights: each lane streams its two 16-byte code chunks per k-block into a
+// per-warp ring kD k-blocks deep, in the CTA's own order across GEMM boundaries,
+// so the next GEMM's first k-blocks arrive while the current one finishes.  The
+// range is processed in windows of up to lmax k-blocks; a window's activation
+// rows (a cyclic run of K: consecutive positions of a range are consecutive k,
+// wrapping to the next tile) are staged once in shared memory with their block
+// sums, together with the scale and delta rows of its positions (small per-lane
+// copies of those per k-block cost a quarter of the streaming rate, measured).
+
 // Dependencies.  The warp that stores a tile of a GEMM that a later GEMM reads
 // publishes it: the stores are fenced, then one thread writes the call's
 // generation number into the tile's done word with release semantics.  Before
@@ -67,12 +68,12 @@
 // chains.
 //
 // Measured on the decode MLP of hidden size 4096 (pair 2 x 11008 with SwiGLU,
-// then down 11008 -> 4096, 4 tokens): 41 us per block against 27 us for the
-// fused-SwiGLU call followed by the down call.  The k-block loop streams at about
-// 20 GB/s per SM (the single-GEMM weight-streaming kernel reaches up to ~43), and
-// the start (~5 us to the first window) and the producer-to-consumer boundary
-// (~8 us: the last tiles' sums through L2, the done words, the consumer's window)
-// come on top.
+// then down 11008 -> 4096, 4 tokens): 34.6 us per block against 27.1 us for the
+// fused-SwiGLU call followed by the down call.  The k-block loop runs at about the
+// single-GEMM kernel's rate; the start (the first window's activations and scale
+// rows, ~6 us) and the producer-to-consumer boundary (~8 us: the last tiles' sums
+// through L2, the done words, the consumer's window) are what the separate calls
+// do not pay.
 #include "wq_chain.h"
 #include "wq_warp.cuh"
 
